@@ -1,0 +1,392 @@
+"""Throughput of the fused vocabulary cross-entropy forward+backward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+One step = one fused forward+backward pass (ce_fwd_bwd through the C ABI:
+ignore-mask count, the main kernel, the fixed-order mean) over the whole
+(4, 4096, 128000) bf16 logits batch, label smoothing 0.1, reduce_loss, 10% of
+the targets ignored, gradient written in place.  The logits (4.2 GB) are far
+larger than the 129 MB L2, so no flush is needed between steps; the in-place
+gradient of step k is the input of step k+1 (same bytes, same work).
+
+Prints one JSON line (rank 0).  N > 1 (torchrun, one process per GPU) runs N
+independent replicas of the workload (weak scaling, no collective on the data
+path); the timed region is bracketed by a barrier and a device synchronize on
+every rank and the slowest rank's time is used.
+
+--impl reference times the CPU oracle (oracle/, double precision, OpenMP)
+on the host cores, one bounded row block of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "CE fwd+bwd tokens/s at V=128000 bf16; achieved HBM GB/s vs GB300 peak"
+DEFAULT_WORKLOAD = "c5t_bsv128000_bf16"
+KERNELS_PER_STEP = {1: 3, 2: 3, 3: 4}   # count + main (+ second stage) + mean
+CLOCK_FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+                "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+                "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+
+# ----------------------------------------------------------------- byte counts
+def logits_bytes(N: int, V: int, elem_bytes: int) -> int:
+    return N * V * elem_bytes
+
+
+def pass_bytes(N: int, V: int, elem_bytes: int) -> int:
+    """Algorithmic bytes of one fused pass: read the logits once, write the
+    gradient once over them, read the int64 targets."""
+    return 2 * logits_bytes(N, V, elem_bytes) + 8 * N
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def aggregate(local_ms: float, local_tokens: int, world: int, all_reduce_max=None):
+    """Whole-job throughput: the units all ranks processed over the slowest
+    rank's time.  all_reduce_max(x) returns the max of x over ranks."""
+    ms = all_reduce_max(local_ms) if all_reduce_max else local_ms
+    return ms, local_tokens * world / (ms / 1e3)
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of the SM clock and throttle reasons, stamped with
+    host time so the samples inside the timed region can be picked out."""
+
+    def __init__(self, gpu_id: str, period_ms: int = 50):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={','.join(CLOCK_FIELDS)}",
+                 "--format=csv,noheader,nounits", "-lms", str(period_ms), "-i", gpu_id],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) == len(CLOCK_FIELDS):
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        window = len(inside)
+        if not inside and self.samples:
+            # region shorter than the sampling period: nearest samples around it
+            near = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:3]
+            inside = [p for (_, p) in near]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = sorted(v for v in (num(p[0]) for p in inside) if v is not None)
+        smax = max((v for v in (num(p[1]) for p in inside) if v is not None), default=None)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for p in inside for k in range(4) if p[4 + k] == "Active"})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": smax,
+                "reasons": reasons, "samples": len(inside), "window_samples": window,
+                "power_w_max": max((v for v in (num(p[2]) for p in inside) if v is not None),
+                                   default=None)}
+
+
+# ----------------------------------------------------------------- CPU oracle timing
+_ORACLE_CODE = {"f32": 0, "bf16": 1, "f16": 2}
+
+
+def _storage(x):
+    """Raw storage of a CPU tensor as numpy (float32, or uint16 bit patterns)."""
+    import numpy as np
+    import torch
+    x = x.contiguous()
+    if x.dtype == torch.float32:
+        return x.numpy().ravel()
+    return x.view(torch.int16).numpy().view(np.uint16).ravel()
+
+
+def oracle_rows_per_s(w, x_host, t_host, budget_s: float, block: int = 256, max_rows=None):
+    """Time the CPU oracle (fwd+bwd, double) on consecutive row blocks of the
+    workload until `budget_s` seconds have passed.  Returns (rows/s, rows,
+    seconds, threads)."""
+    import numpy as np
+
+    import oracle
+    lib = oracle.load()
+    rows_done, t_used = 0, 0.0
+    r0 = 0
+    x2 = x_host.view(w.N, w.V)
+    t1d = t_host.reshape(-1)
+    limit = w.N if max_rows is None else min(w.N, max_rows)
+    while t_used < budget_s and rows_done < limit:
+        r1 = min(limit, r0 + block)
+        xs = _storage(x2[r0:r1])
+        ts = t1d[r0:r1].numpy()
+        t = time.perf_counter()
+        oracle.ce(xs, _ORACLE_CODE[w.dtype], 1, r1 - r0, w.V, targets=ts,
+                  label_smoothing=w.label_smoothing, reduce_loss=True,
+                  dloss=np.array([1.0]), lib=lib)
+        t_used += time.perf_counter() - t
+        rows_done += r1 - r0
+        r0 = r1 % limit
+    return rows_done / t_used, rows_done, t_used, oracle.num_threads(lib)
+
+
+# ----------------------------------------------------------------- arms
+def run_reference(args, w, rank: int, world: int) -> None:
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    from vocabulary_cross_entropy_pass_gb300 import workloads as wl
+    lib = oracle.load()
+    R = args.ref_rows
+    nblk = (w.N + R - 1) // R
+    t_all = wl.targets(w).view(-1)
+
+    def step(i):
+        r0 = (i % nblk) * R
+        r1 = min(w.N, r0 + R)
+        xs = _storage(wl.logits_rows(w, r0, r1))
+        ts = t_all[r0:r1].numpy()
+        t = time.perf_counter()
+        oracle.ce(xs, _ORACLE_CODE[w.dtype], 1, r1 - r0, w.V, targets=ts,
+                  label_smoothing=w.label_smoothing, reduce_loss=True, dloss=np.array([1.0]),
+                  lib=lib)
+        return time.perf_counter() - t, r1 - r0
+
+    for i in range(args.warmup):
+        step(i)
+    tot_t, tot_rows = 0.0, 0
+    for i in range(args.steps):
+        dt, rows = step(args.warmup + i)
+        tot_t += dt
+        tot_rows += rows
+    value = tot_rows / tot_t
+    cores = oracle.num_threads(lib)
+    sample = f"{R} rows of the workload per step (row blocks in turn), fwd+bwd in double"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tot_t / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w, args),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w, args) -> dict:
+    return {"workload": f"{w.name}: logits ({w.dim0},{w.dim1},{w.V}) {w.dtype} "
+                        f"({'B,SQ,V' if w.layout == 'bsv' else 'SQ,B,V'}), N={w.N} rows, "
+                        f"sigma={w.sigma}, {int(w.ignore_frac * 100)}% ignored, "
+                        f"label_smoothing={w.label_smoothing}, reduce_loss={w.reduce_loss}, "
+                        "gradient in place",
+            "tokens_per_step": w.N, "vocab": w.V, "logits_dtype": w.dtype,
+            "accumulate": "f32", "l2": "inputs 4.2 GB >> 129 MB L2 (no flush needed)"
+            if w.logits_bytes > 1 << 30 else "inputs smaller than L2",
+            "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
+
+
+def run_ours(args, w, rank: int, world: int, dist) -> None:
+    import torch
+
+    import vocabulary_cross_entropy_pass_gb300 as pkg
+    from vocabulary_cross_entropy_pass_gb300 import workloads as wl
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    # inputs: pinned host copy (also the e2e source) and a resident device copy
+    x_host = wl.logits(w, pin_memory=True)
+    t_host = wl.targets(w).pin_memory()
+    x = x_host.to(dev, non_blocking=True)
+    t = t_host.to(dev, non_blocking=True)
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    opts = pkg.make_options()
+    ws = torch.empty(pkg.ce_workspace_bytes(w.dim0, w.dim1, w.V, x.dtype, opts),
+                     dtype=torch.uint8, device=dev)
+    path, chunks = pkg.ce_plan_path(x, opts)
+    torch.cuda.synchronize(dev)
+
+    def step(o=opts):
+        pkg.ce_fwd_bwd(x, t, label_smoothing=w.label_smoothing, ignore_idx=w.ignore_idx,
+                       reduce_loss=w.reduce_loss, loss_out=loss, workspace=ws, opts=o)
+
+    for _ in range(args.warmup):
+        step()
+    st, err = pkg.ce_get_error(ws)
+    if st != 0:
+        raise RuntimeError(f"device error word {err:#x} after warm-up")
+
+    # per-launch events around the main kernel, on the launching stream
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    step_opts = [pkg.make_options(event_begin=b.cuda_event, event_end=e.cuda_event)
+                 for (b, e) in evs]
+
+    gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    sampler = ClockSampler(gpu_id)
+    time.sleep(0.3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        step(step_opts[i])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    time.sleep(0.2)
+    sampler.stop()
+    clocks = sampler.summary(t0, t1)
+    total_ms = start.elapsed_time(end)
+    kernel_ms = sum(b.elapsed_time(e) for (b, e) in evs) / args.steps
+
+    def allmax(v):
+        if dist is None:
+            return v
+        tt = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        return float(tt.item())
+
+    ms, tok_s = aggregate(total_ms, w.N * args.steps, world, allmax)
+
+    # end to end through the public call: pinned host -> device inputs, the
+    # pass, the loss back to the host, every step
+    e2e_steps = max(1, min(args.e2e_steps, args.steps))
+    h2d = w.logits_bytes + 8 * w.N
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    loss_host = torch.empty(1, dtype=torch.float32, pin_memory=True)
+    s2.record(stream)
+    for _ in range(e2e_steps):
+        x.copy_(x_host, non_blocking=True)
+        t.copy_(t_host, non_blocking=True)
+        step()
+        loss_host.copy_(loss, non_blocking=True)
+    e2.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms, e2e_tok_s = aggregate(s2.elapsed_time(e2), w.N * e2e_steps, world, allmax)
+    st, err = pkg.ce_get_error(ws)
+    if st != 0:
+        raise RuntimeError(f"device error word {err:#x}")
+    if rank != 0:
+        return
+
+    peaks = measured_peaks()
+    nbytes = pass_bytes(w.N, w.V, w.elem_bytes)
+    achieved = nbytes / (kernel_ms / 1e3) / 1e9
+    cpu = None
+    if not args.no_cpu_baseline:
+        rps, rows, secs, cores = oracle_rows_per_s(w, x_host, t_host, args.cpu_budget)
+        cpu = {"value": rps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{rows} rows of the workload in row blocks of 256 "
+                         f"({secs:.1f} s of oracle time, fwd+bwd in double)"}
+    line = {
+        "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded, see vocabulary_cross_entropy_pass_gb300/workloads.py)",
+        "config": config_of(w, args) | {"path": {1: "row", 2: "cluster", 3: "two_stage"}[path],
+                                         "vocab_chunks": chunks},
+        "hbm_gbs_formula": nbytes * args.steps * world / (ms / 1e3) / 1e9,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "peak_source": peaks["source"], "kernel_ms": kernel_ms,
+                     "algorithmic_bytes": nbytes},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_tok_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": 4, "steps": e2e_steps,
+                "ms_per_step": e2e_ms / e2e_steps},
+        "gpu_launches": KERNELS_PER_STEP[path] * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--ref-rows", type=int, default=32)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    from vocabulary_cross_entropy_pass_gb300 import workloads as wl
+    w = wl.WORKLOADS[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return 0
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, w, rank, world, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

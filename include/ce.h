@@ -1,0 +1,175 @@
+/*
+ * ce.h -- C ABI of libgbce, the fused vocabulary cross-entropy pass for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * One call runs, on one GPU and on the caller's stream, the whole pass the
+ * TENPU "Parallel Cross Entropy (Triton)" issue (Ascend/TransformerEngineNPU
+ * #29) describes in its section 1 "Interface":
+ *
+ *     loss = parallel_cross_entropy(inp, target, label_smoothing, reduce_loss,
+ *                                   dist_process_group, ignore_idx)
+ *
+ *   - inp: logits (B,SQ,V) or (SQ,B,V), FP32 / BF16 (FP16 also accepted);
+ *   - target: (B,SQ) or (SQ,B), global vocabulary indices (int64 here);
+ *   - softmax and loss accumulate in FP32, the loss is FP32, the gradient is
+ *     written back in the input dtype (same section), in place over the
+ *     logits (section 6 "Memory": in-place gradient staging);
+ *   - loss of a row = logsumexp(x) - x[target] (CSDN "Ascend CANN ops-nn
+ *     cross-entropy fusion: from three kernel launches to one", section
+ *     "Fusion scheme: log_softmax + NLL"), with PyTorch-style label smoothing
+ *     (1-a)*nll + a*mean_j(-log_softmax_j);
+ *   - gradient of a row = (softmax - (1-a)*onehot(target) - a/V) * dloss
+ *     (same article, section "Backward" and pitfall 3, with the smoothing mass
+ *     spread over all V classes as torch F.cross_entropy does);
+ *   - rows whose target equals ignore_idx (default -100) get loss 0 and a
+ *     zero gradient and are left out of the mean (TENPU #29 section 1;
+ *     mindspore/hyper-parallel #269 section 3.1);
+ *   - reduce_loss: the mean over kept rows, produced on the device by a
+ *     fixed-order reduction (TENPU #29 counts n_non_ignore on the host,
+ *     section 7 "Known limitations"; here the count runs on the device).
+ *
+ * dist_process_group has no counterpart: the vocabulary-parallel combine of
+ * (max, sum-exp, target logit) that hyper-parallel #269 section 3.1 runs as
+ * MAX/SUM all-reduces plus a gather runs here between vocabulary chunks of
+ * one GPU (thread-block clusters over distributed shared memory, or a second
+ * kernel).
+ *
+ * Conventions for every entry point:
+ *   - every pointer argument is a DEVICE pointer unless it says "host";
+ *   - the caller owns all memory; the library allocates nothing, keeps no
+ *     pointer after the call returns and never synchronises the stream
+ *     (ce_get_error excepted);
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream); all work is enqueued on it in order;
+ *   - dims: the logits have shape (dim0, dim1, V); (B,SQ,V) and (SQ,B,V)
+ *     differ only in which of dim0/dim1 is the batch; row (i, j) is the
+ *     flattened row r = i*dim1 + j; element (i, j, v) sits at
+ *     logits + (i*strides[0] + j*strides[1] + v*strides[2]) elements;
+ *     strides[2] must be 1 (non-unit vocabulary stride: make the tensor
+ *     contiguous first, as TENPU #29 "Problems and solutions" does);
+ *   - targets: int64, target of row (i, j) at targets[i*target_strides[0] +
+ *     j*target_strides[1]];
+ *   - errors found on the host are returned before anything is launched;
+ *     a target outside [0, V) that is not ignore_idx is found on the device:
+ *     that row gets loss NaN and a zero gradient, and the device error word
+ *     in the workspace gets CE_DEVERR_TARGET_RANGE (read it with
+ *     ce_get_error).  Kernels never trap.
+ */
+#ifndef GBCE_CE_H
+#define GBCE_CE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { CE_F32 = 0, CE_BF16 = 1, CE_F16 = 2 } ce_dtype;
+
+/* (B,SQ,V): dim0 = B, dim1 = SQ.  (SQ,B,V): dim0 = SQ, dim1 = B. */
+typedef enum { CE_LAYOUT_BSV = 0, CE_LAYOUT_SBV = 1 } ce_layout;
+
+typedef enum {
+    CE_OK = 0,
+    CE_ERR_INVALID_ARG = 1,        /* null pointer, bad size, smoothing outside [0,1], ... */
+    CE_ERR_UNSUPPORTED_DTYPE = 2,
+    CE_ERR_BAD_STRIDE = 3,         /* strides[2] != 1, a negative stride, or (ce_fwd_bwd)
+                                      rows that share memory */
+    CE_ERR_WORKSPACE_TOO_SMALL = 4,
+    CE_ERR_LAUNCH = 5,             /* a CUDA launch or attribute call failed */
+    CE_ERR_TARGET_RANGE = 6,       /* reported by ce_get_error only */
+    CE_ERR_DEVICE_TIMEOUT = 7,     /* reported by ce_get_error only */
+    CE_ERR_UNSUPPORTED_PATH = 8    /* a forced path cannot run this shape */
+} ce_status;
+
+/* Bits of the device error word (ce_get_error). */
+#define CE_DEVERR_TARGET_RANGE 0x1u
+#define CE_DEVERR_TIMEOUT 0x2u     /* a bounded wait inside a kernel gave up */
+
+typedef enum {
+    CE_PATH_AUTO = 0,
+    CE_PATH_ROW = 1,       /* one CTA holds a whole row in shared memory and registers */
+    CE_PATH_CLUSTER = 2,   /* a thread-block cluster splits each row; combine over DSMEM */
+    CE_PATH_TWO_STAGE = 3  /* per-chunk statistics kernel, then combine + gradient kernel */
+} ce_path;
+
+typedef struct {
+    int force_path;         /* ce_path; CE_PATH_AUTO lets the planner choose */
+    int num_vocab_chunks;   /* 0: planner chooses; K > 0: cut V into K contiguous
+                               chunks of ceil(V/K) (rounded up to 16 bytes on the
+                               row and cluster paths) whose partials are combined
+                               on the device */
+    void* event_begin;      /* cudaEvent_t or NULL: recorded on `stream` right
+                               before the main kernel of the pass */
+    void* event_end;        /* cudaEvent_t or NULL: recorded right after it */
+    int tune_threads;       /* 0 = default; otherwise CTA size (256 or 512) */
+    int tune_stages;        /* 0 = default; otherwise TMA pipeline depth (2..4) */
+    int tune_ctas_per_sm;   /* 0 = as many as fit; otherwise a cap */
+    int reserved[5];        /* must be zero */
+} ce_options;
+
+/* Bytes of device workspace a call with these sizes needs (either entry
+ * point, any path, reduce_loss or not).  Host only; returns 0 for invalid
+ * sizes.  opts may be NULL. */
+size_t ce_workspace_bytes(int64_t dim0, int64_t dim1, int64_t V, ce_dtype dtype,
+                          const ce_options* opts);
+
+/* Forward and backward in one pass.
+ *   logits          (dim0, dim1, V) in `dtype`; read, then overwritten with the
+ *                   gradient (grad_inplace must equal logits).
+ *   label_smoothing a in [0, 1].
+ *   ignore_idx      target value that marks a row as ignored (usually -100).
+ *   reduce_loss     0: per-row losses; 1: mean over rows whose target is not
+ *                   ignore_idx.
+ *   dloss           float32 upstream gradient: one value (reduce_loss = 1; the
+ *                   gradient of the mean, each kept row is scaled by dloss/n)
+ *                   or one value per flattened row (reduce_loss = 0); NULL
+ *                   means 1.
+ *   loss_out        float32: one value (reduce_loss = 1; NaN when every row is
+ *                   ignored) or dim0*dim1 values in flattened row order.
+ *   n_non_ignore_out  int64 count of rows whose target != ignore_idx, or NULL.
+ *   workspace       at least ce_workspace_bytes(...) bytes, 256-byte aligned;
+ *                   its contents need no initialisation and must not be
+ *                   shared by calls that may run concurrently.
+ *   opts            NULL for defaults.
+ * Returns CE_OK once every kernel is enqueued. */
+ce_status ce_fwd_bwd(void* logits, ce_dtype dtype, ce_layout layout, int64_t dim0, int64_t dim1,
+                     int64_t V, const int64_t strides[3], const int64_t* targets,
+                     const int64_t target_strides[2], float label_smoothing, int64_t ignore_idx,
+                     int reduce_loss, const float* dloss, float* loss_out, void* grad_inplace,
+                     int64_t* n_non_ignore_out, void* workspace, size_t workspace_bytes,
+                     const ce_options* opts, void* stream);
+
+/* Forward only: the logits are read, never written.  Same arguments as
+ * ce_fwd_bwd minus dloss and the gradient, plus
+ *   lse_out   float32 logsumexp of every row (NaN for ignored or out-of-range
+ *             rows), or NULL. */
+ce_status ce_fwd_only(const void* logits, ce_dtype dtype, ce_layout layout, int64_t dim0,
+                      int64_t dim1, int64_t V, const int64_t strides[3], const int64_t* targets,
+                      const int64_t target_strides[2], float label_smoothing, int64_t ignore_idx,
+                      int reduce_loss, float* loss_out, float* lse_out, int64_t* n_non_ignore_out,
+                      void* workspace, size_t workspace_bytes, const ce_options* opts,
+                      void* stream);
+
+/* Waits for `stream`, then copies the device error word of the last pass that
+ * used `workspace` into *host_err (host pointer).  Returns CE_OK,
+ * CE_ERR_TARGET_RANGE or CE_ERR_DEVICE_TIMEOUT from its bits, CE_ERR_LAUNCH if
+ * the copy fails.  Diagnostic use: this is the only call that synchronises. */
+ce_status ce_get_error(const void* workspace, void* stream, uint32_t* host_err);
+
+/* Static English description of a status code. */
+const char* ce_status_string(ce_status status);
+
+/* Path the planner would take for these arguments (host only): CE_PATH_ROW,
+ * CE_PATH_CLUSTER or CE_PATH_TWO_STAGE, with the vocabulary chunk count in
+ * *chunks_out (host pointer, may be NULL).  Returns -1 for arguments
+ * ce_fwd_bwd would reject, -2 for a forced path that cannot run them. */
+int ce_plan_path(const void* logits, ce_dtype dtype, int64_t dim0, int64_t dim1, int64_t V,
+                 const int64_t strides[3], const ce_options* opts, int* chunks_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBCE_CE_H */

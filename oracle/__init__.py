@@ -48,6 +48,8 @@ def _bind(lib):
                               c_dbl, c_i64, c_int, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]
     lib.oracle_round.restype = c_dbl
     lib.oracle_round.argtypes = [c_dbl, c_int]
+    lib.oracle_round_array.restype = None
+    lib.oracle_round_array.argtypes = [c_vp, c_i64, c_int, c_vp]
     lib.oracle_encode.restype = ctypes.c_uint32
     lib.oracle_encode.argtypes = [c_dbl, c_int]
     lib.oracle_decode.restype = c_dbl
@@ -113,10 +115,13 @@ def ce(logits: np.ndarray, dtype: int, dim0: int, dim1: int, V: int, strides=Non
 
 
 def round_to(values, dtype: int, lib=None) -> np.ndarray:
-    """Round each double to the storage format (ties to even); result as double."""
+    """Round each double to the storage format (ties to even); result as double,
+    same shape as ``values``."""
     lib = lib or load()
-    v = np.asarray(values, dtype=np.float64).ravel()
-    return np.array([lib.oracle_round(float(x), dtype) for x in v], dtype=np.float64)
+    v = np.ascontiguousarray(values, dtype=np.float64)
+    out = np.empty_like(v)
+    lib.oracle_round_array(_ptr(v), v.size, dtype, _ptr(out))
+    return out
 
 
 def encode(values, dtype: int, lib=None) -> np.ndarray:

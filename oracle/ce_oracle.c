@@ -139,6 +139,11 @@ uint32_t oracle_encode(double v, int dtype) {
     return sign | ((uint32_t)(lead + 15) << 10) | mant;
 }
 
+/* oracle_round over an array (out may alias in). */
+void oracle_round_array(const double* in, int64_t n, int dtype, double* out) {
+    for (int64_t k = 0; k < n; ++k) out[k] = oracle_round(in[k], dtype);
+}
+
 /* ---------------------------------------------------------------------------
  * One token row, from the definitions.
  *   lse    = m + log(sum_j exp(x_j - m)),  m = max_j x_j   [OPSNN-CE pitfall 1]

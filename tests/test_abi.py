@@ -1,0 +1,131 @@
+"""The C ABI on the CPU: the library loads, exports every function the header
+declares, sizes workspaces, and rejects bad arguments on the host before any
+CUDA call (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from vocabulary_cross_entropy_pass_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ce.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from vocabulary_cross_entropy_pass_gb300 import build
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:[A-Za-z_][\w\s\*]*?)\b(ce_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_known_entry_points():
+    assert declared_functions() == sorted(_lib.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    # exported with C linkage: no mangled names needed
+    nm = os.popen(f"nm -D --defined-only {_lib.LIB_PATH}").read()
+    for name in declared_functions():
+        assert re.search(rf"\bT {name}$", nm, flags=re.M), name
+
+
+def test_status_strings(lib):
+    for code in range(9):
+        s = lib.ce_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert lib.ce_status_string(99).decode() == "unknown status"
+
+
+def test_workspace_bytes(lib):
+    ws = lib.ce_workspace_bytes(4, 4096, 128000, 1, None)
+    # header + per-row losses + per-(row, chunk) partials of the fallback path
+    assert ws >= 256 + 4 * 16384 + 16 * 16384 * 32
+    assert lib.ce_workspace_bytes(-1, 4, 10, 1, None) == 0
+    assert lib.ce_workspace_bytes(1, 4, 0, 1, None) == 0
+    assert lib.ce_workspace_bytes(1, 4, 10, 7, None) == 0
+    o = _lib.make_options(num_vocab_chunks=8)
+    assert lib.ce_workspace_bytes(2, 256, 65536, 1, ctypes.byref(o)) >= 16 * 512 * 8
+
+
+def _call(lib, **kw):
+    args = dict(logits=0x1000, dtype=1, layout=0, d0=2, d1=3, V=4096, strides=(3 * 4096, 4096, 1),
+                targets=0x2000, tstrides=(3, 1), a=0.0, ignore=-100, reduce=0, dloss=None,
+                loss=0x3000, grad=None, n=None, ws=0x4000, wsb=1 << 30, opts=None)
+    args.update(kw)
+    if args["grad"] is None:
+        args["grad"] = args["logits"]
+    return lib.ce_fwd_bwd(ctypes.c_void_p(args["logits"]), args["dtype"], args["layout"], args["d0"],
+                          args["d1"], args["V"], _lib.i64_array(args["strides"]),
+                          ctypes.c_void_p(args["targets"]), _lib.i64_array(args["tstrides"]),
+                          args["a"], args["ignore"], args["reduce"], ctypes.c_void_p(args["dloss"]),
+                          ctypes.c_void_p(args["loss"]), ctypes.c_void_p(args["grad"]),
+                          ctypes.c_void_p(args["n"]), ctypes.c_void_p(args["ws"]), args["wsb"],
+                          args["opts"], None)
+
+
+def test_host_validation_rejects_before_launch(lib):
+    # every case below fails in the host checks, before any CUDA call
+    assert _call(lib, dtype=5) == 2
+    assert _call(lib, layout=2) == 1
+    assert _call(lib, logits=0) == 1
+    assert _call(lib, targets=0) == 1
+    assert _call(lib, loss=0) == 1
+    assert _call(lib, ws=0) == 1
+    assert _call(lib, V=0) == 1
+    assert _call(lib, d0=-1) == 1
+    assert _call(lib, a=1.5) == 1
+    assert _call(lib, a=float("nan")) == 1
+    assert _call(lib, strides=(3 * 4096, 4096, 2)) == 3
+    assert _call(lib, strides=(-1, 4096, 1)) == 3
+    assert _call(lib, tstrides=(-3, 1)) == 3
+    assert _call(lib, ws=0x4008) == 1          # not 16-byte aligned
+    assert _call(lib, wsb=100) == 4
+    assert _call(lib, grad=0x9000) == 1        # the gradient must go in place
+    o = _lib.make_options()
+    o.reserved[2] = 1
+    assert _call(lib, opts=ctypes.byref(o)) == 1
+    o = _lib.make_options(tune_threads=300)
+    assert _call(lib, opts=ctypes.byref(o)) == 1
+
+
+def test_planner(lib):
+    def plan(V, dtype=1, strides=None, base=0x1000, **o):
+        opts = _lib.make_options(**o)
+        ch = ctypes.c_int(0)
+        st = strides or (3 * V, V, 1)
+        p = lib.ce_plan_path(ctypes.c_void_p(base), dtype, 2, 3, V, _lib.i64_array(st),
+                             ctypes.byref(opts), ctypes.byref(ch))
+        return p, ch.value
+    assert plan(4096) == (1, 1)
+    assert plan(8192) == (1, 1)
+    assert plan(32000) == (2, 4)
+    assert plan(128000) == (2, 16)
+    assert plan(128000, dtype=0) == (2, 16)
+    assert plan(65536, num_vocab_chunks=8, force_path=2) == (2, 8)
+    assert plan(65536, num_vocab_chunks=8, force_path=3) == (3, 8)
+    assert plan(4095)[0] == 3                      # rows not 16-byte aligned
+    assert plan(4096, base=0x1002)[0] == 3         # base not 16-byte aligned
+    assert plan(4096, force_path=1, base=0x1002)[0] == -2
+    assert plan(4_000_000)[0] == 3                 # too wide for 16 CTAs
+    assert plan(32000, force_path=1)[0] == -2      # one CTA cannot hold the row
+    assert plan(4096, force_path=2) == (2, 2)
+
+
+def test_overlapping_rows_rejected_for_in_place_gradient(lib):
+    # a broadcast (stride 0) or rows closer than V apart cannot take an in-place gradient
+    assert _call(lib, strides=(0, 4096, 1)) == 3
+    assert _call(lib, strides=(3 * 4096, 100, 1)) == 3
+    # a transposed (SQ, B, V) storage read as (B, SQ, V) passes the host checks
+    # and fails later only for want of a GPU
+    assert _call(lib, d0=2, d1=3, strides=(4096, 2 * 4096, 1)) not in (1, 2, 3, 4)

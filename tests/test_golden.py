@@ -47,3 +47,13 @@ def test_pitfall3_smoothing_share_of_gradient(oracle_lib):
     # the target class gets back (1 - a) of its one-hot minus the same share
     assert math.isclose(ga[11] - g0[11], g["label_smoothing"] - share, rel_tol=1e-9)
 
+
+
+def test_fused_table_matrix_bytes():
+    import bench
+    g = _read("ops_nn_fused_table_bytes.txt")
+    B, V, s = int(g["B"]), int(g["V"]), int(g["elem_bytes"])
+    logits_bytes = bench.logits_bytes(B, V, s)
+    assert round(logits_bytes / 1e6) == g["matrix_MB"]
+    # one read of the logits + one gradient write + int64 targets
+    assert bench.pass_bytes(B, V, s) == 2 * logits_bytes + 8 * B

@@ -1,0 +1,226 @@
+"""Edge cases of the GPU pass against the CPU oracle: tiny and unaligned
+vocabularies, padded and transposed rows, empty and ragged vocabulary chunks,
+all-ignored rows, out-of-range targets, N = 0, forward-only, determinism of
+the mean, and the full-size throughput workload on sampled rows."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import vocabulary_cross_entropy_pass_gb300 as pkg
+from tests import harness
+from vocabulary_cross_entropy_pass_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda")
+TDT = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
+
+
+def _compare(w, x_cpu, t_cpu, loss, g_dev, n_dev=None, strides=None, tstrides=None):
+    """Oracle on the CPU copy (same storage/strides) vs GPU outputs."""
+    dl = np.array([1.0]) if w.reduce_loss else None
+    ref = oracle.ce(harness.storage_np(x_cpu), harness.CODE[w.dtype], w.dim0, w.dim1, w.V,
+                    strides=strides, targets=t_cpu.contiguous().numpy().ravel(),
+                    target_strides=tstrides,
+                    label_smoothing=w.label_smoothing, ignore_idx=w.ignore_idx,
+                    reduce_loss=w.reduce_loss, dloss=dl)
+    harness.check_loss(loss.cpu().numpy(), ref["loss"], w.dtype, w.name)
+    if n_dev is not None:
+        assert int(n_dev.item()) == ref["n"]
+    if g_dev is not None:
+        g = g_dev.float().cpu().numpy().reshape(w.N, w.V).astype(np.float64)
+        excess, _ = harness.grad_errors(g, ref["grad"], w.dtype)
+        assert excess <= 0.0, f"{w.name}: gradient exceeds tolerance by {excess:.3e}"
+    return ref
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("V", [1, 7, 8, 9, 33, 4095, 4096, 8200])
+def test_small_and_unaligned_vocab(dtype, V):
+    for N, a, red in ((1, 0.0, False), (3, 0.2, True), (5, 0.0, False)):
+        w = wl.Workload(f"v{V}", 1, N, V, dtype, sigma=2.0, ignore_frac=0.2 if N > 3 else 0.0,
+                        label_smoothing=a, reduce_loss=red, seed=11 + V + N)
+        x = wl.logits(w)
+        t = wl.targets(w)
+        xd, td = x.to(DEV), t.to(DEV)
+        n = torch.zeros(1, dtype=torch.int64, device=DEV)
+        loss = pkg.ce_fwd_bwd(xd, td, label_smoothing=a, reduce_loss=red, n_non_ignore_out=n)
+        _compare(w, x, t, loss, xd, n)
+
+
+@pytest.mark.parametrize("dtype,pad", [("bf16", 8), ("bf16", 3), ("f32", 4), ("f16", 16)])
+def test_padded_rows(dtype, pad):
+    w = wl.Workload("pad", 2, 5, 4000, dtype, sigma=2.0, label_smoothing=0.1, seed=31)
+    x = wl.logits(w)
+    buf = torch.zeros(2, 5, 4000 + pad, dtype=TDT[dtype])
+    buf[:, :, :4000] = x
+    t = wl.targets(w)
+    bd = buf.to(DEV)
+    view = bd[:, :, :4000]
+    loss = pkg.ce_fwd_bwd(view, t.to(DEV), label_smoothing=0.1)
+    _compare(w, buf, t, loss, None, strides=(5 * (4000 + pad), 4000 + pad))
+    g = view.float().cpu().numpy().reshape(w.N, w.V)
+    ref = harness.oracle_run(w, x, t)
+    excess, _ = harness.grad_errors(g.astype(np.float64), ref["grad"], dtype)
+    assert excess <= 0.0
+    # the padding is never touched
+    assert torch.all(bd[:, :, 4000:].cpu() == 0)
+
+
+@pytest.mark.parametrize("V", [4096, 32000])
+def test_transposed_view(V):
+    # storage (SQ, B, V), read as (B, SQ, V) through strides
+    SQ, B = 6, 3
+    w = wl.Workload("tr", SQ, B, V, "bf16", sigma=2.0, label_smoothing=0.1, seed=41)
+    x = wl.logits(w)                # (SQ, B, V)
+    t = wl.targets(w)               # (SQ, B)
+    xd = x.to(DEV)
+    td = t.to(DEV)
+    v = xd.permute(1, 0, 2)         # (B, SQ, V), strides (V, B*V, 1)
+    tv = td.t()                     # (B, SQ), strides (1, B)
+    loss = pkg.ce_fwd_bwd(v, tv, label_smoothing=0.1)
+    ref = oracle.ce(harness.storage_np(x), oracle.BF16, B, SQ, V, strides=(V, B * V),
+                    targets=t.numpy().ravel(), target_strides=(1, B), label_smoothing=0.1)
+    harness.check_loss(loss.cpu().numpy(), ref["loss"], "bf16")
+    g = v.float().cpu().numpy().reshape(B * SQ, V).astype(np.float64)
+    excess, _ = harness.grad_errors(g, ref["grad"], "bf16")
+    assert excess <= 0.0
+
+
+@pytest.mark.parametrize("K", [2, 3, 5, 8, 16])
+def test_cluster_chunk_counts(K):
+    w = wl.Workload("k", 1, 40, 24000, "bf16", sigma=2.0, label_smoothing=0.1, reduce_loss=True,
+                    seed=50 + K)
+    harness.run_gpu_vs_oracle(w, force_path=2, num_vocab_chunks=K)
+    harness.run_gpu_vs_oracle(w, force_path=3, num_vocab_chunks=K)
+
+
+def test_empty_chunks():
+    # V = 16 bf16 over 8 CTAs: 16-byte chunks of 8 columns leave six CTAs empty
+    w = wl.Workload("e", 1, 7, 16, "bf16", sigma=3.0, seed=61)
+    harness.run_gpu_vs_oracle(w, force_path=2, num_vocab_chunks=8)
+    w = wl.Workload("e", 1, 7, 40, "f32", sigma=3.0, seed=62)
+    harness.run_gpu_vs_oracle(w, force_path=2, num_vocab_chunks=16)
+
+
+@pytest.mark.parametrize("path", [0, 3])
+def test_all_ignored_mean_is_nan(path):
+    x = torch.randn(3, 4, 1024, device=DEV).to(torch.bfloat16)
+    t = torch.full((3, 4), -100, dtype=torch.int64, device=DEV)
+    n = torch.ones(1, dtype=torch.int64, device=DEV)
+    loss = pkg.ce_fwd_bwd(x, t, reduce_loss=True, n_non_ignore_out=n, force_path=path)
+    assert math.isnan(loss.item()) and int(n.item()) == 0
+    assert torch.all(x == 0)
+
+
+@pytest.mark.parametrize("path", [0, 2, 3])
+def test_out_of_range_target_sets_error(path):
+    w = wl.Workload("oor", 1, 6, 8192, "bf16", sigma=2.0, ignore_frac=0.0, seed=71)
+    x = wl.logits(w)
+    t = wl.targets(w)
+    t[0, 2] = 8192
+    t[0, 4] = -7
+    xd, td = x.to(DEV), t.to(DEV)
+    ws = torch.empty(pkg.ce_workspace_bytes(1, 6, 8192, torch.bfloat16), dtype=torch.uint8,
+                     device=DEV)
+    loss = pkg.ce_fwd_bwd(xd, td, workspace=ws, force_path=path)
+    st, err = pkg.ce_get_error(ws)
+    assert err & 1 and st == 6
+    lc = loss.cpu().numpy()
+    assert math.isnan(lc[2]) and math.isnan(lc[4])
+    assert torch.all(xd[0, 2] == 0) and torch.all(xd[0, 4] == 0)
+    ref = harness.oracle_run(w, x, t)
+    keep = [0, 1, 3, 5]
+    harness.check_loss(lc[keep], ref["loss"][keep], "bf16")
+    # a later clean pass on the same workspace clears the error word
+    loss = pkg.ce_fwd_bwd(x.to(DEV), wl.targets(w).to(DEV), workspace=ws, force_path=path)
+    assert pkg.ce_get_error(ws) == (0, 0)
+
+
+def test_non_negative_ignore_index():
+    w = wl.Workload("ig", 1, 9, 512, "f32", sigma=1.0, ignore_frac=0.0, seed=81)
+    x = wl.logits(w)
+    t = wl.targets(w)
+    t[0, 3] = 5
+    w2 = w.with_(ignore_idx=5)
+    xd = x.to(DEV)
+    loss = pkg.ce_fwd_bwd(xd, t.to(DEV), ignore_idx=5)
+    ref = harness.oracle_run(w2, x, t)
+    harness.check_loss(loss.cpu().numpy(), ref["loss"], "f32")
+    assert loss[3].item() == 0.0 and torch.all(xd[0, 3] == 0)
+
+
+def test_zero_rows():
+    x = torch.empty(0, 4, 4096, dtype=torch.bfloat16, device=DEV)
+    t = torch.empty(0, 4, dtype=torch.int64, device=DEV)
+    loss = pkg.ce_fwd_bwd(x, t, reduce_loss=True)
+    assert math.isnan(loss.item())
+    loss = pkg.ce_fwd_bwd(x, t, reduce_loss=False)
+    assert loss.numel() == 0
+
+
+@pytest.mark.parametrize("name,path", [("c5_bsv128000_bf16_ls", 0), ("c3_bsv32000_bf16_spiked", 0),
+                                       ("c2_sbv8192_bf16", 0), ("c4_bsv65536_bf16_split8", 3)])
+def test_fwd_only_matches(name, path):
+    w = wl.WORKLOADS[name]
+    x = wl.logits(w)
+    t = wl.targets(w)
+    xd, td = x.to(DEV), t.to(DEV)
+    lse = torch.empty(w.N, dtype=torch.float32, device=DEV)
+    loss = pkg.ce_fwd_only(xd, td, label_smoothing=w.label_smoothing, reduce_loss=False,
+                           lse_out=lse, force_path=path)
+    assert torch.equal(xd.cpu(), x)  # logits untouched
+    ref = harness.oracle_run(w.with_(reduce_loss=False), x, t, want_grad=False)
+    harness.check_loss(loss.cpu().numpy(), ref["loss"], w.dtype)
+    lse_ref = ref["lse"]
+    lg = lse.cpu().numpy().astype(np.float64)
+    ok = ~np.isnan(lse_ref)
+    assert np.all(np.isnan(lg[~ok]))
+    assert np.max(np.abs(lg[ok] - lse_ref[ok]) / np.maximum(np.abs(lse_ref[ok]), 1)) <= 1e-5
+    # forward-only losses equal the fused pass's losses bit for bit on the fused paths
+    loss2 = pkg.ce_fwd_bwd(xd.clone(), td, label_smoothing=w.label_smoothing, force_path=path)
+    if path != 3:
+        assert torch.equal(loss, loss2)
+
+
+def test_mean_is_deterministic():
+    w = wl.WORKLOADS["c5_bsv128000_bf16_ls"]
+    x = wl.logits(w).to(DEV)
+    t = wl.targets(w).to(DEV)
+    vals = []
+    for _ in range(10):
+        loss = pkg.ce_fwd_bwd(x.clone(), t, label_smoothing=0.1, reduce_loss=True)
+        vals.append(loss.cpu().numpy().tobytes())
+    assert len(set(vals)) == 1
+
+
+def test_full_size_sampled_rows():
+    """The throughput workload (4, 4096, 128000) bf16 in the launch
+    configuration the bench times: the mean against the oracle over all rows,
+    and the gradient of sampled rows element by element."""
+    w = wl.WORKLOADS["c5t_bsv128000_bf16"]
+    x = wl.logits(w)
+    t = wl.targets(w)
+    rng = np.random.default_rng(5)
+    rows = np.sort(rng.choice(w.N, 48, replace=False))
+    rows = np.unique(np.concatenate([rows, wl.ignored_rows(w)[:4], [0, w.N - 1]]))
+    xd = x.to(DEV)
+    td = t.to(DEV)
+    n = torch.zeros(1, dtype=torch.int64, device=DEV)
+    loss = pkg.ce_fwd_bwd(xd, td, label_smoothing=w.label_smoothing, reduce_loss=True,
+                          n_non_ignore_out=n)
+    g_rows = xd.view(w.N, w.V)[torch.as_tensor(rows, device=DEV)].float().cpu().numpy()
+    del xd
+    ref_all = harness.oracle_run(w, x, t, want_grad=False)
+    assert int(n.item()) == ref_all["n"]
+    harness.check_loss(loss.cpu().numpy(), ref_all["loss"], "bf16", "full-size mean")
+    # per-row oracle on the sampled rows, scale dloss/n of the full pass
+    sub = x.view(w.N, w.V)[torch.as_tensor(rows)].contiguous()
+    tsub = t.view(-1)[torch.as_tensor(rows)].contiguous()
+    scale = np.full(len(rows), 1.0 / ref_all["n"])
+    ref = oracle.ce(harness.storage_np(sub), oracle.BF16, 1, len(rows), w.V,
+                    targets=tsub.numpy(), label_smoothing=w.label_smoothing, dloss=scale)
+    excess, _ = harness.grad_errors(g_rows.astype(np.float64), ref["grad"], "bf16")
+    assert excess <= 0.0

@@ -1,0 +1,54 @@
+"""GPU (through the C ABI) against the CPU oracle on every workload family,
+on each path that can run it.  Needs a GB300 and the built library."""
+import numpy as np
+import pytest
+import torch
+
+from tests import harness
+from vocabulary_cross_entropy_pass_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+AUTO, ROW, CLUSTER, TWO = 0, 1, 2, 3
+
+CASES = [
+    ("c1_bsv4096_f32", AUTO, None), ("c1_bsv4096_f32", TWO, None),
+    ("c2_sbv8192_bf16", AUTO, None), ("c2_sbv8192_bf16", CLUSTER, None),
+    ("c2_sbv8192_bf16", TWO, None),
+    ("c3_bsv32000_bf16_spiked", AUTO, None), ("c3_bsv32000_bf16_spiked", TWO, None),
+    ("c3h_bsv32000_f16_spiked", AUTO, None), ("c3h_bsv32000_f16_spiked", TWO, None),
+    ("c4_bsv65536_bf16_split8", CLUSTER, 8), ("c4_bsv65536_bf16_split8", TWO, 8),
+    ("c5_bsv128000_bf16", AUTO, None), ("c5_bsv128000_bf16_ls", AUTO, None),
+    ("c5_bsv128000_bf16_ls", TWO, None),
+    ("c5_bsv128000_f32", AUTO, None), ("c5_bsv128000_f32_ls", AUTO, None),
+    ("c5_bsv128000_f32_ls", TWO, None),
+]
+
+
+@pytest.mark.parametrize("name,path,chunks", CASES,
+                         ids=[f"{n}-p{p}" + (f"-k{k}" if k else "") for n, p, k in CASES])
+def test_workload_parity(name, path, chunks):
+    w = wl.WORKLOADS[name]
+    res = harness.run_gpu_vs_oracle(w, force_path=path, num_vocab_chunks=chunks)
+    print(name, path, res)
+
+
+def test_per_row_dloss():
+    w = wl.WORKLOADS["c3_bsv32000_bf16_spiked"].with_(dim0=1, dim1=96)
+    harness.run_gpu_vs_oracle(w, per_row_dloss=True)
+    w = wl.WORKLOADS["c1_bsv4096_f32"].with_(label_smoothing=0.3)
+    harness.run_gpu_vs_oracle(w, per_row_dloss=True)
+
+
+def test_planner_paths():
+    import vocabulary_cross_entropy_pass_gb300 as pkg
+    dev = torch.device("cuda")
+    x = torch.empty(2, 3, 4096, dtype=torch.bfloat16, device=dev)
+    assert pkg.ce_plan_path(x)[0] == ROW
+    x = torch.empty(2, 3, 128000, dtype=torch.bfloat16, device=dev)
+    assert pkg.ce_plan_path(x)[0] == CLUSTER
+    x = torch.empty(2, 3, 4095, dtype=torch.bfloat16, device=dev)  # rows not 16-byte aligned
+    assert pkg.ce_plan_path(x)[0] == TWO
+    opts = pkg.make_options(force_path=CLUSTER, num_vocab_chunks=8)
+    x = torch.empty(2, 256, 65536, dtype=torch.bfloat16, device=dev)
+    assert pkg.ce_plan_path(x, opts) == (CLUSTER, 8)

@@ -1,0 +1,189 @@
+"""Fused vocabulary cross-entropy forward+backward for NVIDIA GB300 (sm_103a).
+
+The work runs in libgbce.so (hand-written CUDA kernels behind a C ABI,
+include/ce.h); this package only marshals torch tensors into that ABI.  The
+entry points keep the C names:
+
+  ce_fwd_bwd(logits, targets, ...)   loss; the gradient overwrites logits
+  ce_fwd_only(logits, targets, ...)  loss (and optionally lse); logits kept
+  ce_workspace_bytes(...), ce_get_error(...), ce_status_string(...),
+  ce_plan_path(...)
+
+whose arguments follow the TENPU "Parallel Cross Entropy (Triton)" interface
+(Ascend/TransformerEngineNPU issue #29, section 1).
+
+Importing the package does not load the library; the first call does, and
+raises if it is missing.  There is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import (CE_PATH_AUTO, CE_PATH_CLUSTER, CE_PATH_ROW, CE_PATH_TWO_STAGE, CEError,
+                   ce_options, make_options)
+
+__all__ = ["ce_fwd_bwd", "ce_fwd_only", "ce_workspace_bytes", "ce_get_error", "ce_status_string",
+           "ce_plan_path", "CEError", "make_options", "ce_options",
+           "CE_PATH_AUTO", "CE_PATH_ROW", "CE_PATH_CLUSTER", "CE_PATH_TWO_STAGE"]
+
+_DTYPE = {torch.float32: _lib.CE_F32, torch.bfloat16: _lib.CE_BF16, torch.float16: _lib.CE_F16}
+_LAYOUT = {"bsv": _lib.CE_LAYOUT_BSV, "sbv": _lib.CE_LAYOUT_SBV}
+
+
+def _dims(logits: torch.Tensor):
+    if logits.dim() == 3:
+        d0, d1, V = logits.shape
+        s = logits.stride()
+        return d0, d1, V, (s[0], s[1], s[2])
+    if logits.dim() == 2:
+        N, V = logits.shape
+        s = logits.stride()
+        return 1, N, V, (N * s[0], s[0], s[1])
+    raise ValueError("logits must be (dim0, dim1, V) or (N, V)")
+
+
+def _tstrides(targets: torch.Tensor, d0: int, d1: int):
+    if targets.dim() == 2:
+        if tuple(targets.shape) != (d0, d1):
+            raise ValueError(f"targets shape {tuple(targets.shape)} does not match ({d0}, {d1})")
+        return targets.stride()[0], targets.stride()[1]
+    if targets.dim() == 1 and targets.shape[0] == d0 * d1 and d0 == 1:
+        return d1 * targets.stride()[0], targets.stride()[0]
+    raise ValueError("targets must be (dim0, dim1) (or (N,) with (N, V) logits)")
+
+
+def _check(logits, targets):
+    if not logits.is_cuda or not targets.is_cuda:
+        raise ValueError("logits and targets must be CUDA tensors (there is no CPU path)")
+    if logits.device != targets.device:
+        raise ValueError("logits and targets must be on the same device")
+    if logits.dtype not in _DTYPE:
+        raise TypeError(f"unsupported logits dtype {logits.dtype}")
+    if targets.dtype != torch.int64:
+        raise TypeError("targets must be int64")
+    if logits.stride(-1) != 1:
+        raise ValueError("the vocabulary dimension must be contiguous (call .contiguous())")
+
+
+def _options(opts, force_path, num_vocab_chunks):
+    if opts is None:
+        opts = make_options(force_path=force_path, num_vocab_chunks=num_vocab_chunks)
+    return opts
+
+
+def _raise(st: int, what: str):
+    if st != 0:
+        raise CEError(st, what)
+
+
+def ce_workspace_bytes(dim0: int, dim1: int, V: int, dtype: torch.dtype, opts=None) -> int:
+    lib = _lib.load()
+    return int(lib.ce_workspace_bytes(dim0, dim1, V, _DTYPE[dtype],
+                                      ctypes.byref(opts) if opts is not None else None))
+
+
+def ce_plan_path(logits: torch.Tensor, opts=None):
+    """(path, chunks) the planner picks for these logits."""
+    lib = _lib.load()
+    d0, d1, V, st = _dims(logits)
+    chunks = ctypes.c_int(0)
+    path = lib.ce_plan_path(ctypes.c_void_p(logits.data_ptr()), _DTYPE[logits.dtype], d0, d1, V,
+                            _lib.i64_array(st), ctypes.byref(opts) if opts is not None else None,
+                            ctypes.byref(chunks))
+    return int(path), int(chunks.value)
+
+
+def _workspace(workspace, d0, d1, V, dtype, opts, device):
+    need = ce_workspace_bytes(d0, d1, V, dtype, opts)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+def _stream(device, stream):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def ce_fwd_bwd(logits: torch.Tensor, targets: torch.Tensor, label_smoothing: float = 0.0,
+               ignore_idx: int = -100, reduce_loss: bool = False, dloss: torch.Tensor | None = None,
+               layout: str = "bsv", loss_out: torch.Tensor | None = None,
+               n_non_ignore_out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+               force_path: int = CE_PATH_AUTO, num_vocab_chunks: int = 0, opts=None,
+               stream=None) -> torch.Tensor:
+    """Loss of every row (or the mean); the gradient overwrites ``logits``.
+
+    ``dloss``: float32 CUDA tensor, one value (reduce_loss) or one per row;
+    None means 1.  Returns ``loss_out`` (allocated when None).
+    """
+    _check(logits, targets)
+    lib = _lib.load()
+    d0, d1, V, st = _dims(logits)
+    ts = _tstrides(targets, d0, d1)
+    opts = _options(opts, force_path, num_vocab_chunks)
+    dev = logits.device
+    if loss_out is None:
+        loss_out = torch.empty(1 if reduce_loss else d0 * d1, dtype=torch.float32, device=dev)
+    if dloss is not None and (dloss.dtype != torch.float32 or not dloss.is_cuda):
+        raise TypeError("dloss must be a float32 CUDA tensor")
+    ws, wsb = _workspace(workspace, d0, d1, V, logits.dtype, opts, dev)
+    rc = lib.ce_fwd_bwd(ctypes.c_void_p(logits.data_ptr()), _DTYPE[logits.dtype], _LAYOUT[layout],
+                        d0, d1, V, _lib.i64_array(st), ctypes.c_void_p(targets.data_ptr()),
+                        _lib.i64_array(ts), float(label_smoothing), int(ignore_idx),
+                        int(bool(reduce_loss)),
+                        ctypes.c_void_p(dloss.data_ptr() if dloss is not None else None),
+                        ctypes.c_void_p(loss_out.data_ptr()), ctypes.c_void_p(logits.data_ptr()),
+                        ctypes.c_void_p(n_non_ignore_out.data_ptr()
+                                        if n_non_ignore_out is not None else None),
+                        ctypes.c_void_p(ws.data_ptr()), wsb, ctypes.byref(opts),
+                        _stream(dev, stream))
+    _raise(rc, "ce_fwd_bwd")
+    return loss_out
+
+
+def ce_fwd_only(logits: torch.Tensor, targets: torch.Tensor, label_smoothing: float = 0.0,
+                ignore_idx: int = -100, reduce_loss: bool = False, layout: str = "bsv",
+                loss_out: torch.Tensor | None = None, lse_out: torch.Tensor | None = None,
+                n_non_ignore_out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                force_path: int = CE_PATH_AUTO, num_vocab_chunks: int = 0, opts=None,
+                stream=None) -> torch.Tensor:
+    """Loss of every row (or the mean); ``logits`` is left untouched."""
+    _check(logits, targets)
+    lib = _lib.load()
+    d0, d1, V, st = _dims(logits)
+    ts = _tstrides(targets, d0, d1)
+    opts = _options(opts, force_path, num_vocab_chunks)
+    dev = logits.device
+    if loss_out is None:
+        loss_out = torch.empty(1 if reduce_loss else d0 * d1, dtype=torch.float32, device=dev)
+    ws, wsb = _workspace(workspace, d0, d1, V, logits.dtype, opts, dev)
+    rc = lib.ce_fwd_only(ctypes.c_void_p(logits.data_ptr()), _DTYPE[logits.dtype], _LAYOUT[layout],
+                         d0, d1, V, _lib.i64_array(st), ctypes.c_void_p(targets.data_ptr()),
+                         _lib.i64_array(ts), float(label_smoothing), int(ignore_idx),
+                         int(bool(reduce_loss)), ctypes.c_void_p(loss_out.data_ptr()),
+                         ctypes.c_void_p(lse_out.data_ptr() if lse_out is not None else None),
+                         ctypes.c_void_p(n_non_ignore_out.data_ptr()
+                                         if n_non_ignore_out is not None else None),
+                         ctypes.c_void_p(ws.data_ptr()), wsb, ctypes.byref(opts),
+                         _stream(dev, stream))
+    _raise(rc, "ce_fwd_only")
+    return loss_out
+
+
+def ce_get_error(workspace: torch.Tensor, stream=None) -> tuple[int, int]:
+    """(status, device error word) of the last pass that used ``workspace``;
+    waits for the stream."""
+    lib = _lib.load()
+    err = ctypes.c_uint32(0)
+    rc = lib.ce_get_error(ctypes.c_void_p(workspace.data_ptr()), _stream(workspace.device, stream),
+                          ctypes.byref(err))
+    return int(rc), int(err.value)
+
+
+def ce_status_string(status: int) -> str:
+    return _lib.load().ce_status_string(int(status)).decode()
+

@@ -1,0 +1,299 @@
+// ce_api.cu -- the C ABI of libgbce: argument checks, the path planner and
+// the launch sequence.  Every entry point is declared and documented in
+// include/ce.h.
+//
+// One pass enqueues, on the caller's stream:
+//   1. ce_count_kernel    -- n_non_ignore and the target range check (needed
+//                            before any gradient: a kept row is scaled by
+//                            dloss/n under reduce_loss);
+//   2. the main kernel(s) -- the fused row/cluster kernel, or the two stage
+//                            kernels of the split path;
+//   3. ce_mean_kernel     -- reduce_loss only: the fixed-order mean.
+// Nothing is allocated and nothing waits for the device.
+#include <math.h>
+#include <string.h>
+
+#include "ce_internal.h"
+
+namespace gbce {
+
+int elem_size(int dtype) { return dtype == CE_F32 ? 4 : 2; }
+
+namespace {
+
+constexpr int kMaxCluster = 16;
+constexpr size_t kSmemLimit = 227 * 1024;
+
+struct Plan {
+    int path;  // CE_PATH_ROW / CLUSTER / TWO_STAGE, or < 0 on error
+    FusedPlan fused;
+    SplitPlan split;
+};
+
+int round_up_int(int64_t x, int64_t m) { return (int)((x + m - 1) / m * m); }
+
+bool opts_clean(const ce_options* o) {
+    if (!o) return true;
+    for (int i = 0; i < 5; ++i)
+        if (o->reserved[i] != 0) return false;
+    if (o->force_path < 0 || o->force_path > CE_PATH_TWO_STAGE) return false;
+    if (o->num_vocab_chunks < 0) return false;
+    if (o->tune_threads != 0 && o->tune_threads != 256 && o->tune_threads != 512) return false;
+    if (o->tune_stages < 0 || o->tune_stages > 4 || o->tune_stages == 1) return false;
+    if (o->tune_ctas_per_sm < 0) return false;
+    return true;
+}
+
+// Choose the fused-kernel shape; returns false when the fused kernel cannot
+// take this problem (V too large for 16 CTAs, a forced K it cannot honour).
+bool plan_fused(int dtype, int64_t V, const ce_options* o, bool want_cluster, FusedPlan* fp) {
+    const int es = elem_size(dtype);
+    const int vec = 16 / es;
+    const int K = o ? o->num_vocab_chunks : 0;
+    int C;
+    if (K > 0) {
+        C = K;
+    } else {
+        // prefer 256-thread CTAs (several resident per SM); 512-thread CTAs
+        // only when 16 of the smaller ones cannot hold a row
+        C = (int)((V + 8191) / 8192);
+        if (C > kMaxCluster) C = (int)((V + 16383) / 16384);
+        if (want_cluster && C < 2) C = 2;
+    }
+    if (C < 1 || C > kMaxCluster) return false;
+    const int64_t chunk = round_up_int((V + C - 1) / C, vec);
+    int threads = (o && o->tune_threads) ? o->tune_threads : (chunk <= 8192 ? 256 : 512);
+    if (chunk > (int64_t)fused_capacity(dtype, threads)) {
+        if (o && o->tune_threads) return false;
+        threads = 512;
+        if (chunk > (int64_t)fused_capacity(dtype, threads)) return false;
+    }
+    const size_t stage_bytes = align_up((size_t)chunk * es, 128);
+    int stages = (o && o->tune_stages) ? o->tune_stages : (stage_bytes <= 40 * 1024 ? 3 : 2);
+    while (stages > 2 && stages * stage_bytes + 2048 > kSmemLimit) --stages;
+    if (stages * stage_bytes + 2048 > kSmemLimit) return false;
+    fp->threads = threads;
+    fp->cluster = C;
+    fp->chunk = (int)chunk;
+    fp->stages = stages;
+    fp->ctas_per_sm_cap = o ? o->tune_ctas_per_sm : 0;
+    return true;
+}
+
+int split_chunks(int64_t V, const ce_options* o) {
+    const int K = o ? o->num_vocab_chunks : 0;
+    if (K > 0) return (int)(K < V ? K : V);
+    return split_auto_chunks(V);
+}
+
+Plan make_plan(const Problem& p, const ce_options* o) {
+    Plan pl;
+    memset(&pl, 0, sizeof pl);
+    const int force = o ? o->force_path : CE_PATH_AUTO;
+    const bool aligned = fused_aligned(p) && p.V <= 0x7fffffffLL;
+    if (force == CE_PATH_TWO_STAGE || (force == CE_PATH_AUTO && !aligned)) {
+        pl.path = CE_PATH_TWO_STAGE;
+    } else if (!aligned) {
+        pl.path = -2;  // row / cluster forced on rows that are not 16-byte aligned
+        return pl;
+    } else if (plan_fused(p.dtype, p.V, o, force == CE_PATH_CLUSTER, &pl.fused)) {
+        pl.path = pl.fused.cluster == 1 ? CE_PATH_ROW : CE_PATH_CLUSTER;
+        if (force == CE_PATH_ROW && pl.path != CE_PATH_ROW) pl.path = -2;
+        if (force == CE_PATH_CLUSTER && pl.path != CE_PATH_CLUSTER) pl.path = -2;
+        return pl;
+    } else if (force == CE_PATH_AUTO) {
+        pl.path = CE_PATH_TWO_STAGE;
+    } else {
+        pl.path = -2;
+        return pl;
+    }
+    pl.split.chunks = split_chunks(p.V, o);
+    pl.split.chunk = (p.V + pl.split.chunks - 1) / pl.split.chunks;
+    return pl;
+}
+
+size_t workspace_need(int64_t N, int64_t V, const ce_options* o) {
+    const size_t rows = align_up((size_t)N * sizeof(float), 256);
+    const size_t parts = align_up((size_t)N * (size_t)split_chunks(V, o) * sizeof(float4), 256);
+    return kWsHeaderBytes + rows + parts;
+}
+
+ce_status check_common(const void* logits, int dtype, int layout, int64_t dim0, int64_t dim1,
+                       int64_t V, const int64_t* strides, const int64_t* targets,
+                       const int64_t* tstrides, float a, float* loss_out, void* ws,
+                       size_t ws_bytes, const ce_options* o) {
+    if (dtype < CE_F32 || dtype > CE_F16) return CE_ERR_UNSUPPORTED_DTYPE;
+    if (layout != CE_LAYOUT_BSV && layout != CE_LAYOUT_SBV) return CE_ERR_INVALID_ARG;
+    if (!logits || !targets || !loss_out || !ws || !strides || !tstrides) return CE_ERR_INVALID_ARG;
+    if (dim0 < 0 || dim1 < 0 || V < 1 || V > 0x7fffffffLL) return CE_ERR_INVALID_ARG;
+    if (!(a >= 0.f && a <= 1.f)) return CE_ERR_INVALID_ARG;
+    if (!opts_clean(o)) return CE_ERR_INVALID_ARG;
+    if (strides[2] != 1 || strides[0] < 0 || strides[1] < 0) return CE_ERR_BAD_STRIDE;
+    if (tstrides[0] < 0 || tstrides[1] < 0) return CE_ERR_BAD_STRIDE;
+    if (reinterpret_cast<uintptr_t>(ws) % 16) return CE_ERR_INVALID_ARG;
+    if (ws_bytes < workspace_need(dim0 * dim1, V, o)) return CE_ERR_WORKSPACE_TOO_SMALL;
+    return CE_OK;
+}
+
+ce_status run_pass(Problem& pb, const ce_options* o, float* loss_out, int64_t* n_out,
+                   void* ws, cudaStream_t s) {
+    Plan pl = make_plan(pb, o);
+    if (pl.path < 0) return CE_ERR_UNSUPPORTED_PATH;
+    char* w = static_cast<char*>(ws);
+    pb.err = reinterpret_cast<uint32_t*>(w + kWsErrOffset);
+    pb.n_dev = reinterpret_cast<int64_t*>(w + kWsCountOffset);
+    float* rows = reinterpret_cast<float*>(w + kWsHeaderBytes);
+    float4* parts = reinterpret_cast<float4*>(
+        w + kWsHeaderBytes + align_up((size_t)pb.N * sizeof(float), 256));
+    pb.loss_rows = pb.reduce ? rows : loss_out;
+
+    if (launch_count(pb, n_out, s) != cudaSuccess) return CE_ERR_LAUNCH;
+    cudaEvent_t eb = o ? static_cast<cudaEvent_t>(o->event_begin) : nullptr;
+    cudaEvent_t ee = o ? static_cast<cudaEvent_t>(o->event_end) : nullptr;
+    if (eb && cudaEventRecord(eb, s) != cudaSuccess) return CE_ERR_LAUNCH;
+    if (pb.N > 0) {
+        cudaError_t e = (pl.path == CE_PATH_TWO_STAGE) ? launch_split(pb, pl.split, parts, s)
+                                                       : launch_fused(pb, pl.fused, s);
+        if (e != cudaSuccess) return CE_ERR_LAUNCH;
+    }
+    if (ee && cudaEventRecord(ee, s) != cudaSuccess) return CE_ERR_LAUNCH;
+    if (pb.reduce && launch_reduce_mean(pb, loss_out, s) != cudaSuccess) return CE_ERR_LAUNCH;
+    return CE_OK;
+}
+
+// True when distinct rows never share an element: with the two row strides
+// sorted, the inner one spans at least a row of V and the outer one spans
+// every inner step.  (Sufficient, not necessary; covers contiguous, padded and
+// transposed layouts.)  Required of the in-place gradient pass.
+bool rows_disjoint(int64_t dim0, int64_t dim1, int64_t V, int64_t s0, int64_t s1) {
+    int64_t in_s = s1, in_n = dim1, out_s = s0, out_n = dim0;
+    if (in_n <= 1 || (out_n > 1 && s0 < s1)) {
+        in_s = s0; in_n = dim0; out_s = s1; out_n = dim1;
+    }
+    if (in_n > 1 && in_s < V) return false;
+    if (out_n > 1 && out_s < (in_n > 1 ? in_s * in_n : V)) return false;
+    return true;
+}
+
+void fill_problem(Problem& pb, const void* logits, int dtype, int64_t dim0, int64_t dim1,
+                  int64_t V, const int64_t* strides, const int64_t* targets, const int64_t* tstrides,
+                  float a, int64_t ignore_idx, int reduce) {
+    memset(&pb, 0, sizeof pb);
+    pb.logits = static_cast<char*>(const_cast<void*>(logits));
+    pb.dtype = dtype;
+    pb.es = elem_size(dtype);
+    pb.dim0 = dim0;
+    pb.dim1 = dim1;
+    pb.N = dim0 * dim1;
+    pb.V = V;
+    pb.s0 = strides[0];
+    pb.s1 = strides[1];
+    pb.targets = targets;
+    pb.ts0 = tstrides[0];
+    pb.ts1 = tstrides[1];
+    pb.a = a;
+    pb.ignore_idx = ignore_idx;
+    pb.reduce = reduce ? 1 : 0;
+}
+
+}  // namespace
+}  // namespace gbce
+
+using namespace gbce;
+
+extern "C" {
+
+size_t ce_workspace_bytes(int64_t dim0, int64_t dim1, int64_t V, ce_dtype dtype,
+                          const ce_options* opts) {
+    if (dim0 < 0 || dim1 < 0 || V < 1 || (int)dtype < CE_F32 || (int)dtype > CE_F16) return 0;
+    if (!opts_clean(opts)) return 0;
+    return workspace_need(dim0 * dim1, V, opts);
+}
+
+ce_status ce_fwd_bwd(void* logits, ce_dtype dtype, ce_layout layout, int64_t dim0, int64_t dim1,
+                     int64_t V, const int64_t strides[3], const int64_t* targets,
+                     const int64_t target_strides[2], float label_smoothing, int64_t ignore_idx,
+                     int reduce_loss, const float* dloss, float* loss_out, void* grad_inplace,
+                     int64_t* n_non_ignore_out, void* workspace, size_t workspace_bytes,
+                     const ce_options* opts, void* stream) {
+    ce_status st = check_common(logits, dtype, layout, dim0, dim1, V, strides, targets,
+                                target_strides, label_smoothing, loss_out, workspace,
+                                workspace_bytes, opts);
+    if (st != CE_OK) return st;
+    if (grad_inplace != logits) return CE_ERR_INVALID_ARG;
+    if (!rows_disjoint(dim0, dim1, V, strides[0], strides[1])) return CE_ERR_BAD_STRIDE;
+    Problem pb;
+    fill_problem(pb, logits, dtype, dim0, dim1, V, strides, targets, target_strides,
+                 label_smoothing, ignore_idx, reduce_loss);
+    pb.dloss = dloss;
+    pb.grad = true;
+    return run_pass(pb, opts, loss_out, n_non_ignore_out, workspace,
+                    static_cast<cudaStream_t>(stream));
+}
+
+ce_status ce_fwd_only(const void* logits, ce_dtype dtype, ce_layout layout, int64_t dim0,
+                      int64_t dim1, int64_t V, const int64_t strides[3], const int64_t* targets,
+                      const int64_t target_strides[2], float label_smoothing, int64_t ignore_idx,
+                      int reduce_loss, float* loss_out, float* lse_out, int64_t* n_non_ignore_out,
+                      void* workspace, size_t workspace_bytes, const ce_options* opts,
+                      void* stream) {
+    ce_status st = check_common(logits, dtype, layout, dim0, dim1, V, strides, targets,
+                                target_strides, label_smoothing, loss_out, workspace,
+                                workspace_bytes, opts);
+    if (st != CE_OK) return st;
+    Problem pb;
+    fill_problem(pb, logits, dtype, dim0, dim1, V, strides, targets, target_strides,
+                 label_smoothing, ignore_idx, reduce_loss);
+    pb.lse_out = lse_out;
+    pb.grad = false;
+    return run_pass(pb, opts, loss_out, n_non_ignore_out, workspace,
+                    static_cast<cudaStream_t>(stream));
+}
+
+ce_status ce_get_error(const void* workspace, void* stream, uint32_t* host_err) {
+    if (!workspace || !host_err) return CE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t v = 0;
+    if (cudaMemcpyAsync(&v, static_cast<const char*>(workspace) + kWsErrOffset, sizeof v,
+                        cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return CE_ERR_LAUNCH;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return CE_ERR_LAUNCH;
+    *host_err = v;
+    if (v & CE_DEVERR_TIMEOUT) return CE_ERR_DEVICE_TIMEOUT;
+    if (v & CE_DEVERR_TARGET_RANGE) return CE_ERR_TARGET_RANGE;
+    return CE_OK;
+}
+
+const char* ce_status_string(ce_status status) {
+    switch (status) {
+        case CE_OK: return "ok";
+        case CE_ERR_INVALID_ARG: return "invalid argument";
+        case CE_ERR_UNSUPPORTED_DTYPE: return "unsupported dtype";
+        case CE_ERR_BAD_STRIDE:
+            return "bad stride: the vocabulary stride must be 1, no stride negative, and (for the "
+                   "in-place gradient) no two rows may share memory";
+        case CE_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than ce_workspace_bytes()";
+        case CE_ERR_LAUNCH: return "a CUDA launch or runtime call failed";
+        case CE_ERR_TARGET_RANGE: return "a target outside [0, V) that is not ignore_idx";
+        case CE_ERR_DEVICE_TIMEOUT: return "a bounded wait inside a kernel gave up";
+        case CE_ERR_UNSUPPORTED_PATH: return "the forced path cannot run this shape";
+    }
+    return "unknown status";
+}
+
+int ce_plan_path(const void* logits, ce_dtype dtype, int64_t dim0, int64_t dim1, int64_t V,
+                 const int64_t strides[3], const ce_options* opts, int* chunks_out) {
+    if ((int)dtype < CE_F32 || (int)dtype > CE_F16 || !strides || V < 1 || dim0 < 0 || dim1 < 0)
+        return -1;
+    if (strides[2] != 1 || strides[0] < 0 || strides[1] < 0 || !opts_clean(opts)) return -1;
+    static const int64_t zero_t[2] = {0, 0};
+    Problem pb;
+    fill_problem(pb, logits, dtype, dim0, dim1, V, strides, nullptr, zero_t, 0.f, -100, 0);
+    Plan pl = make_plan(pb, opts);
+    if (pl.path < 0) return pl.path;
+    if (chunks_out)
+        *chunks_out = pl.path == CE_PATH_TWO_STAGE ? pl.split.chunks : pl.fused.cluster;
+    return pl.path;
+}
+
+}  // extern "C"

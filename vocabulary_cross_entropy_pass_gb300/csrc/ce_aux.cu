@@ -1,0 +1,90 @@
+// ce_aux.cu -- the small kernels around the main pass.
+//
+// ce_count_kernel: the ignore mask count n_non_ignore and the target range
+//   check.  TENPU "Parallel Cross Entropy (Triton)" issue #29 (section 7,
+//   "Known limitations") counts n_non_ignore on the host because atomic adds
+//   were unreliable there; here one CTA counts on the device with a
+//   fixed-order integer reduction, before the gradient pass needs dloss/n.
+// ce_mean_kernel: reduce_loss -- the mean of the per-row losses over the kept
+//   rows, summed in a fixed order (fixed per-thread strides, then a fixed
+//   butterfly and a fixed cross-warp order), so the result is bitwise the same
+//   on every run.
+#include "ce_device.cuh"
+#include "ce_internal.h"
+
+namespace gbce {
+namespace {
+
+constexpr int kAuxThreads = 1024;
+
+__global__ void __launch_bounds__(kAuxThreads)
+ce_count_kernel(const int64_t* __restrict__ targets, int64_t ts0, int64_t ts1, int64_t dim1,
+                int64_t N, int64_t V, int64_t ignore_idx, int64_t* n_ws, int64_t* n_out,
+                uint32_t* err) {
+    __shared__ long long s_n[kAuxThreads / 32];
+    __shared__ unsigned s_e[kAuxThreads / 32];
+    long long n = 0;
+    unsigned e = 0;
+    for (int64_t r = threadIdx.x; r < N; r += kAuxThreads) {
+        const int64_t i = r / dim1, j = r - i * dim1;
+        const int64_t y = targets[i * ts0 + j * ts1];
+        if (y == ignore_idx) continue;
+        ++n;
+        if (y < 0 || y >= V) e |= CE_DEVERR_TARGET_RANGE;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        n += __shfl_xor_sync(kFull, n, off);
+        e |= __shfl_xor_sync(kFull, e, off);
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) {
+        s_n[warp] = n;
+        s_e[warp] = e;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        long long tn = 0;
+        unsigned te = 0;
+        for (int w = 0; w < kAuxThreads / 32; ++w) {
+            tn += s_n[w];
+            te |= s_e[w];
+        }
+        *n_ws = tn;
+        if (n_out) *n_out = tn;
+        *err = te;  // starts the error word of this pass
+    }
+}
+
+__global__ void __launch_bounds__(kAuxThreads)
+ce_mean_kernel(const float* __restrict__ loss_rows, int64_t N, const int64_t* n_dev, float* out) {
+    __shared__ double s_sum[kAuxThreads / 32];
+    double acc = 0.0;
+    for (int64_t r = threadIdx.x; r < N; r += kAuxThreads) acc += (double)loss_rows[r];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(kFull, acc, off);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) s_sum[warp] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double t = 0.0;
+        for (int w = 0; w < kAuxThreads / 32; ++w) t += s_sum[w];
+        const long long n = *n_dev;
+        out[0] = (float)(t / (double)n);  // 0/0 = NaN when every row is ignored
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_count(const Problem& p, int64_t* n_out, cudaStream_t s) {
+    ce_count_kernel<<<1, kAuxThreads, 0, s>>>(p.targets, p.ts0, p.ts1, p.dim1, p.N, p.V,
+                                              p.ignore_idx, p.n_dev, n_out, p.err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_reduce_mean(const Problem& p, float* loss_out, cudaStream_t s) {
+    ce_mean_kernel<<<1, kAuxThreads, 0, s>>>(p.loss_rows, p.N, p.n_dev, loss_out);
+    return cudaGetLastError();
+}
+
+}  // namespace gbce

@@ -1,0 +1,69 @@
+// ce_internal.h -- host-side structures shared by the C-ABI layer and the
+// kernel launchers of libgbce.  Not part of the public interface.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/ce.h"
+
+namespace gbce {
+
+// Workspace layout (byte offsets from the caller's workspace pointer):
+//   [0, 4)      uint32 device error word
+//   [8, 16)     int64 n_non_ignore of the last pass
+//   [256, ...)  float per-row losses (N) -- used when reduce_loss
+//   [...]       float4 per-(row, chunk) partials of the two-stage path
+constexpr size_t kWsErrOffset = 0;
+constexpr size_t kWsCountOffset = 8;
+constexpr size_t kWsHeaderBytes = 256;
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Problem {
+    char* logits;              // byte address of element (0,0,0)
+    int dtype;                 // ce_dtype
+    int es;                    // element size in bytes
+    int64_t dim0, dim1, N, V;
+    int64_t s0, s1;            // element strides of dims 0 and 1
+    const int64_t* targets;
+    int64_t ts0, ts1;
+    float a;                   // label smoothing
+    int64_t ignore_idx;
+    int reduce;
+    const float* dloss;
+    float* loss_rows;          // per-row loss destination (loss_out or workspace)
+    float* lse_out;            // optional
+    bool grad;                 // write the gradient in place
+    uint32_t* err;             // device error word
+    int64_t* n_dev;            // device count
+};
+
+// Plan of the fused (row / cluster) kernel.
+struct FusedPlan {
+    int threads;               // 256 or 512
+    int cluster;               // CTAs per row (1 = row path)
+    int chunk;                 // elements per CTA slice, multiple of the 16-byte vector
+    int stages;                // TMA pipeline depth
+    int ctas_per_sm_cap;       // 0 = no cap
+};
+
+// Plan of the two-stage kernels.
+struct SplitPlan {
+    int chunks;                // K
+    int64_t chunk;             // elements per chunk (ceil(V/K))
+};
+
+int elem_size(int dtype);
+bool fused_aligned(const Problem& p);
+int fused_capacity(int dtype, int threads);  // elements one CTA can hold
+int split_auto_chunks(int64_t V);
+
+cudaError_t launch_count(const Problem& p, int64_t* n_out, cudaStream_t s);
+cudaError_t launch_reduce_mean(const Problem& p, float* loss_out, cudaStream_t s);
+cudaError_t launch_fused(const Problem& p, const FusedPlan& plan, cudaStream_t s);
+cudaError_t launch_split(const Problem& p, const SplitPlan& plan, float4* partials,
+                         cudaStream_t s);
+
+}  // namespace gbce

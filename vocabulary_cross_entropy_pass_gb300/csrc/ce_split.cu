@@ -1,0 +1,209 @@
+// ce_split.cu -- the two-stage split-vocabulary path.
+//
+// Stage 1 (ce_split_stats_kernel): one CTA per (row, chunk) computes the
+// chunk's (max, sum-exp, sum, target logit) partial and writes it to the
+// workspace.  Stage 2 (ce_split_grad_kernel): one CTA per (row, chunk)
+// combines the row's K partials in chunk order -- the MAX all-reduce, SUM
+// all-reduce and target gather that mindspore/hyper-parallel #269 (section
+// 3.1) runs between vocabulary-parallel ranks, with the uneven ceil(V/K)
+// split it describes -- then rereads its chunk and writes the gradient in
+// place.  The kernel boundary orders every read of a row before any write.
+//
+// This path takes any alignment and any row strides (scalar element loads);
+// the row and cluster paths need 16-byte aligned rows.  It reads the logits
+// twice, so it is the fallback, and the forced second implementation of the
+// vocabulary-split workloads.
+#include "ce_device.cuh"
+#include "ce_internal.h"
+
+namespace gbce {
+namespace {
+
+constexpr int kSplitThreads = 256;
+constexpr int kSplitWarps = kSplitThreads / 32;
+
+struct SplitArgs {
+    char* logits;
+    int64_t s0, s1, dim1, N, V, chunk;
+    int K;
+    const int64_t* targets;
+    int64_t ts0, ts1, ignore_idx;
+    float a, a_over_v;
+    int reduce;
+    const float* dloss;
+    float* loss;
+    float* lse_out;
+    const int64_t* n_dev;
+    float4* part;  // [N][K]
+};
+
+__device__ __forceinline__ void row_of(const SplitArgs& p, int64_t r, int64_t& y, int64_t& off) {
+    const int64_t i = r / p.dim1, j = r - i * p.dim1;
+    y = p.targets[i * p.ts0 + j * p.ts1];
+    off = i * p.s0 + j * p.s1;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kSplitThreads) ce_split_stats_kernel(const __grid_constant__ SplitArgs p) {
+    using VT = Vec<T>;
+    __shared__ float s_red[kSplitWarps];
+    __shared__ float4 s_part[kSplitWarps];
+    const int64_t b = blockIdx.x;
+    const int64_t r = b / p.K;
+    const int k = (int)(b - r * p.K);
+    int64_t y, off;
+    row_of(p, r, y, off);
+    if (y == p.ignore_idx || y < 0 || y >= p.V) return;
+    const int64_t k0 = (int64_t)k * p.chunk;
+    const int64_t k1 = min(p.V, k0 + p.chunk);
+    const char* row = p.logits + off * (int64_t)sizeof(T);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+    float m = -INFINITY;
+    for (int64_t v = k0 + threadIdx.x; v < k1; v += kSplitThreads)
+        m = fmaxf(m, VT::load1(row + v * (int64_t)sizeof(T)));
+    m = warp_allmax(m);
+    if (lane == 0) s_red[warp] = m;
+    __syncthreads();
+    m = -INFINITY;
+    for (int w = 0; w < kSplitWarps; ++w) m = fmaxf(m, s_red[w]);
+    const float ml = (m == -INFINITY) ? 0.f : m * kLog2e;
+
+    float d = 0.f, S = 0.f;
+    for (int64_t v = k0 + threadIdx.x; v < k1; v += kSplitThreads) {
+        const float x = VT::load1(row + v * (int64_t)sizeof(T));
+        d += ex2_approx(fmaf(x, kLog2e, -ml));
+        S += x;
+    }
+    d = warp_allsum(d);
+    S = warp_allsum(S);
+    if (lane == 0) s_part[warp] = make_float4(0.f, d, S, 0.f);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float td = 0.f, tS = 0.f;
+        for (int w = 0; w < kSplitWarps; ++w) {
+            td += s_part[w].y;
+            tS += s_part[w].z;
+        }
+        const float xy = (y >= k0 && y < k1) ? VT::load1(row + y * (int64_t)sizeof(T)) : 0.f;
+        p.part[r * p.K + k] = make_float4(m, td, tS, xy);
+    }
+}
+
+template <typename T, bool GRAD>
+__global__ void __launch_bounds__(kSplitThreads) ce_split_grad_kernel(const __grid_constant__ SplitArgs p) {
+    using VT = Vec<T>;
+    __shared__ float s_lse, s_S, s_xy;
+    const int kper = GRAD ? p.K : 1;  // without a gradient one CTA per row
+    const int64_t b = blockIdx.x;
+    const int64_t r = b / kper;
+    const int k = (int)(b - r * kper);
+    int64_t y, off;
+    row_of(p, r, y, off);
+    const int64_t k0 = (int64_t)k * p.chunk;
+    const int64_t k1 = min(p.V, k0 + p.chunk);
+    char* row = p.logits + off * (int64_t)sizeof(T);
+
+    if (y == p.ignore_idx || y < 0 || y >= p.V) {
+        if (GRAD)
+            for (int64_t v = k0 + threadIdx.x; v < k1; v += kSplitThreads)
+                VT::store1(row + v * (int64_t)sizeof(T), 0.f);
+        if (k == 0 && threadIdx.x == 0) {
+            p.loss[r] = (y == p.ignore_idx) ? 0.f : __int_as_float(0x7fc00000);
+            if (p.lse_out) p.lse_out[r] = __int_as_float(0x7fc00000);
+        }
+        return;
+    }
+
+    if (threadIdx.x == 0) {
+        // combine the K partials in chunk order
+        Part G = part_identity();
+        const float4* pr = p.part + r * p.K;
+        for (int q = 0; q < p.K; ++q) {
+            const float4 w = pr[q];
+            G = part_combine(G, Part{w.x, w.y, w.z});
+        }
+        const float lse = G.m + logf(G.d);
+        s_lse = lse;
+        s_S = G.S;
+        s_xy = pr[y / p.chunk].w;
+        if (k == 0) {
+            p.loss[r] = lse - (1.f - p.a) * pr[y / p.chunk].w - p.a_over_v * G.S;
+            if (p.lse_out) p.lse_out[r] = lse;
+        }
+    }
+    if (!GRAD) return;
+    __syncthreads();
+    const float lse = s_lse;
+    float g;
+    if (p.reduce)
+        g = (p.dloss ? p.dloss[0] : 1.f) / (float)(*p.n_dev);
+    else
+        g = p.dloss ? p.dloss[r] : 1.f;
+    const float bb = g * p.a_over_v;
+    const float lsel = lse * kLog2e;
+    for (int64_t v = k0 + threadIdx.x; v < k1; v += kSplitThreads) {
+        const float x = VT::load1(row + v * (int64_t)sizeof(T));
+        float o = fmaf(ex2_approx(fmaf(x, kLog2e, -lsel)), g, -bb);
+        if (v == y) o -= g * (1.f - p.a);
+        VT::store1(row + v * (int64_t)sizeof(T), o);
+    }
+}
+
+template <typename T>
+cudaError_t launch_split_typed(const Problem& pb, const SplitPlan& plan, float4* partials,
+                               cudaStream_t s) {
+    SplitArgs a;
+    a.logits = pb.logits;
+    a.s0 = pb.s0;
+    a.s1 = pb.s1;
+    a.dim1 = pb.dim1;
+    a.N = pb.N;
+    a.V = pb.V;
+    a.chunk = plan.chunk;
+    a.K = plan.chunks;
+    a.targets = pb.targets;
+    a.ts0 = pb.ts0;
+    a.ts1 = pb.ts1;
+    a.ignore_idx = pb.ignore_idx;
+    a.a = pb.a;
+    a.a_over_v = pb.a / (float)pb.V;
+    a.reduce = pb.reduce;
+    a.dloss = pb.dloss;
+    a.loss = pb.loss_rows;
+    a.lse_out = pb.lse_out;
+    a.n_dev = pb.n_dev;
+    a.part = partials;
+    const int64_t blocks = pb.N * plan.chunks;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    ce_split_stats_kernel<T><<<(unsigned)blocks, kSplitThreads, 0, s>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (pb.grad)
+        ce_split_grad_kernel<T, true><<<(unsigned)blocks, kSplitThreads, 0, s>>>(a);
+    else
+        ce_split_grad_kernel<T, false><<<(unsigned)pb.N, kSplitThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int split_auto_chunks(int64_t V) {
+    int64_t k = (V + 4095) / 4096;  // about 16 elements per thread
+    if (k < 1) k = 1;
+    if (k > 4096) k = 4096;
+    return (int)k;
+}
+
+cudaError_t launch_split(const Problem& p, const SplitPlan& plan, float4* partials, cudaStream_t s) {
+    switch (p.dtype) {
+        case CE_F32:
+            return launch_split_typed<float>(p, plan, partials, s);
+        case CE_BF16:
+            return launch_split_typed<__nv_bfloat16>(p, plan, partials, s);
+        default:
+            return launch_split_typed<__half>(p, plan, partials, s);
+    }
+}
+
+}  // namespace gbce
