@@ -263,8 +263,13 @@ def run_ours(args, w, rank: int, world: int, dist) -> None:
     # per-launch events around the main kernel, on the launching stream
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
+    for (b, e) in evs:  # torch creates an event on its first record
+        b.record(stream)
+        e.record(stream)
+    torch.cuda.synchronize(dev)
     step_opts = [pkg.make_options(event_begin=b.cuda_event, event_end=e.cuda_event)
                  for (b, e) in evs]
+    assert all(o.event_begin and o.event_end for o in step_opts)
 
     gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     sampler = ClockSampler(gpu_id)

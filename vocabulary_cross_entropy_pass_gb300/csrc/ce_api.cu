@@ -120,12 +120,17 @@ size_t workspace_need(int64_t N, int64_t V, const ce_options* o) {
 
 ce_status check_common(const void* logits, int dtype, int layout, int64_t dim0, int64_t dim1,
                        int64_t V, const int64_t* strides, const int64_t* targets,
-                       const int64_t* tstrides, float a, float* loss_out, void* ws,
+                       const int64_t* tstrides, float a, int reduce, float* loss_out, void* ws,
                        size_t ws_bytes, const ce_options* o) {
     if (dtype < CE_F32 || dtype > CE_F16) return CE_ERR_UNSUPPORTED_DTYPE;
     if (layout != CE_LAYOUT_BSV && layout != CE_LAYOUT_SBV) return CE_ERR_INVALID_ARG;
-    if (!logits || !targets || !loss_out || !ws || !strides || !tstrides) return CE_ERR_INVALID_ARG;
+    if (!ws || !strides || !tstrides) return CE_ERR_INVALID_ARG;
     if (dim0 < 0 || dim1 < 0 || V < 1 || V > 0x7fffffffLL) return CE_ERR_INVALID_ARG;
+    // with no rows the logits, targets and per-row losses may be empty (NULL);
+    // a mean still needs its one output value
+    const bool empty = dim0 * dim1 == 0;
+    if (!empty && (!logits || !targets || !loss_out)) return CE_ERR_INVALID_ARG;
+    if (empty && reduce && !loss_out) return CE_ERR_INVALID_ARG;
     if (!(a >= 0.f && a <= 1.f)) return CE_ERR_INVALID_ARG;
     if (!opts_clean(o)) return CE_ERR_INVALID_ARG;
     if (strides[2] != 1 || strides[0] < 0 || strides[1] < 0) return CE_ERR_BAD_STRIDE;
@@ -217,8 +222,8 @@ ce_status ce_fwd_bwd(void* logits, ce_dtype dtype, ce_layout layout, int64_t dim
                      int64_t* n_non_ignore_out, void* workspace, size_t workspace_bytes,
                      const ce_options* opts, void* stream) {
     ce_status st = check_common(logits, dtype, layout, dim0, dim1, V, strides, targets,
-                                target_strides, label_smoothing, loss_out, workspace,
-                                workspace_bytes, opts);
+                                target_strides, label_smoothing, reduce_loss, loss_out,
+                                workspace, workspace_bytes, opts);
     if (st != CE_OK) return st;
     if (grad_inplace != logits) return CE_ERR_INVALID_ARG;
     if (!rows_disjoint(dim0, dim1, V, strides[0], strides[1])) return CE_ERR_BAD_STRIDE;
@@ -238,8 +243,8 @@ ce_status ce_fwd_only(const void* logits, ce_dtype dtype, ce_layout layout, int6
                       void* workspace, size_t workspace_bytes, const ce_options* opts,
                       void* stream) {
     ce_status st = check_common(logits, dtype, layout, dim0, dim1, V, strides, targets,
-                                target_strides, label_smoothing, loss_out, workspace,
-                                workspace_bytes, opts);
+                                target_strides, label_smoothing, reduce_loss, loss_out,
+                                workspace, workspace_bytes, opts);
     if (st != CE_OK) return st;
     Problem pb;
     fill_problem(pb, logits, dtype, dim0, dim1, V, strides, targets, target_strides,
