@@ -34,7 +34,7 @@ if ROOT not in sys.path:
 
 METRIC = "CE fwd+bwd tokens/s at V=128000 bf16; achieved HBM GB/s vs GB300 peak"
 DEFAULT_WORKLOAD = "c5t_bsv128000_bf16"
-KERNELS_PER_STEP = {1: 3, 2: 3, 3: 4}   # count + main (+ second stage) + mean
+KERNELS_PER_STEP = {1: 3, 2: 3, 3: 4, 4: 3}   # count + main (+ second stage) + mean
 CLOCK_FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
                 "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
                 "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
@@ -244,7 +244,10 @@ def run_ours(args, w, rank: int, world: int, dist) -> None:
     x = x_host.to(dev, non_blocking=True)
     t = t_host.to(dev, non_blocking=True)
     loss = torch.empty(1, dtype=torch.float32, device=dev)
-    opts = pkg.make_options()
+    tune = dict(force_path=args.force_path, num_vocab_chunks=args.chunks,
+                tune_threads=args.tune_threads, tune_stages=args.tune_stages,
+                tune_ctas_per_sm=args.tune_ctas_per_sm, tune_l2_keep=args.tune_l2_keep)
+    opts = pkg.make_options(**tune)
     ws = torch.empty(pkg.ce_workspace_bytes(w.dim0, w.dim1, w.V, x.dtype, opts),
                      dtype=torch.uint8, device=dev)
     path, chunks = pkg.ce_plan_path(x, opts)
@@ -267,7 +270,7 @@ def run_ours(args, w, rank: int, world: int, dist) -> None:
         b.record(stream)
         e.record(stream)
     torch.cuda.synchronize(dev)
-    step_opts = [pkg.make_options(event_begin=b.cuda_event, event_end=e.cuda_event)
+    step_opts = [pkg.make_options(event_begin=b.cuda_event, event_end=e.cuda_event, **tune)
                  for (b, e) in evs]
     assert all(o.event_begin and o.event_end for o in step_opts)
 
@@ -340,7 +343,7 @@ def run_ours(args, w, rank: int, world: int, dist) -> None:
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded, see vocabulary_cross_entropy_pass_gb300/workloads.py)",
-        "config": config_of(w, args) | {"path": {1: "row", 2: "cluster", 3: "two_stage"}[path],
+        "config": config_of(w, args) | {"path": {1: "row", 2: "cluster", 3: "two_stage", 4: "stream"}[path],
                                          "vocab_chunks": chunks},
         "hbm_gbs_formula": nbytes * args.steps * world / (ms / 1e3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
@@ -368,6 +371,13 @@ def main(argv=None) -> int:
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--ref-rows", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    # planner overrides, for tuning sweeps (defaults: the planner's choice)
+    ap.add_argument("--force-path", type=int, default=0)
+    ap.add_argument("--chunks", type=int, default=0)
+    ap.add_argument("--tune-threads", type=int, default=0)
+    ap.add_argument("--tune-stages", type=int, default=0)
+    ap.add_argument("--tune-ctas-per-sm", type=int, default=0)
+    ap.add_argument("--tune-l2-keep", type=int, default=0)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -91,7 +91,9 @@ typedef enum {
     CE_PATH_AUTO = 0,
     CE_PATH_ROW = 1,       /* one CTA holds a whole row in shared memory and registers */
     CE_PATH_CLUSTER = 2,   /* a thread-block cluster splits each row; combine over DSMEM */
-    CE_PATH_TWO_STAGE = 3  /* per-chunk statistics kernel, then combine + gradient kernel */
+    CE_PATH_TWO_STAGE = 3, /* per-chunk statistics kernel, then combine + gradient kernel */
+    CE_PATH_STREAM = 4     /* one CTA streams whole rows twice through a TMA ring; the
+                              second read of a row is served by L2 */
 } ce_path;
 
 typedef struct {
@@ -103,10 +105,14 @@ typedef struct {
     void* event_begin;      /* cudaEvent_t or NULL: recorded on `stream` right
                                before the main kernel of the pass */
     void* event_end;        /* cudaEvent_t or NULL: recorded right after it */
-    int tune_threads;       /* 0 = default; otherwise CTA size (256 or 512) */
-    int tune_stages;        /* 0 = default; otherwise TMA pipeline depth (2..4) */
+    int tune_threads;       /* 0 = default; otherwise CTA size (256 or 512; on the stream
+                               path the number of consuming threads) */
+    int tune_stages;        /* 0 = default; otherwise TMA pipeline depth (2..4 rows on the
+                               row/cluster paths, 2..8 tiles on the stream path) */
     int tune_ctas_per_sm;   /* 0 = as many as fit; otherwise a cap */
-    int reserved[5];        /* must be zero */
+    int tune_l2_keep;       /* stream path: 0 = default, 1 = first read asks L2 to keep
+                               the row (evict-last), 2 = it does not (evict-first) */
+    int reserved[4];        /* must be zero */
 } ce_options;
 
 /* Bytes of device workspace a call with these sizes needs (either entry
@@ -162,7 +168,7 @@ ce_status ce_get_error(const void* workspace, void* stream, uint32_t* host_err);
 const char* ce_status_string(ce_status status);
 
 /* Path the planner would take for these arguments (host only): CE_PATH_ROW,
- * CE_PATH_CLUSTER or CE_PATH_TWO_STAGE, with the vocabulary chunk count in
+ * CE_PATH_CLUSTER, CE_PATH_TWO_STAGE or CE_PATH_STREAM, with the vocabulary chunk count in
  * *chunks_out (host pointer, may be NULL).  Returns -1 for arguments
  * ce_fwd_bwd would reject, -2 for a forced path that cannot run them. */
 int ce_plan_path(const void* logits, ce_dtype dtype, int64_t dim0, int64_t dim1, int64_t V,

@@ -97,6 +97,10 @@ def test_host_validation_rejects_before_launch(lib):
     assert _call(lib, opts=ctypes.byref(o)) == 1
     o = _lib.make_options(tune_threads=300)
     assert _call(lib, opts=ctypes.byref(o)) == 1
+    o = _lib.make_options(tune_l2_keep=3)
+    assert _call(lib, opts=ctypes.byref(o)) == 1
+    o = _lib.make_options(force_path=5)
+    assert _call(lib, opts=ctypes.byref(o)) == 1
 
 
 def test_planner(lib):
@@ -109,15 +113,20 @@ def test_planner(lib):
         return p, ch.value
     assert plan(4096) == (1, 1)
     assert plan(8192) == (1, 1)
-    assert plan(32000) == (2, 4)
-    assert plan(128000) == (2, 16)
-    assert plan(128000, dtype=0) == (2, 16)
+    assert plan(32000) == (4, 1)                   # wider than one CTA: stream path
+    assert plan(128000) == (4, 1)
+    assert plan(128000, dtype=0) == (4, 1)
+    assert plan(128000, force_path=2) == (2, 16)
+    assert plan(32000, force_path=2) == (2, 4)
+    assert plan(4096, force_path=4) == (4, 1)
+    assert plan(4095, force_path=4)[0] == -2       # the stream path needs aligned rows too
     assert plan(65536, num_vocab_chunks=8, force_path=2) == (2, 8)
     assert plan(65536, num_vocab_chunks=8, force_path=3) == (3, 8)
     assert plan(4095)[0] == 3                      # rows not 16-byte aligned
     assert plan(4096, base=0x1002)[0] == 3         # base not 16-byte aligned
     assert plan(4096, force_path=1, base=0x1002)[0] == -2
-    assert plan(4_000_000)[0] == 3                 # too wide for 16 CTAs
+    assert plan(4_000_000)[0] == 4                 # any width streams
+    assert plan(4_000_000, force_path=2)[0] == -2  # too wide for 16 CTAs
     assert plan(32000, force_path=1)[0] == -2      # one CTA cannot hold the row
     assert plan(4096, force_path=2) == (2, 2)
 

@@ -50,7 +50,8 @@ def test_small_and_unaligned_vocab(dtype, V):
         _compare(w, x, t, loss, xd, n)
 
 
-@pytest.mark.parametrize("dtype,pad", [("bf16", 8), ("bf16", 3), ("f32", 4), ("f16", 16)])
+@pytest.mark.parametrize("dtype,pad", [("bf16", 8), ("bf16", 3), ("f32", 4), ("f16", 16),
+                                       ("bf16", 32000)])
 def test_padded_rows(dtype, pad):
     w = wl.Workload("pad", 2, 5, 4000, dtype, sigma=2.0, label_smoothing=0.1, seed=31)
     x = wl.logits(w)
@@ -105,7 +106,7 @@ def test_empty_chunks():
     harness.run_gpu_vs_oracle(w, force_path=2, num_vocab_chunks=16)
 
 
-@pytest.mark.parametrize("path", [0, 3])
+@pytest.mark.parametrize("path", [0, 3, 4])
 def test_all_ignored_mean_is_nan(path):
     x = torch.randn(3, 4, 1024, device=DEV).to(torch.bfloat16)
     t = torch.full((3, 4), -100, dtype=torch.int64, device=DEV)
@@ -115,7 +116,7 @@ def test_all_ignored_mean_is_nan(path):
     assert torch.all(x == 0)
 
 
-@pytest.mark.parametrize("path", [0, 2, 3])
+@pytest.mark.parametrize("path", [0, 2, 3, 4])
 def test_out_of_range_target_sets_error(path):
     w = wl.Workload("oor", 1, 6, 8192, "bf16", sigma=2.0, ignore_frac=0.0, seed=71)
     x = wl.logits(w)
@@ -162,7 +163,8 @@ def test_zero_rows():
 
 
 @pytest.mark.parametrize("name,path", [("c5_bsv128000_bf16_ls", 0), ("c3_bsv32000_bf16_spiked", 0),
-                                       ("c2_sbv8192_bf16", 0), ("c4_bsv65536_bf16_split8", 3)])
+                                       ("c2_sbv8192_bf16", 0), ("c4_bsv65536_bf16_split8", 3),
+                                       ("c5_bsv128000_bf16_ls", 2)])
 def test_fwd_only_matches(name, path):
     w = wl.WORKLOADS[name]
     x = wl.logits(w)

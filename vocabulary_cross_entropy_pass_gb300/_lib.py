@@ -16,7 +16,7 @@ LIB_PATH = os.path.join(HERE, "libgbce.so")
 
 CE_F32, CE_BF16, CE_F16 = 0, 1, 2
 CE_LAYOUT_BSV, CE_LAYOUT_SBV = 0, 1
-CE_PATH_AUTO, CE_PATH_ROW, CE_PATH_CLUSTER, CE_PATH_TWO_STAGE = 0, 1, 2, 3
+CE_PATH_AUTO, CE_PATH_ROW, CE_PATH_CLUSTER, CE_PATH_TWO_STAGE, CE_PATH_STREAM = 0, 1, 2, 3, 4
 CE_DEVERR_TARGET_RANGE, CE_DEVERR_TIMEOUT = 0x1, 0x2
 
 STATUS = {
@@ -45,7 +45,8 @@ class ce_options(ctypes.Structure):
         ("tune_threads", ctypes.c_int),
         ("tune_stages", ctypes.c_int),
         ("tune_ctas_per_sm", ctypes.c_int),
-        ("reserved", ctypes.c_int * 5),
+        ("tune_l2_keep", ctypes.c_int),
+        ("reserved", ctypes.c_int * 4),
     ]
 
 
@@ -97,7 +98,8 @@ def i64_array(vals):
 
 
 def make_options(force_path: int = 0, num_vocab_chunks: int = 0, event_begin=None, event_end=None,
-                 tune_threads: int = 0, tune_stages: int = 0, tune_ctas_per_sm: int = 0):
+                 tune_threads: int = 0, tune_stages: int = 0, tune_ctas_per_sm: int = 0,
+                 tune_l2_keep: int = 0):
     o = ce_options()
     o.force_path = force_path
     o.num_vocab_chunks = num_vocab_chunks
@@ -106,4 +108,5 @@ def make_options(force_path: int = 0, num_vocab_chunks: int = 0, event_begin=Non
     o.tune_threads = tune_threads
     o.tune_stages = tune_stages
     o.tune_ctas_per_sm = tune_ctas_per_sm
+    o.tune_l2_keep = tune_l2_keep
     return o

@@ -25,22 +25,34 @@ constexpr int kMaxCluster = 16;
 constexpr size_t kSmemLimit = 227 * 1024;
 
 struct Plan {
-    int path;  // CE_PATH_ROW / CLUSTER / TWO_STAGE, or < 0 on error
+    int path;  // CE_PATH_ROW / CLUSTER / TWO_STAGE / STREAM, or < 0 on error
     FusedPlan fused;
     SplitPlan split;
+    StreamPlan stream;
 };
+
+// Row-streaming kernel: tiles of threads*64 bytes, `stages` of them in flight.
+bool plan_stream(const ce_options* o, StreamPlan* sp) {
+    sp->threads = (o && o->tune_threads) ? o->tune_threads : 256;
+    sp->stages = (o && o->tune_stages) ? o->tune_stages : 6;
+    sp->ctas_per_sm_cap = o ? o->tune_ctas_per_sm : 0;
+    sp->l2_keep = (o && o->tune_l2_keep == 2) ? 0 : 1;
+    const size_t tile = (size_t)sp->threads * 64;
+    return sp->stages * tile + 1024 <= kSmemLimit;
+}
 
 int round_up_int(int64_t x, int64_t m) { return (int)((x + m - 1) / m * m); }
 
 bool opts_clean(const ce_options* o) {
     if (!o) return true;
-    for (int i = 0; i < 5; ++i)
+    for (int i = 0; i < 4; ++i)
         if (o->reserved[i] != 0) return false;
-    if (o->force_path < 0 || o->force_path > CE_PATH_TWO_STAGE) return false;
+    if (o->force_path < 0 || o->force_path > CE_PATH_STREAM) return false;
     if (o->num_vocab_chunks < 0) return false;
     if (o->tune_threads != 0 && o->tune_threads != 256 && o->tune_threads != 512) return false;
-    if (o->tune_stages < 0 || o->tune_stages > 4 || o->tune_stages == 1) return false;
+    if (o->tune_stages < 0 || o->tune_stages > 8 || o->tune_stages == 1) return false;
     if (o->tune_ctas_per_sm < 0) return false;
+    if (o->tune_l2_keep < 0 || o->tune_l2_keep > 2) return false;
     return true;
 }
 
@@ -70,6 +82,7 @@ bool plan_fused(int dtype, int64_t V, const ce_options* o, bool want_cluster, Fu
     }
     const size_t stage_bytes = align_up((size_t)chunk * es, 128);
     int stages = (o && o->tune_stages) ? o->tune_stages : (stage_bytes <= 40 * 1024 ? 3 : 2);
+    if (stages > 4) return false;
     while (stages > 2 && stages * stage_bytes + 2048 > kSmemLimit) --stages;
     if (stages * stage_bytes + 2048 > kSmemLimit) return false;
     fp->threads = threads;
@@ -91,6 +104,19 @@ Plan make_plan(const Problem& p, const ce_options* o) {
     memset(&pl, 0, sizeof pl);
     const int force = o ? o->force_path : CE_PATH_AUTO;
     const bool aligned = fused_aligned(p) && p.V <= 0x7fffffffLL;
+    const int K = o ? o->num_vocab_chunks : 0;
+    // Rows wider than one CTA's registers go through the stream kernel unless
+    // a vocabulary split is asked for.
+    const bool stream_auto = force == CE_PATH_AUTO && aligned && K == 0 &&
+                             p.V > (int64_t)fused_capacity(p.dtype, 256);
+    if (force == CE_PATH_STREAM || stream_auto) {
+        if (!aligned || !plan_stream(o, &pl.stream)) {
+            pl.path = -2;
+            return pl;
+        }
+        pl.path = CE_PATH_STREAM;
+        return pl;
+    }
     if (force == CE_PATH_TWO_STAGE || (force == CE_PATH_AUTO && !aligned)) {
         pl.path = CE_PATH_TWO_STAGE;
     } else if (!aligned) {
@@ -157,8 +183,13 @@ ce_status run_pass(Problem& pb, const ce_options* o, float* loss_out, int64_t* n
     cudaEvent_t ee = o ? static_cast<cudaEvent_t>(o->event_end) : nullptr;
     if (eb && cudaEventRecord(eb, s) != cudaSuccess) return CE_ERR_LAUNCH;
     if (pb.N > 0) {
-        cudaError_t e = (pl.path == CE_PATH_TWO_STAGE) ? launch_split(pb, pl.split, parts, s)
-                                                       : launch_fused(pb, pl.fused, s);
+        cudaError_t e;
+        if (pl.path == CE_PATH_TWO_STAGE)
+            e = launch_split(pb, pl.split, parts, s);
+        else if (pl.path == CE_PATH_STREAM)
+            e = launch_stream(pb, pl.stream, s);
+        else
+            e = launch_fused(pb, pl.fused, s);
         if (e != cudaSuccess) return CE_ERR_LAUNCH;
     }
     if (ee && cudaEventRecord(ee, s) != cudaSuccess) return CE_ERR_LAUNCH;
@@ -297,7 +328,9 @@ int ce_plan_path(const void* logits, ce_dtype dtype, int64_t dim0, int64_t dim1,
     Plan pl = make_plan(pb, opts);
     if (pl.path < 0) return pl.path;
     if (chunks_out)
-        *chunks_out = pl.path == CE_PATH_TWO_STAGE ? pl.split.chunks : pl.fused.cluster;
+        *chunks_out = pl.path == CE_PATH_TWO_STAGE ? pl.split.chunks
+                      : pl.path == CE_PATH_STREAM  ? 1
+                                                   : pl.fused.cluster;
     return pl.path;
 }
 

@@ -49,6 +49,14 @@ struct FusedPlan {
     int ctas_per_sm_cap;       // 0 = no cap
 };
 
+// Plan of the row-streaming kernel.
+struct StreamPlan {
+    int threads;               // consumer threads: 256 (4 vectors each) or 512 (2 each)
+    int stages;                // ring depth (tiles of threads*64 bytes)
+    int ctas_per_sm_cap;       // 0 = no cap
+    int l2_keep;               // 1: first-pass copies use an L2 evict-last policy
+};
+
 // Plan of the two-stage kernels.
 struct SplitPlan {
     int chunks;                // K
@@ -63,6 +71,7 @@ int split_auto_chunks(int64_t V);
 cudaError_t launch_count(const Problem& p, int64_t* n_out, cudaStream_t s);
 cudaError_t launch_reduce_mean(const Problem& p, float* loss_out, cudaStream_t s);
 cudaError_t launch_fused(const Problem& p, const FusedPlan& plan, cudaStream_t s);
+cudaError_t launch_stream(const Problem& p, const StreamPlan& plan, cudaStream_t s);
 cudaError_t launch_split(const Problem& p, const SplitPlan& plan, float4* partials,
                          cudaStream_t s);
 
