@@ -110,8 +110,8 @@ typedef struct {
     int tune_stages;        /* 0 = default; otherwise TMA pipeline depth (2..4 rows on the
                                row/cluster paths, 2..8 tiles on the stream path) */
     int tune_ctas_per_sm;   /* 0 = as many as fit; otherwise a cap */
-    int tune_l2_keep;       /* stream path: 0 = default, 1 = first read asks L2 to keep
-                               the row (evict-last), 2 = it does not (evict-first) */
+    int tune_l2_keep;       /* stream path: 0 = default (evict-first), 1 = the first read
+                               asks L2 to keep the row (evict-last), 2 = evict-first */
     int reserved[4];        /* must be zero */
 } ce_options;
 

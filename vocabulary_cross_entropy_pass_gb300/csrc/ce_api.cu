@@ -32,12 +32,15 @@ struct Plan {
 };
 
 // Row-streaming kernel: tiles of threads*64 bytes, `stages` of them in flight.
+// Row-streaming kernel: 16 KB tiles (256 threads x 4 vectors or 512 x 2),
+// `stages` of them in flight.  Defaults from a sweep on the (4,4096,128000)
+// bf16 workload: 512 consuming threads, 6 stages, evict-first L2 policy.
 bool plan_stream(const ce_options* o, StreamPlan* sp) {
-    sp->threads = (o && o->tune_threads) ? o->tune_threads : 256;
+    sp->threads = (o && o->tune_threads) ? o->tune_threads : 512;
     sp->stages = (o && o->tune_stages) ? o->tune_stages : 6;
     sp->ctas_per_sm_cap = o ? o->tune_ctas_per_sm : 0;
-    sp->l2_keep = (o && o->tune_l2_keep == 2) ? 0 : 1;
-    const size_t tile = (size_t)sp->threads * 64;
+    sp->l2_keep = (o && o->tune_l2_keep == 1) ? 1 : 0;
+    const size_t tile = 16 * 1024;
     return sp->stages * tile + 1024 <= kSmemLimit;
 }
 
