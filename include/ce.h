@@ -158,6 +158,38 @@ ce_status ce_fwd_only(const void* logits, ce_dtype dtype, ce_layout layout, int6
                       void* workspace, size_t workspace_bytes, const ce_options* opts,
                       void* stream);
 
+/* ce_fwd_bwd without a workspace argument: the pass keeps its scratch in a
+ * fixed 2 MiB array of device memory that the library itself reserves on
+ * every GPU where it is loaded (held until the process exits).  The pages have
+ * no counterpart of this entry point; it exists for callers that must not
+ * allocate device memory for a call: runtimes that plan every byte of device
+ * memory before they start and give custom operators no workspace, and
+ * latency-critical loops where cudaMalloc (which may synchronise the device or
+ * fail on a fragmented heap) is not acceptable.  The caller still passes the
+ * logits, targets and outputs, as for ce_fwd_bwd; this call allocates nothing.
+ *
+ * Limit: the scratch must hold 256 bytes + 4*dim0*dim1 bytes rounded up to
+ * 256 (per-row losses), plus 16*dim0*dim1*K bytes rounded up to 256 when the
+ * planner takes the two-stage path with K chunks.  Larger problems are
+ * rejected with CE_ERR_WORKSPACE_TOO_SMALL before anything is launched
+ * (about 520,000 rows on the row, cluster and stream paths).
+ *
+ * Set-up: the first call on a device looks up the scratch's device address
+ * with that device current (the caller's current device); make that first
+ * call before any stream capture.  No part of the scratch needs clearing:
+ * every pass writes what it later reads.  All calls on a device share the one
+ * array and it keeps the last call's contents, so calls that may overlap on
+ * the GPU (different streams, or threads enqueuing at once) race on it:
+ * serialise them.  The error word lives in that internal scratch, so
+ * ce_get_error cannot read it; out-of-range targets still show as NaN row
+ * losses. */
+ce_status ce_fwd_bwd_noalloc(void* logits, ce_dtype dtype, ce_layout layout, int64_t dim0,
+                             int64_t dim1, int64_t V, const int64_t strides[3],
+                             const int64_t* targets, const int64_t target_strides[2],
+                             float label_smoothing, int64_t ignore_idx, int reduce_loss,
+                             const float* dloss, float* loss_out, void* grad_inplace,
+                             int64_t* n_non_ignore_out, const ce_options* opts, void* stream);
+
 /* Waits for `stream`, then copies the device error word of the last pass that
  * used `workspace` into *host_err (host pointer).  Returns CE_OK,
  * CE_ERR_TARGET_RANGE or CE_ERR_DEVICE_TIMEOUT from its bits, CE_ERR_LAUNCH if

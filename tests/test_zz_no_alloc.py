@@ -1,0 +1,93 @@
+"""ce_fwd_bwd_noalloc: the pass for callers that must not allocate device
+memory per call (runtimes that plan all device memory before they start and
+give custom operators no workspace; latency-critical loops that cannot risk
+cudaMalloc's device synchronisation or failure).  Its scratch is the library's
+own fixed device array, so these tests compare it with ce_fwd_bwd, which uses a
+caller-provided workspace, on the same inputs, twice in a row (the second call
+reuses the array the first one left behind).
+
+This file is collected last so that a run stopping at the first failure has
+already run every other test."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from tests import harness
+from vocabulary_cross_entropy_pass_gb300 import _lib
+from vocabulary_cross_entropy_pass_gb300 import workloads as wl
+
+
+def _noalloc_c(x, t, loss, a, reduce, opts=None):
+    """Call the C entry point directly through ctypes."""
+    lib = _lib.load()
+    d0, d1, V = x.shape
+    st = _lib.i64_array(x.stride())
+    ts = _lib.i64_array(t.stride())
+    stream = torch.cuda.current_stream().cuda_stream if x.is_cuda else 0
+    return lib.ce_fwd_bwd_noalloc(ctypes.c_void_p(x.data_ptr()), {torch.float32: 0,
+                                  torch.bfloat16: 1, torch.float16: 2}[x.dtype], 0, d0, d1, V, st,
+                                  ctypes.c_void_p(t.data_ptr()), ts, float(a), -100, int(reduce),
+                                  None, ctypes.c_void_p(loss.data_ptr()),
+                                  ctypes.c_void_p(x.data_ptr()), None,
+                                  ctypes.byref(opts) if opts is not None else None,
+                                  ctypes.c_void_p(stream))
+
+
+def test_oversized_problems_are_rejected_on_the_host():
+    # no GPU needed: the size test runs before any CUDA call
+    from vocabulary_cross_entropy_pass_gb300 import build
+    build.build()
+    lib = _lib.load()
+    loss = ctypes.c_void_p(0x3000)
+
+    def call(d1, V, **o):
+        opts = _lib.make_options(**o)
+        return lib.ce_fwd_bwd_noalloc(ctypes.c_void_p(0x1000), 1, 0, 1, d1, V,
+                                      _lib.i64_array((d1 * V, V, 1)), ctypes.c_void_p(0x2000),
+                                      _lib.i64_array((d1, 1)), 0.0, -100, 1, None, loss,
+                                      ctypes.c_void_p(0x1000), None, ctypes.byref(opts), None)
+    assert call(600_000, 4096) == 4                 # per-row losses alone exceed 2 MiB
+    assert call(5_000, 128000, force_path=3) == 4   # two-stage partials exceed 2 MiB
+    assert call(8, 4096, tune_threads=300) == 1     # ordinary argument checks still apply
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name,path", [("c2_sbv8192_bf16", 0), ("c5_bsv128000_bf16_ls", 0),
+                                       ("c3_bsv32000_bf16_spiked", 3),
+                                       ("c1_bsv4096_f32", 0)])
+def test_noalloc_matches_workspace_entry_point(name, path):
+    import vocabulary_cross_entropy_pass_gb300 as pkg
+    w = wl.WORKLOADS[name]
+    dev = torch.device("cuda")
+    x = wl.logits(w).to(dev)
+    t = wl.targets(w).to(dev)
+    opts = _lib.make_options(force_path=path)
+    for _call in range(2):   # two calls in a row share the fixed scratch
+        xa, xb = x.clone(), x.clone()
+        la = pkg.ce_fwd_bwd(xa, t, label_smoothing=w.label_smoothing,
+                            reduce_loss=w.reduce_loss, force_path=path)
+        lb = torch.full_like(la, float("nan"))
+        rc = _noalloc_c(xb, t, lb, w.label_smoothing, w.reduce_loss, opts)
+        assert rc == 0, _lib.STATUS.get(rc, rc)
+        torch.cuda.synchronize()
+        # the same tolerances as against the oracle, with ce_fwd_bwd as reference
+        harness.check_loss(lb.cpu().numpy(), la.cpu().numpy().astype(np.float64), w.dtype, name)
+        ga = xa.float().cpu().numpy().astype(np.float64).reshape(w.N, w.V)
+        gb = xb.float().cpu().numpy().astype(np.float64).reshape(w.N, w.V)
+        excess, _ = harness.grad_errors(gb, ga, w.dtype)
+        assert excess <= 0.0
+
+
+@pytest.mark.gpu
+def test_noalloc_python_binding():
+    import vocabulary_cross_entropy_pass_gb300 as pkg
+    w = wl.WORKLOADS["c2_sbv8192_bf16"]
+    dev = torch.device("cuda")
+    x = wl.logits(w).to(dev)
+    t = wl.targets(w).to(dev)
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    ref = pkg.ce_fwd_bwd(x.clone(), t, label_smoothing=w.label_smoothing, reduce_loss=True)
+    pkg.ce_fwd_bwd_noalloc(x, t, loss, label_smoothing=w.label_smoothing, reduce_loss=True)
+    harness.check_loss(loss.cpu().numpy(), ref.cpu().numpy().astype(np.float64), "bf16")

@@ -25,7 +25,7 @@ from . import _lib
 from ._lib import (CE_PATH_AUTO, CE_PATH_CLUSTER, CE_PATH_ROW, CE_PATH_STREAM,
                    CE_PATH_TWO_STAGE, CEError, ce_options, make_options)
 
-__all__ = ["ce_fwd_bwd", "ce_fwd_only", "ce_workspace_bytes", "ce_get_error", "ce_status_string",
+__all__ = ["ce_fwd_bwd", "ce_fwd_bwd_noalloc", "ce_fwd_only", "ce_workspace_bytes", "ce_get_error", "ce_status_string",
            "ce_plan_path", "CEError", "make_options", "ce_options",
            "CE_PATH_AUTO", "CE_PATH_ROW", "CE_PATH_CLUSTER", "CE_PATH_TWO_STAGE", "CE_PATH_STREAM"]
 
@@ -171,6 +171,35 @@ def ce_fwd_only(logits: torch.Tensor, targets: torch.Tensor, label_smoothing: fl
                          ctypes.c_void_p(ws.data_ptr()), wsb, ctypes.byref(opts),
                          _stream(dev, stream))
     _raise(rc, "ce_fwd_only")
+    return loss_out
+
+
+def ce_fwd_bwd_noalloc(logits: torch.Tensor, targets: torch.Tensor, loss_out: torch.Tensor,
+                       label_smoothing: float = 0.0, ignore_idx: int = -100,
+                       reduce_loss: bool = False, dloss: torch.Tensor | None = None,
+                       layout: str = "bsv", n_non_ignore_out: torch.Tensor | None = None,
+                       opts=None, stream=None) -> torch.Tensor:
+    """ce_fwd_bwd for callers that cannot hand out device memory: the pass
+    keeps its scratch in the library's own fixed device array, so nothing is
+    allocated here either (``loss_out`` must be given).  Calls that may
+    overlap on the GPU share that array and must be serialised."""
+    _check(logits, targets)
+    lib = _lib.load()
+    d0, d1, V, st = _dims(logits)
+    ts = _tstrides(targets, d0, d1)
+    opts = _options(opts, CE_PATH_AUTO, 0)
+    rc = lib.ce_fwd_bwd_noalloc(
+        ctypes.c_void_p(logits.data_ptr()), _DTYPE[logits.dtype], _LAYOUT[layout], d0, d1, V,
+        _lib.i64_array(st), ctypes.c_void_p(targets.data_ptr()), _lib.i64_array(ts),
+        float(label_smoothing), int(ignore_idx), int(bool(reduce_loss)),
+        ctypes.c_void_p(dloss.data_ptr() if dloss is not None else None),
+        ctypes.c_void_p(loss_out.data_ptr()), ctypes.c_void_p(logits.data_ptr()),
+        ctypes.c_void_p(n_non_ignore_out.data_ptr() if n_non_ignore_out is not None else None),
+        ctypes.byref(opts), _stream(logits.device, stream))
+    if rc == 4:
+        raise CEError(rc, "ce_fwd_bwd_noalloc: the problem needs more scratch than the "
+                          "library's fixed 2 MiB array holds")
+    _raise(rc, "ce_fwd_bwd_noalloc")
     return loss_out
 
 

@@ -338,3 +338,87 @@ int ce_plan_path(const void* logits, ce_dtype dtype, int64_t dim0, int64_t dim1,
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// ce_fwd_bwd_noalloc: the pass with its scratch in a fixed device array.
+//
+// Scratch (error word, row count, per-row losses of the mean, two-stage
+// partials) normally lives in the caller's workspace.  This entry point takes
+// it from g_noalloc_scratch, a file-scope __device__ array that every GPU
+// loading the library holds until the process exits.  In host code the name
+// g_noalloc_scratch denotes a host-side shadow, not device memory, so it is
+// never handed to a kernel: its device address is looked up once per device
+// with cudaGetSymbolAddress (with that device current) and cached.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace gbce {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = (size_t)2 << 20;  // 2 MiB per GPU
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mutex;
+void* g_noalloc_device_ptr[kNoAllocMaxDevices];  // device address per device, set once
+
+// Device address of the scratch on the current device (set-up on first use).
+ce_status noalloc_scratch(void** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices)
+        return CE_ERR_LAUNCH;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_device_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return CE_ERR_LAUNCH;
+        g_noalloc_device_ptr[dev] = p;
+    }
+    *out = g_noalloc_device_ptr[dev];
+    return CE_OK;
+}
+
+// Scratch bytes the planned pass actually touches: the header, the per-row
+// loss slots, and the two-stage partials when that path runs.
+size_t noalloc_need(const Problem& pb, const Plan& pl) {
+    size_t need = kWsHeaderBytes + align_up((size_t)pb.N * sizeof(float), 256);
+    if (pl.path == CE_PATH_TWO_STAGE)
+        need += align_up((size_t)pb.N * (size_t)pl.split.chunks * sizeof(float4), 256);
+    return need;
+}
+
+}  // namespace
+}  // namespace gbce
+
+extern "C" ce_status ce_fwd_bwd_noalloc(void* logits, ce_dtype dtype, ce_layout layout,
+                                        int64_t dim0, int64_t dim1, int64_t V,
+                                        const int64_t strides[3], const int64_t* targets,
+                                        const int64_t target_strides[2], float label_smoothing,
+                                        int64_t ignore_idx, int reduce_loss, const float* dloss,
+                                        float* loss_out, void* grad_inplace,
+                                        int64_t* n_non_ignore_out, const ce_options* opts,
+                                        void* stream) {
+    if (dim0 < 0 || dim1 < 0 || V < 1 || V > 0x7fffffffLL || !strides) return CE_ERR_INVALID_ARG;
+    // argument checks of ce_fwd_bwd; the workspace test is replaced by the
+    // scratch-size test below, so a placeholder aligned pointer stands in here
+    ce_status st = check_common(logits, dtype, layout, dim0, dim1, V, strides, targets,
+                                target_strides, label_smoothing, reduce_loss, loss_out,
+                                reinterpret_cast<void*>(256), workspace_need(dim0 * dim1, V, opts),
+                                opts);
+    if (st != CE_OK) return st;
+    if (grad_inplace != logits) return CE_ERR_INVALID_ARG;
+    if (!rows_disjoint(dim0, dim1, V, strides[0], strides[1])) return CE_ERR_BAD_STRIDE;
+    Problem pb;
+    fill_problem(pb, logits, dtype, dim0, dim1, V, strides, targets, target_strides,
+                 label_smoothing, ignore_idx, reduce_loss);
+    pb.dloss = dloss;
+    pb.grad = true;
+    Plan pl = make_plan(pb, opts);
+    if (pl.path < 0) return CE_ERR_UNSUPPORTED_PATH;
+    if (noalloc_need(pb, pl) > kNoAllocScratchBytes) return CE_ERR_WORKSPACE_TOO_SMALL;
+    void* scratch = nullptr;
+    st = noalloc_scratch(&scratch);
+    if (st != CE_OK) return st;
+    return run_pass(pb, opts, loss_out, n_non_ignore_out, scratch,
+                    static_cast<cudaStream_t>(stream));
+}
