@@ -246,7 +246,8 @@ def run_ours(args, w, rank: int, world: int, dist) -> None:
     loss = torch.empty(1, dtype=torch.float32, device=dev)
     tune = dict(force_path=args.force_path, num_vocab_chunks=args.chunks,
                 tune_threads=args.tune_threads, tune_stages=args.tune_stages,
-                tune_ctas_per_sm=args.tune_ctas_per_sm, tune_l2_keep=args.tune_l2_keep)
+                tune_ctas_per_sm=args.tune_ctas_per_sm, tune_l2_keep=args.tune_l2_keep,
+                tune_tile_kb=args.tune_tile_kb)
     opts = pkg.make_options(**tune)
     ws = torch.empty(pkg.ce_workspace_bytes(w.dim0, w.dim1, w.V, x.dtype, opts),
                      dtype=torch.uint8, device=dev)
@@ -378,6 +379,7 @@ def main(argv=None) -> int:
     ap.add_argument("--tune-stages", type=int, default=0)
     ap.add_argument("--tune-ctas-per-sm", type=int, default=0)
     ap.add_argument("--tune-l2-keep", type=int, default=0)
+    ap.add_argument("--tune-tile-kb", type=int, default=0)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -108,11 +108,12 @@ typedef struct {
     int tune_threads;       /* 0 = default; otherwise CTA size (256 or 512; on the stream
                                path the number of consuming threads) */
     int tune_stages;        /* 0 = default; otherwise TMA pipeline depth (2..4 rows on the
-                               row/cluster paths, 2..8 tiles on the stream path) */
+                               row/cluster paths, 2..12 tiles on the stream path) */
     int tune_ctas_per_sm;   /* 0 = as many as fit; otherwise a cap */
-    int tune_l2_keep;       /* stream path: 0 = default (evict-first), 1 = the first read
-                               asks L2 to keep the row (evict-last), 2 = evict-first */
-    int reserved[4];        /* must be zero */
+    int tune_l2_keep;       /* stream path: 0 = default (1), 1 = the first read asks L2 to
+                               keep the row for the second (evict-last), 2 = evict-first */
+    int tune_tile_kb;       /* stream path: 0 = default, else the ring tile size (16 or 32 KB) */
+    int reserved[3];        /* must be zero */
 } ce_options;
 
 /* Bytes of device workspace a call with these sizes needs (either entry

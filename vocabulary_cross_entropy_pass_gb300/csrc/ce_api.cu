@@ -32,15 +32,16 @@ struct Plan {
 };
 
 // Row-streaming kernel: tiles of threads*64 bytes, `stages` of them in flight.
-// Row-streaming kernel: 16 KB tiles (256 threads x 4 vectors or 512 x 2),
-// `stages` of them in flight.  Defaults from a sweep on the (4,4096,128000)
-// bf16 workload: 512 consuming threads, 6 stages, evict-first L2 policy.
+// Row-streaming kernel: tiles of 16 or 32 KB consumed by 256 or 512 threads,
+// `stages` of them in flight.  Defaults from sweeps on the (4,4096,128000)
+// bf16 workload.
 bool plan_stream(const ce_options* o, StreamPlan* sp) {
     sp->threads = (o && o->tune_threads) ? o->tune_threads : 512;
-    sp->stages = (o && o->tune_stages) ? o->tune_stages : 6;
+    sp->tile_kb = (o && o->tune_tile_kb) ? o->tune_tile_kb : 32;
+    sp->stages = (o && o->tune_stages) ? o->tune_stages : (sp->tile_kb == 32 ? 6 : 10);
     sp->ctas_per_sm_cap = o ? o->tune_ctas_per_sm : 0;
-    sp->l2_keep = (o && o->tune_l2_keep == 1) ? 1 : 0;
-    const size_t tile = 16 * 1024;
+    sp->l2_keep = (o && o->tune_l2_keep == 2) ? 0 : 1;
+    const size_t tile = (size_t)sp->tile_kb * 1024;
     return sp->stages * tile + 1024 <= kSmemLimit;
 }
 
@@ -48,12 +49,13 @@ int round_up_int(int64_t x, int64_t m) { return (int)((x + m - 1) / m * m); }
 
 bool opts_clean(const ce_options* o) {
     if (!o) return true;
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 3; ++i)
         if (o->reserved[i] != 0) return false;
+    if (o->tune_tile_kb != 0 && o->tune_tile_kb != 16 && o->tune_tile_kb != 32) return false;
     if (o->force_path < 0 || o->force_path > CE_PATH_STREAM) return false;
     if (o->num_vocab_chunks < 0) return false;
     if (o->tune_threads != 0 && o->tune_threads != 256 && o->tune_threads != 512) return false;
-    if (o->tune_stages < 0 || o->tune_stages > 8 || o->tune_stages == 1) return false;
+    if (o->tune_stages < 0 || o->tune_stages > 12 || o->tune_stages == 1) return false;
     if (o->tune_ctas_per_sm < 0) return false;
     if (o->tune_l2_keep < 0 || o->tune_l2_keep > 2) return false;
     return true;

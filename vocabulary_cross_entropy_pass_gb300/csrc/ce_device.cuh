@@ -165,6 +165,20 @@ struct Vec<float> {
         return make_uint4(__float_as_uint(g[0]), __float_as_uint(g[1]), __float_as_uint(g[2]),
                           __float_as_uint(g[3]));
     }
+    // pairs of consecutive elements, for packed f32x2 arithmetic
+    __device__ __forceinline__ static void unpack2(const uint4& r, float2* x) {
+        x[0] = make_float2(__uint_as_float(r.x), __uint_as_float(r.y));
+        x[1] = make_float2(__uint_as_float(r.z), __uint_as_float(r.w));
+    }
+    __device__ __forceinline__ static uint4 pack2(const float2* g) {
+        return make_uint4(__float_as_uint(g[0].x), __float_as_uint(g[0].y), __float_as_uint(g[1].x),
+                          __float_as_uint(g[1].y));
+    }
+    // running max of a tile: kept as a float for fp32
+    using Max = float;
+    __device__ __forceinline__ static Max max_init() { return -INFINITY; }
+    __device__ __forceinline__ static Max max_acc(Max m, const uint4& r) { return fmaxf(m, vmax(r)); }
+    __device__ __forceinline__ static float max_done(Max m) { return m; }
     __device__ __forceinline__ static float load1(const void* p) {
         return *reinterpret_cast<const float*>(p);
     }
@@ -208,6 +222,28 @@ struct Vec<__nv_bfloat16> {
                           bf162_bits(__floats2bfloat162_rn(g[4], g[5])),
                           bf162_bits(__floats2bfloat162_rn(g[6], g[7])));
     }
+    __device__ __forceinline__ static void unpack2(const uint4& r, float2* x) {
+        x[0] = make_float2(__uint_as_float(r.x << 16), __uint_as_float(r.x & 0xffff0000u));
+        x[1] = make_float2(__uint_as_float(r.y << 16), __uint_as_float(r.y & 0xffff0000u));
+        x[2] = make_float2(__uint_as_float(r.z << 16), __uint_as_float(r.z & 0xffff0000u));
+        x[3] = make_float2(__uint_as_float(r.w << 16), __uint_as_float(r.w & 0xffff0000u));
+    }
+    __device__ __forceinline__ static uint4 pack2(const float2* g) {
+        return make_uint4(bf162_bits(__floats2bfloat162_rn(g[0].x, g[0].y)),
+                          bf162_bits(__floats2bfloat162_rn(g[1].x, g[1].y)),
+                          bf162_bits(__floats2bfloat162_rn(g[2].x, g[2].y)),
+                          bf162_bits(__floats2bfloat162_rn(g[3].x, g[3].y)));
+    }
+    // running max of a tile: kept packed (max is exact in bf16)
+    using Max = __nv_bfloat162;
+    __device__ __forceinline__ static Max max_init() { return as_bf162(0xff80ff80u); }  // -inf, -inf
+    __device__ __forceinline__ static Max max_acc(Max m, const uint4& r) {
+        return __hmax2(m, __hmax2(__hmax2(as_bf162(r.x), as_bf162(r.y)),
+                                  __hmax2(as_bf162(r.z), as_bf162(r.w))));
+    }
+    __device__ __forceinline__ static float max_done(Max m) {
+        return fmaxf(__low2float(m), __high2float(m));
+    }
     __device__ __forceinline__ static float load1(const void* p) {
         return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(p));
     }
@@ -234,6 +270,24 @@ struct Vec<__half> {
     __device__ __forceinline__ static uint4 pack(const float* g) {
         return make_uint4(h2_bits(__floats2half2_rn(g[0], g[1])), h2_bits(__floats2half2_rn(g[2], g[3])),
                           h2_bits(__floats2half2_rn(g[4], g[5])), h2_bits(__floats2half2_rn(g[6], g[7])));
+    }
+    __device__ __forceinline__ static void unpack2(const uint4& r, float2* x) {
+        x[0] = __half22float2(as_h2(r.x));
+        x[1] = __half22float2(as_h2(r.y));
+        x[2] = __half22float2(as_h2(r.z));
+        x[3] = __half22float2(as_h2(r.w));
+    }
+    __device__ __forceinline__ static uint4 pack2(const float2* g) {
+        return make_uint4(h2_bits(__floats2half2_rn(g[0].x, g[0].y)), h2_bits(__floats2half2_rn(g[1].x, g[1].y)),
+                          h2_bits(__floats2half2_rn(g[2].x, g[2].y)), h2_bits(__floats2half2_rn(g[3].x, g[3].y)));
+    }
+    using Max = __half2;
+    __device__ __forceinline__ static Max max_init() { return as_h2(0xfc00fc00u); }  // -inf, -inf
+    __device__ __forceinline__ static Max max_acc(Max m, const uint4& r) {
+        return __hmax2(m, __hmax2(__hmax2(as_h2(r.x), as_h2(r.y)), __hmax2(as_h2(r.z), as_h2(r.w))));
+    }
+    __device__ __forceinline__ static float max_done(Max m) {
+        return fmaxf(__low2float(m), __high2float(m));
     }
     __device__ __forceinline__ static float load1(const void* p) {
         return __half2float(*reinterpret_cast<const __half*>(p));

@@ -51,8 +51,9 @@ struct FusedPlan {
 
 // Plan of the row-streaming kernel.
 struct StreamPlan {
-    int threads;               // consumer threads: 256 (4 vectors each) or 512 (2 each)
-    int stages;                // ring depth (tiles of threads*64 bytes)
+    int threads;               // consumer threads: 256 or 512
+    int tile_kb;               // ring tile size: 16 or 32 KB
+    int stages;                // ring depth in tiles
     int ctas_per_sm_cap;       // 0 = no cap
     int l2_keep;               // 1: first-pass copies use an L2 evict-last policy
 };

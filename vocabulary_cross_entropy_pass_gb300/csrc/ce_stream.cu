@@ -64,19 +64,105 @@ __device__ __forceinline__ uint64_t l2_evict_last_policy() {
     return pol;
 }
 
+// One ring slot: stage index and phase parity, advanced without division.
+struct Ring {
+    int s = 0;
+    uint32_t ph = 0;
+    int n;
+    __device__ explicit Ring(int stages) : n(stages) {}
+    __device__ __forceinline__ void next() {
+        if (++s == n) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+};
+
+// Pass-1 work on one tile: running max, then p = 2^((x - m) log2e) summed,
+// and the plain sum, in packed f32x2 arithmetic.  FULL: every vector valid.
+template <typename T, int NC, int NV, bool FULL>
+__device__ __forceinline__ void stats_tile(const uint4* tile, int tid, int nvec, float& m,
+                                           float2& d2, float2& s2) {
+    using VT = Vec<T>;
+    constexpr int P = VT::kElems / 2;  // float2 pairs per vector
+    uint4 raw[NV];
+    typename VT::Max tm = VT::max_init();
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        if (FULL || tid + i * NC < nvec) {
+            raw[i] = tile[tid + i * NC];
+            tm = VT::max_acc(tm, raw[i]);
+        }
+    }
+    const float tmf = VT::max_done(tm);
+    if (tmf > m) {  // new running max: rescale what was summed so far
+        if (m != -INFINITY) {
+            const float c = ex2_approx((m - tmf) * kLog2e);
+            d2.x *= c;
+            d2.y *= c;
+        }
+        m = tmf;
+    }
+    const float nml = (m == -INFINITY) ? 0.f : -m * kLog2e;
+    const float2 L2 = make_float2(kLog2e, kLog2e);
+    const float2 NM = make_float2(nml, nml);
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        if (FULL || tid + i * NC < nvec) {
+            float2 x[P];
+            VT::unpack2(raw[i], x);
+#pragma unroll
+            for (int j = 0; j < P; ++j) {
+                const float2 a = __ffma2_rn(x[j], L2, NM);
+                d2 = __fadd2_rn(d2, make_float2(ex2_approx(a.x), ex2_approx(a.y)));
+                s2 = __fadd2_rn(s2, x[j]);
+            }
+        }
+    }
+}
+
+// Pass-2 work on one tile: g * 2^((x - lse) log2e) - g a/V, rounded to T and
+// stored over the logits.
+template <typename T, int NC, int NV, bool FULL>
+__device__ __forceinline__ void grad_tile(const uint4* tile, uint4* dst, int tid, int nvec,
+                                          float2 NL, float2 G2, float2 NB) {
+    using VT = Vec<T>;
+    constexpr int P = VT::kElems / 2;
+    const float2 L2 = make_float2(kLog2e, kLog2e);
+    uint4 raw[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i)
+        if (FULL || tid + i * NC < nvec) raw[i] = tile[tid + i * NC];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        if (FULL || tid + i * NC < nvec) {
+            float2 x[P], o[P];
+            VT::unpack2(raw[i], x);
+#pragma unroll
+            for (int j = 0; j < P; ++j) {
+                const float2 a = __ffma2_rn(x[j], L2, NL);
+                o[j] = __ffma2_rn(make_float2(ex2_approx(a.x), ex2_approx(a.y)), G2, NB);
+            }
+            stg128_stream(dst + tid + i * NC, VT::pack2(o));
+        }
+    }
+}
+
 template <typename T, int NC, int NV, bool GRAD>
 __global__ void __launch_bounds__(NC + 32, 1)
 ce_stream_kernel(const __grid_constant__ StreamArgs p) {
     using VT = Vec<T>;
     constexpr int VEC = VT::kElems;
     constexpr int ES = sizeof(T);
-    constexpr int NW = NC / 32;  // consumer warps
+    constexpr int NW = NC / 32;           // consumer warps
+    constexpr int TB = NC * NV * 16;      // tile bytes
+    constexpr int TV = NC * NV;           // vectors per tile
 
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* ring = smem;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)p.stages * p.tile_bytes);
-    uint64_t* empty = full + 8;
-    float4* red = reinterpret_cast<float4*>(empty + 8);   // [2][NW]
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)p.stages * TB);
+    uint64_t* empty = full + 12;
+    float4* red = reinterpret_cast<float4*>(empty + 12);  // [2][NW]
     float* xy_s = reinterpret_cast<float*>(red + 2 * NW);  // [2]
     volatile int* abort_flag = reinterpret_cast<volatile int*>(xy_s + 2);
 
@@ -103,37 +189,39 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
         return y != p.ignore_idx && y >= 0 && y < (int64_t)p.V;
     };
     const int npass = GRAD ? 2 : 1;
+    const int last_nvec = (int)(p.last_bytes / 16);
 
     // ------------------------------------------------------------ producer warp
     if (warp == NW) {
         if (lane == 0) {
             const uint64_t pol_keep = p.l2_keep ? l2_evict_last_policy() : l2_evict_first_policy();
             const uint64_t pol_drop = l2_evict_first_policy();
-            uint32_t k = 0;
+            Ring rg(p.stages);
+            uint32_t issued = 0;
             for (int64_t r = blockIdx.x; r < p.N && !*abort_flag; r += gridDim.x) {
                 if (!is_loaded(row_target(r))) continue;
                 const char* row = row_ptr(r);
                 for (int pass = 0; pass < npass && !*abort_flag; ++pass) {
-                    for (int t = 0; t < p.ntiles; ++t, ++k) {
-                        const int s = (int)(k % (uint32_t)p.stages);
-                        const uint32_t ph = (k / (uint32_t)p.stages) & 1u;
-                        if (!mbar_wait_bounded(&empty[s], ph ^ 1u)) {
+                    for (int t = 0; t < p.ntiles; ++t) {
+                        if (!mbar_wait_bounded(&empty[rg.s], rg.ph ^ 1u)) {
                             atomicOr(p.err, CE_DEVERR_TIMEOUT);
                             *abort_flag = 1;
                             break;
                         }
-                        const uint32_t bytes = (t == p.ntiles - 1) ? p.last_bytes : p.tile_bytes;
-                        mbar_arrive_expect_tx(&full[s], bytes);
-                        tma_load_1d(ring + (size_t)s * p.tile_bytes, row + (size_t)t * p.tile_bytes,
-                                    bytes, &full[s], pass == 0 ? pol_keep : pol_drop);
+                        const uint32_t bytes = (t == p.ntiles - 1) ? p.last_bytes : (uint32_t)TB;
+                        mbar_arrive_expect_tx(&full[rg.s], bytes);
+                        tma_load_1d(ring + (size_t)rg.s * TB, row + (size_t)t * TB, bytes, &full[rg.s],
+                                    pass == 0 ? pol_keep : pol_drop);
+                        rg.next();
+                        ++issued;
                     }
                 }
             }
             if (*abort_flag) {
                 // let every copy already issued land before the CTA goes away
                 for (int s = 0; s < p.stages; ++s) {
-                    if (k > (uint32_t)s) {
-                        const uint32_t last = (k - 1u - (uint32_t)s) / (uint32_t)p.stages;
+                    if (issued > (uint32_t)s) {
+                        const uint32_t last = (issued - 1u - (uint32_t)s) / (uint32_t)p.stages;
                         (void)mbar_wait_bounded(&full[s], last & 1u);
                     }
                 }
@@ -145,8 +233,19 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
     // ------------------------------------------------------------ consumer warps
     float g_reduce = 1.f;
     if (p.reduce) g_reduce = (p.dloss ? __ldg(p.dloss) : 1.f) / (float)(*p.n_dev);
-    uint32_t k = 0;
+    Ring rg(p.stages);
     int par = 0;
+    auto wait_full = [&]() {
+        if (!*abort_flag && !mbar_wait_bounded(&full[rg.s], rg.ph)) {
+            atomicOr(p.err, CE_DEVERR_TIMEOUT);
+            *abort_flag = 1;
+        }
+    };
+    auto release = [&]() {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[rg.s]);
+        rg.next();
+    };
     for (int64_t r = blockIdx.x; r < p.N; r += gridDim.x) {
         const int64_t y = row_target(r);
         char* rowp = row_ptr(r);
@@ -164,56 +263,25 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
         }
         const float g = p.reduce ? g_reduce : (p.dloss ? __ldg(p.dloss + r) : 1.f);
         const int64_t ybyte = y * ES;
+        const int ty = (int)(ybyte / TB);                 // tile holding the target
+        const int yv = (int)((ybyte - (int64_t)ty * TB) / 16);  // its vector in that tile
 
         // pass 1: running statistics over the tiles
-        float m = -INFINITY, d = 0.f, S = 0.f;
-        for (int t = 0; t < p.ntiles; ++t, ++k) {
-            const int s = (int)(k % (uint32_t)p.stages);
-            const uint32_t ph = (k / (uint32_t)p.stages) & 1u;
-            if (!*abort_flag && !mbar_wait_bounded(&full[s], ph)) {
-                atomicOr(p.err, CE_DEVERR_TIMEOUT);
-                *abort_flag = 1;
-            }
-            const unsigned char* tile = ring + (size_t)s * p.tile_bytes;
-            const int nvec = (int)(((t == p.ntiles - 1) ? p.last_bytes : p.tile_bytes) / 16);
-            uint4 raw[NV];
-            float tm = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < NV; ++i) {
-                const int v = tid + i * NC;
-                if (v < nvec) {
-                    raw[i] = lds128(tile + (size_t)v * 16);
-                    tm = fmaxf(tm, VT::vmax(raw[i]));
-                }
-            }
-            // the target logit lives in this tile at byte offset ybyte - t*tile_bytes
-            const int64_t yoff = ybyte - (int64_t)t * p.tile_bytes;
-            if (tid == 0 && yoff >= 0 && yoff < (int64_t)nvec * 16)
-                xy_s[par] = VT::load1(tile + yoff);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
-            if (tm > m) {
-                if (m != -INFINITY) d *= ex2_approx((m - tm) * kLog2e);
-                m = tm;
-            }
-            const float ml = (m == -INFINITY) ? 0.f : m * kLog2e;
-#pragma unroll
-            for (int i = 0; i < NV; ++i) {
-                const int v = tid + i * NC;
-                if (v < nvec) {
-                    float x[VEC];
-                    VT::unpack(raw[i], x);
-#pragma unroll
-                    for (int e = 0; e < VEC; ++e) {
-                        d += ex2_approx(fmaf(x[e], kLog2e, -ml));
-                        S += x[e];
-                    }
-                }
-            }
+        float m = -INFINITY;
+        float2 d2 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
+        for (int t = 0; t < p.ntiles; ++t) {
+            wait_full();
+            const uint4* tile = reinterpret_cast<const uint4*>(ring + (size_t)rg.s * TB);
+            if (t == ty && tid == 0) xy_s[par] = VT::load1(ring + (size_t)rg.s * TB + (ybyte - (int64_t)ty * TB));
+            if (t < p.ntiles - 1)
+                stats_tile<T, NC, NV, true>(tile, tid, TV, m, d2, s2);
+            else
+                stats_tile<T, NC, NV, false>(tile, tid, last_nvec, m, d2, s2);
+            release();
         }
 
         // CTA combine, fixed order
-        Part q = warp_allreduce_part(Part{m, d, S});
+        Part q = warp_allreduce_part(Part{m, d2.x + d2.y, s2.x + s2.y});
         if (lane == 0) red[par * NW + warp] = make_float4(q.m, q.d, q.S, 0.f);
         named_bar_sync(1, NC);
         Part G = part_identity();
@@ -223,53 +291,34 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
             G = part_combine(G, Part{v4.x, v4.y, v4.z});
         }
         const float lse = G.m + logf(G.d);
+        const float xy = xy_s[par];
         if (tid == 0) {
-            p.loss[r] = lse - (1.f - p.a) * xy_s[par] - p.a_over_v * G.S;
+            p.loss[r] = lse - (1.f - p.a) * xy - p.a_over_v * G.S;
             if (p.lse_out) p.lse_out[r] = lse;
         }
 
         // pass 2: gradient
         if (GRAD) {
-            const float lsel = lse * kLog2e;
+            const float nll = -lse * kLog2e;
             const float bb = g * p.a_over_v;
-            const float hit = g * (1.f - p.a);
-            for (int t = 0; t < p.ntiles; ++t, ++k) {
-                const int s = (int)(k % (uint32_t)p.stages);
-                const uint32_t ph = (k / (uint32_t)p.stages) & 1u;
-                if (!*abort_flag && !mbar_wait_bounded(&full[s], ph)) {
-                    atomicOr(p.err, CE_DEVERR_TIMEOUT);
-                    *abort_flag = 1;
-                }
-                const unsigned char* tile = ring + (size_t)s * p.tile_bytes;
-                const int nvec = (int)(((t == p.ntiles - 1) ? p.last_bytes : p.tile_bytes) / 16);
-                char* gdst = rowp + (size_t)t * p.tile_bytes;
-                const int64_t yoff = ybyte - (int64_t)t * p.tile_bytes;
-                const int64_t yv = (yoff >= 0 && yoff < (int64_t)nvec * 16) ? yoff / 16 : -1;
-                const int ye = (int)(y % VEC);
-                uint4 raw[NV];
-#pragma unroll
-                for (int i = 0; i < NV; ++i) {
-                    const int v = tid + i * NC;
-                    if (v < nvec) raw[i] = lds128(tile + (size_t)v * 16);
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[s]);
-#pragma unroll
-                for (int i = 0; i < NV; ++i) {
-                    const int v = tid + i * NC;
-                    if (v < nvec) {
-                        float x[VEC], o[VEC];
-                        VT::unpack(raw[i], x);
-#pragma unroll
-                        for (int e = 0; e < VEC; ++e)
-                            o[e] = fmaf(ex2_approx(fmaf(x[e], kLog2e, -lsel)), g, -bb);
-                        if ((int64_t)v == yv) {
-#pragma unroll
-                            for (int e = 0; e < VEC; ++e)
-                                if (e == ye) o[e] -= hit;
-                        }
-                        stg128_stream(gdst + (size_t)v * 16, VT::pack(o));
-                    }
+            const float2 NL = make_float2(nll, nll);
+            const float2 G2 = make_float2(g, g);
+            const float2 NB = make_float2(-bb, -bb);
+            for (int t = 0; t < p.ntiles; ++t) {
+                wait_full();
+                const uint4* tile = reinterpret_cast<const uint4*>(ring + (size_t)rg.s * TB);
+                uint4* dst = reinterpret_cast<uint4*>(rowp + (size_t)t * TB);
+                if (t < p.ntiles - 1)
+                    grad_tile<T, NC, NV, true>(tile, dst, tid, TV, NL, G2, NB);
+                else
+                    grad_tile<T, NC, NV, false>(tile, dst, tid, last_nvec, NL, G2, NB);
+                release();
+                // the target element: the thread that stored its vector rewrites
+                // it with the one-hot term subtracted (same thread, so the second
+                // store lands after the first)
+                if (t == ty && tid == yv % NC) {
+                    const float e = ex2_approx(fmaf(xy, kLog2e, nll));
+                    VT::store1(rowp + ybyte, fmaf(e, g, -bb) - g * (1.f - p.a));
                 }
             }
         }
@@ -289,7 +338,7 @@ cudaError_t launch_stream_one(const Problem& pb, const StreamPlan& plan, cudaStr
     a.N = pb.N;
     a.V = (int32_t)pb.V;
     a.stages = plan.stages;
-    a.tile_bytes = (uint32_t)(NC * NV * 16);
+    a.tile_bytes = (uint32_t)(NC * NV * 16);  // must match the kernel's TB
     const int64_t row_bytes = pb.V * (int64_t)sizeof(T);
     a.ntiles = (int32_t)((row_bytes + a.tile_bytes - 1) / a.tile_bytes);
     a.last_bytes = (uint32_t)(row_bytes - (int64_t)(a.ntiles - 1) * a.tile_bytes);
@@ -306,7 +355,7 @@ cudaError_t launch_stream_one(const Problem& pb, const StreamPlan& plan, cudaStr
     a.n_dev = pb.n_dev;
     a.err = pb.err;
     a.l2_keep = plan.l2_keep;
-    const size_t smem = (size_t)plan.stages * a.tile_bytes + 16 * sizeof(uint64_t) +
+    const size_t smem = (size_t)plan.stages * a.tile_bytes + 24 * sizeof(uint64_t) +
                         2 * NW * sizeof(float4) + 2 * sizeof(float) + 16;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -324,10 +373,14 @@ cudaError_t launch_stream_one(const Problem& pb, const StreamPlan& plan, cudaStr
     return cudaGetLastError();
 }
 
+// Tiles of 16 or 32 KB, consumed by 256 or 512 threads.
 template <typename T, bool GRAD>
 cudaError_t launch_stream_typed(const Problem& pb, const StreamPlan& plan, cudaStream_t s) {
-    if (plan.threads == 512) return launch_stream_one<T, 512, 2, GRAD>(pb, plan, s);
-    return launch_stream_one<T, 256, 4, GRAD>(pb, plan, s);
+    if (plan.tile_kb == 16)
+        return plan.threads == 512 ? launch_stream_one<T, 512, 2, GRAD>(pb, plan, s)
+                                   : launch_stream_one<T, 256, 4, GRAD>(pb, plan, s);
+    return plan.threads == 512 ? launch_stream_one<T, 512, 4, GRAD>(pb, plan, s)
+                               : launch_stream_one<T, 256, 8, GRAD>(pb, plan, s);
 }
 
 }  // namespace
