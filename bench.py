@@ -34,7 +34,7 @@ if ROOT not in sys.path:
 
 METRIC = "CE fwd+bwd tokens/s at V=128000 bf16; achieved HBM GB/s vs GB300 peak"
 DEFAULT_WORKLOAD = "c5t_bsv128000_bf16"
-KERNELS_PER_STEP = {1: 3, 2: 3, 3: 4, 4: 3}   # count + main (+ second stage) + mean
+KERNELS_PER_STEP = {1: 3, 2: 3, 3: 4, 4: 2}   # count + main (+ second stage) (+ mean)
 CLOCK_FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
                 "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
                 "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]

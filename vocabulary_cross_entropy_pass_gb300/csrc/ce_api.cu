@@ -36,9 +36,9 @@ struct Plan {
 // `stages` of them in flight.  Defaults from sweeps on the (4,4096,128000)
 // bf16 workload.
 bool plan_stream(const ce_options* o, StreamPlan* sp) {
-    sp->threads = (o && o->tune_threads) ? o->tune_threads : 512;
-    sp->tile_kb = (o && o->tune_tile_kb) ? o->tune_tile_kb : 32;
-    sp->stages = (o && o->tune_stages) ? o->tune_stages : (sp->tile_kb == 32 ? 6 : 10);
+    sp->threads = (o && o->tune_threads) ? o->tune_threads : 256;
+    sp->tile_kb = (o && o->tune_tile_kb) ? o->tune_tile_kb : 16;
+    sp->stages = (o && o->tune_stages) ? o->tune_stages : (sp->tile_kb == 32 ? 5 : 12);
     sp->ctas_per_sm_cap = o ? o->tune_ctas_per_sm : 0;
     sp->l2_keep = (o && o->tune_l2_keep == 2) ? 0 : 1;
     const size_t tile = (size_t)sp->tile_kb * 1024;
@@ -178,6 +178,10 @@ ce_status run_pass(Problem& pb, const ce_options* o, float* loss_out, int64_t* n
     char* w = static_cast<char*>(ws);
     pb.err = reinterpret_cast<uint32_t*>(w + kWsErrOffset);
     pb.n_dev = reinterpret_cast<int64_t*>(w + kWsCountOffset);
+    pb.ticket = reinterpret_cast<uint32_t*>(w + kWsTicketOffset);
+    // the stream kernel computes the mean itself (its last CTA)
+    const bool mean_in_kernel = pb.reduce && pl.path == CE_PATH_STREAM && pb.N > 0;
+    pb.mean_out = mean_in_kernel ? loss_out : nullptr;
     float* rows = reinterpret_cast<float*>(w + kWsHeaderBytes);
     float4* parts = reinterpret_cast<float4*>(
         w + kWsHeaderBytes + align_up((size_t)pb.N * sizeof(float), 256));
@@ -198,7 +202,8 @@ ce_status run_pass(Problem& pb, const ce_options* o, float* loss_out, int64_t* n
         if (e != cudaSuccess) return CE_ERR_LAUNCH;
     }
     if (ee && cudaEventRecord(ee, s) != cudaSuccess) return CE_ERR_LAUNCH;
-    if (pb.reduce && launch_reduce_mean(pb, loss_out, s) != cudaSuccess) return CE_ERR_LAUNCH;
+    if (pb.reduce && !mean_in_kernel && launch_reduce_mean(pb, loss_out, s) != cudaSuccess)
+        return CE_ERR_LAUNCH;
     return CE_OK;
 }
 

@@ -20,7 +20,10 @@ constexpr int kAuxThreads = 1024;
 __global__ void __launch_bounds__(kAuxThreads)
 ce_count_kernel(const int64_t* __restrict__ targets, int64_t ts0, int64_t ts1, int64_t dim1,
                 int64_t N, int64_t V, int64_t ignore_idx, int64_t* n_ws, int64_t* n_out,
-                uint32_t* err) {
+                uint32_t* err, uint32_t* ticket) {
+    // the pass launched after this kernel may start now: it waits for this
+    // kernel's results itself (griddepcontrol.wait) before it reads them
+    griddep_launch_dependents();
     __shared__ long long s_n[kAuxThreads / 32];
     __shared__ unsigned s_e[kAuxThreads / 32];
     long long n = 0;
@@ -52,7 +55,8 @@ ce_count_kernel(const int64_t* __restrict__ targets, int64_t ts0, int64_t ts1, i
         }
         *n_ws = tn;
         if (n_out) *n_out = tn;
-        *err = te;  // starts the error word of this pass
+        *err = te;     // starts the error word of this pass
+        *ticket = 0u;  // no CTA of the pass has finished yet
     }
 }
 
@@ -78,8 +82,13 @@ ce_mean_kernel(const float* __restrict__ loss_rows, int64_t N, const int64_t* n_
 
 cudaError_t launch_count(const Problem& p, int64_t* n_out, cudaStream_t s) {
     ce_count_kernel<<<1, kAuxThreads, 0, s>>>(p.targets, p.ts0, p.ts1, p.dim1, p.N, p.V,
-                                              p.ignore_idx, p.n_dev, n_out, p.err);
+                                              p.ignore_idx, p.n_dev, n_out, p.err, p.ticket);
     return cudaGetLastError();
+}
+
+void set_pdl_attr(cudaLaunchAttribute* attr) {
+    attr->id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr->val.programmaticStreamSerializationAllowed = 1;
 }
 
 cudaError_t launch_reduce_mean(const Problem& p, float* loss_out, cudaStream_t s) {

@@ -136,6 +136,15 @@ __device__ __forceinline__ float4 ld_dsmem_f4(const void* local, uint32_t rank) 
     return v;
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start before the previous kernel on the stream ends;
+// griddep_wait() blocks until that kernel has finished and its writes are
+// visible, griddep_launch_dependents() lets the next kernel start early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint4 lds128(const void* p) {
     return *reinterpret_cast<const uint4*>(p);
 }

@@ -13,10 +13,12 @@ namespace gbce {
 // Workspace layout (byte offsets from the caller's workspace pointer):
 //   [0, 4)      uint32 device error word
 //   [8, 16)     int64 n_non_ignore of the last pass
+//   [16, 20)    uint32 count of CTAs done (the stream kernel's in-kernel mean)
 //   [256, ...)  float per-row losses (N) -- used when reduce_loss
 //   [...]       float4 per-(row, chunk) partials of the two-stage path
 constexpr size_t kWsErrOffset = 0;
 constexpr size_t kWsCountOffset = 8;
+constexpr size_t kWsTicketOffset = 16;
 constexpr size_t kWsHeaderBytes = 256;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -38,6 +40,8 @@ struct Problem {
     bool grad;                 // write the gradient in place
     uint32_t* err;             // device error word
     int64_t* n_dev;            // device count
+    uint32_t* ticket;          // CTAs-done counter, zeroed by the count kernel
+    float* mean_out;           // stream path with reduce_loss: the mean, written in-kernel
 };
 
 // Plan of the fused (row / cluster) kernel.
@@ -70,6 +74,8 @@ int fused_capacity(int dtype, int threads);  // elements one CTA can hold
 int split_auto_chunks(int64_t V);
 
 cudaError_t launch_count(const Problem& p, int64_t* n_out, cudaStream_t s);
+// the count kernel and the pass after it overlap (programmatic dependent launch)
+void set_pdl_attr(cudaLaunchAttribute* attr);
 cudaError_t launch_reduce_mean(const Problem& p, float* loss_out, cudaStream_t s);
 cudaError_t launch_fused(const Problem& p, const FusedPlan& plan, cudaStream_t s);
 cudaError_t launch_stream(const Problem& p, const StreamPlan& plan, cudaStream_t s);

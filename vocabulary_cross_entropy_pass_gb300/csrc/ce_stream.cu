@@ -48,6 +48,8 @@ struct StreamArgs {
     const int64_t* n_dev;
     uint32_t* err;
     int l2_keep;           // 1: pass-1 copies ask L2 to keep the row for pass 2
+    uint32_t* ticket;      // CTAs done (zeroed by the count kernel)
+    float* mean_out;       // reduce_loss: the last CTA to finish writes the mean here
 };
 
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
@@ -165,6 +167,7 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
     float4* red = reinterpret_cast<float4*>(empty + 12);  // [2][NW]
     float* xy_s = reinterpret_cast<float*>(red + 2 * NW);  // [2]
     volatile int* abort_flag = reinterpret_cast<volatile int*>(xy_s + 2);
+    volatile int* last_flag = abort_flag + 1;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) {
@@ -173,6 +176,7 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
             mbar_init(&empty[s], NW);
         }
         *abort_flag = 0;
+        *last_flag = 0;
         fence_barrier_init();
     }
     __syncthreads();
@@ -204,6 +208,7 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
                 for (int pass = 0; pass < npass && !*abort_flag; ++pass) {
                     for (int t = 0; t < p.ntiles; ++t) {
                         if (!mbar_wait_bounded(&empty[rg.s], rg.ph ^ 1u)) {
+                            griddep_wait();  // the count kernel starts the error word
                             atomicOr(p.err, CE_DEVERR_TIMEOUT);
                             *abort_flag = 1;
                             break;
@@ -231,6 +236,9 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
     }
 
     // ------------------------------------------------------------ consumer warps
+    // the count kernel before this one may still run: wait for n and the
+    // error word (the producer's first copies are already in flight)
+    griddep_wait();
     float g_reduce = 1.f;
     if (p.reduce) g_reduce = (p.dloss ? __ldg(p.dloss) : 1.f) / (float)(*p.n_dev);
     Ring rg(p.stages);
@@ -324,6 +332,34 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
         }
         par ^= 1;
     }
+
+    // reduce_loss: the last CTA to finish sums the per-row losses in a fixed
+    // order (fixed strides per thread, butterflies, warps in order) -- the
+    // mean of TENPU #29 section 1, computed on the device
+    if (p.mean_out) {
+        named_bar_sync(1, NC);  // every loss row of this CTA is written
+        if (tid == 0) {
+            __threadfence();
+            const unsigned t = atomicAdd(p.ticket, 1u);
+            *last_flag = (t == gridDim.x - 1) ? 1 : 0;
+        }
+        named_bar_sync(1, NC);
+        if (*last_flag) {
+            __threadfence();
+            double acc = 0.0;
+            for (int64_t r = tid; r < p.N; r += NC) acc += (double)__ldcg(p.loss + r);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(kFull, acc, off);
+            double* dred = reinterpret_cast<double*>(red);
+            if (lane == 0) dred[warp] = acc;
+            named_bar_sync(1, NC);
+            if (tid == 0) {
+                double tot = 0.0;
+                for (int w = 0; w < NW; ++w) tot += dred[w];
+                p.mean_out[0] = (float)(tot / (double)(*p.n_dev));  // 0/0 = NaN: all ignored
+            }
+        }
+    }
 }
 
 template <typename T, int NC, int NV, bool GRAD>
@@ -355,8 +391,10 @@ cudaError_t launch_stream_one(const Problem& pb, const StreamPlan& plan, cudaStr
     a.n_dev = pb.n_dev;
     a.err = pb.err;
     a.l2_keep = plan.l2_keep;
+    a.ticket = pb.ticket;
+    a.mean_out = pb.mean_out;
     const size_t smem = (size_t)plan.stages * a.tile_bytes + 24 * sizeof(uint64_t) +
-                        2 * NW * sizeof(float4) + 2 * sizeof(float) + 16;
+                        2 * NW * sizeof(float4) + 2 * sizeof(float) + 2 * sizeof(int) + 16;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0, per_sm = 0;
@@ -369,8 +407,16 @@ cudaError_t launch_stream_one(const Problem& pb, const StreamPlan& plan, cudaStr
     int64_t grid = (int64_t)per_sm * sms;
     if (grid > pb.N) grid = pb.N;
     if (grid < 1) grid = 1;
-    kern<<<(unsigned)grid, NC + 32, smem, s>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    set_pdl_attr(&attr[0]);
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(NC + 32, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 // Tiles of 16 or 32 KB, consumed by 256 or 512 threads.
