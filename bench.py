@@ -60,6 +60,28 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
+def profiled_traffic(w, path: int):
+    """DRAM bytes per launch of the main kernel from the committed ncu capture
+    (profiles/ce_stream_kernel_traffic.json), scaled from the captured rows to
+    this workload's rows; None when the kernel sources changed since the
+    capture, or the workload or path differ from what was captured."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "ce_stream_kernel_traffic.json")
+    if path != 4 or not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f)
+    for rel, digest in rec["sources_sha256"].items():
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != digest:
+                return None
+    from vocabulary_cross_entropy_pass_gb300 import workloads as wl
+    cap = wl.WORKLOADS[rec["captured_workload"]]
+    if (cap.V, cap.dtype, cap.ignore_frac) != (w.V, w.dtype, w.ignore_frac):
+        return None
+    return (rec["dram_bytes_read"] + rec["dram_bytes_write"]) * w.N / rec["captured_rows"]
+
+
 def aggregate(local_ms: float, local_tokens: int, world: int, all_reduce_max=None):
     """Whole-job throughput: the units all ranks processed over the slowest
     rank's time.  all_reduce_max(x) returns the max of x over ranks."""
@@ -348,7 +370,10 @@ def run_ours(args, w, rank: int, world: int, dist) -> None:
                                          "vocab_chunks": chunks},
         "hbm_gbs_formula": nbytes * args.steps * world / (ms / 1e3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": profiled_traffic(w, path),
+                     "traffic_source": "ncu dram__bytes_read+write of the committed capture "
+                                       "(profiles/ce_stream_kernel_traffic.json) scaled by rows",
                      "peak_source": peaks["source"], "kernel_ms": kernel_ms,
                      "algorithmic_bytes": nbytes},
         "cpu_baseline": cpu,

@@ -87,3 +87,26 @@ def test_clock_summary_flags_throttling():
     c = s.summary(0.9, 1.3)
     assert c["sm_mhz"] == 1900.0 and c["sm_max_mhz"] == 2070.0
     assert c["reasons"] == ["sw_power_cap"] and c["samples"] == 3
+
+
+def test_profiled_traffic_follows_the_kernel_sources(tmp_path, monkeypatch):
+    from vocabulary_cross_entropy_pass_gb300 import workloads as wl
+    w = wl.WORKLOADS["c5t_bsv128000_bf16"]
+    t = bench.profiled_traffic(w, 4)
+    # the capture covers 4096 rows; the bench workload has 16384 (same V, dtype, ignore fraction)
+    assert t is not None and 0.85 * bench.pass_bytes(w.N, w.V, 2) < t < 1.05 * bench.pass_bytes(w.N, w.V, 2)
+    assert bench.profiled_traffic(w, 2) is None          # another path: no counters
+    assert bench.profiled_traffic(w.with_(V=64000), 4) is None
+    # a changed kernel source invalidates the counters
+    import shutil
+    root = tmp_path / "repo"
+    shutil.copytree(os.path.join(ROOT, "profiles"), root / "profiles")
+    csrc = root / "vocabulary_cross_entropy_pass_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for f in ("ce_stream.cu", "ce_device.cuh"):
+        shutil.copy(os.path.join(ROOT, "vocabulary_cross_entropy_pass_gb300", "csrc", f), csrc / f)
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    assert bench.profiled_traffic(w, 4) == t
+    with open(csrc / "ce_stream.cu", "a") as f:
+        f.write("\n// edited\n")
+    assert bench.profiled_traffic(w, 4) is None
