@@ -110,7 +110,8 @@ typedef struct {
     int tune_threads;       /* 0 = default; otherwise CTA size (256 or 512; on the stream
                                path the number of consuming threads) */
     int tune_stages;        /* 0 = default; otherwise TMA pipeline depth (2..4 rows on the
-                               row/cluster paths, 2..12 tiles on the stream path) */
+                               row/cluster paths, 2..12 tiles on the stream path, 6 or 12
+                               tiles on the warp path) */
     int tune_ctas_per_sm;   /* 0 = as many as fit; otherwise a cap */
     int tune_l2_keep;       /* stream path: 0 = default (1), 1 = the first read asks L2 to
                                keep the row for the second (evict-last), 2 = evict-first */

@@ -230,3 +230,26 @@ def test_full_size_sampled_rows():
                     targets=tsub.numpy(), label_smoothing=w.label_smoothing, dloss=scale)
     excess, _ = harness.grad_errors(g_rows.astype(np.float64), ref["grad"], "bf16")
     assert excess <= 0.0
+
+
+@pytest.mark.parametrize("V,dtype,tile_kb,stages", [(12000, "bf16", 0, 0), (16384, "bf16", 0, 0),
+                                                    (8192, "f32", 0, 0), (5000, "f32", 0, 0),
+                                                    (8192, "bf16", 16, 6), (4096, "f16", 32, 6),
+                                                    (2048, "bf16", 16, 12)])
+def test_warp_path_tiles(V, dtype, tile_kb, stages):
+    """Rows of up to one 16 or 32 KB tile on the warp-per-row path: every
+    consumer warp owns its tiles; rows, ignored rows and tiles do not line up."""
+    for N, a, red in ((1, 0.1, True), (37, 0.0, False), (301, 0.1, True)):
+        w = wl.Workload(f"warp{V}", 1, N, V, dtype, sigma=2.0, ignore_frac=0.15,
+                        label_smoothing=a, reduce_loss=red, seed=V + N)
+        opts = pkg.make_options(force_path=5, tune_tile_kb=tile_kb, tune_stages=stages)
+        x = wl.logits(w)
+        t = wl.targets(w)
+        xd, td = x.to(DEV), t.to(DEV)
+        ws = torch.empty(pkg.ce_workspace_bytes(1, N, V, xd.dtype, opts), dtype=torch.uint8,
+                         device=DEV)
+        n = torch.zeros(1, dtype=torch.int64, device=DEV)
+        loss = pkg.ce_fwd_bwd(xd, td, label_smoothing=a, reduce_loss=red, n_non_ignore_out=n,
+                              workspace=ws, opts=opts)
+        assert pkg.ce_get_error(ws) == (0, 0)
+        _compare(w, x, t, loss, xd, n)

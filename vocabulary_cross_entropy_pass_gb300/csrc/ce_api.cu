@@ -32,11 +32,13 @@ struct Plan {
     RowsPlan rows;
 };
 
-// Warp-per-row kernel: the row must fit one tile of 16 or 32 KB.
+// Warp-per-row kernel: the row must fit one tile of 16 or 32 KB; each of its
+// 6 consumer warps owns stages/6 tiles, so stages is a multiple of 6.
 bool plan_rows(int64_t row_bytes, const ce_options* o, RowsPlan* rp) {
     rp->tile_kb = (o && o->tune_tile_kb) ? o->tune_tile_kb : (row_bytes <= 16 * 1024 ? 16 : 32);
     if (row_bytes > (int64_t)rp->tile_kb * 1024) return false;
     rp->stages = (o && o->tune_stages) ? o->tune_stages : (rp->tile_kb == 16 ? 12 : 6);
+    if (rp->stages % 6 != 0) return false;
     rp->ctas_per_sm_cap = o ? o->tune_ctas_per_sm : 0;
     return rp->stages * (size_t)rp->tile_kb * 1024 + 1024 <= kSmemLimit;
 }

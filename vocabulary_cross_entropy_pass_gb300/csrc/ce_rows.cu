@@ -5,9 +5,9 @@
 // reduction of the stream kernel are the cost, not the bytes.  Here one warp
 // owns a row from start to end:
 //
-//   - a producer warp copies each kept row into the next tile of a ring with one
-//     1-D TMA bulk copy (rows of ignored targets are not read: the producer
-//     warp writes their zero gradient itself);
+//   - a producer warp copies each kept row with one 1-D TMA bulk copy into a
+//     tile of the warp that will take it (rows of ignored targets are not read:
+//     the producer warp writes their zero gradient itself);
 //   - consumer warp w takes the kept rows w, w + NW, w + 2 NW, ... of its CTA
 //     and makes three sweeps over the tile in shared memory: the row max, the
 //     sum of 2^((x - m) log2e) and the plain sum (warp shuffles combine the
@@ -15,6 +15,10 @@
 //     pitfall 1), then the gradient g (softmax - a/V) - g (1-a) [j == y]
 //     (same article, "Backward", pitfall 3, smoothing over V) stored in place
 //     over the row (TENPU #29 section 6) with 16-byte streaming stores.
+//
+// Each consumer warp owns TPW tiles of its own (TPW = stages / NW), used in
+// turn, so every mbarrier phase of a tile is waited on by that one warp, in
+// order: a parity wait can never mistake a later phase for an earlier one.
 //
 // One HBM read and one HBM write per element, two exponentials per element,
 // no barrier wider than a warp after set-up.  Every wait is bounded.
@@ -52,6 +56,8 @@ __device__ __forceinline__ uint64_t l2_evict_first() {
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
     return pol;
 }
+
+constexpr int kRowsWarps = 6;  // consumer warps per CTA
 
 template <typename T, int NW, int TB, bool GRAD>
 __global__ void __launch_bounds__(NW * 32 + 32, 1)
@@ -92,11 +98,13 @@ ce_rows_kernel(const __grid_constant__ RowsArgs p) {
         return y != p.ignore_idx && y >= 0 && y < (int64_t)p.V;
     };
     const int nvec = (int)(p.row_bytes / 16);
+    const int tpw = p.stages / NW;  // tiles per consumer warp
 
     // ------------------------------------------------------------ producer warp
     if (warp == NW) {
         const uint64_t pol = l2_evict_first();
-        uint32_t k = 0;  // kept rows issued
+        uint32_t k = 0;         // kept rows seen
+        uint32_t k_issued = 0;  // kept rows whose copy was issued (a prefix of them)
         for (int64_t r = blockIdx.x; r < p.N; r += gridDim.x) {
             const int64_t y = row_target(r);
             char* row = row_ptr(r);
@@ -113,26 +121,34 @@ ce_rows_kernel(const __grid_constant__ RowsArgs p) {
                 continue;
             }
             if (lane == 0 && !flags[0]) {
-                const int s = (int)(k % (uint32_t)p.stages);
-                const uint32_t ph = (k / (uint32_t)p.stages) & 1u;
-                if (!mbar_wait_bounded(&empty[s], ph ^ 1u)) {
+                // kept row k goes to warp k % NW, whose j-th row uses its tile j % TPW
+                const uint32_t j = k / NW;
+                const int tile = (int)(k % NW) * tpw + (int)(j % (uint32_t)tpw);
+                const uint32_t ph = (j / (uint32_t)tpw) & 1u;
+                if (!mbar_wait_bounded(&empty[tile], ph ^ 1u)) {
                     griddep_wait();  // the count kernel starts the error word
                     atomicOr(p.err, CE_DEVERR_TIMEOUT);
                     flags[0] = 1;
                 } else {
-                    mbar_arrive_expect_tx(&full[s], p.row_bytes);
-                    tma_load_1d(ring + (size_t)s * TB, row, p.row_bytes, &full[s], pol);
+                    mbar_arrive_expect_tx(&full[tile], p.row_bytes);
+                    tma_load_1d(ring + (size_t)tile * TB, row, p.row_bytes, &full[tile], pol);
+                    k_issued = k + 1;
                 }
             }
             ++k;
         }
         __syncwarp();
         if (lane == 0 && flags[0]) {
-            // let every copy already issued land before the CTA goes away
-            for (int s = 0; s < p.stages; ++s) {
-                if (k > (uint32_t)s) {
-                    const uint32_t last = (k - 1u - (uint32_t)s) / (uint32_t)p.stages;
-                    (void)mbar_wait_bounded(&full[s], last & 1u);
+            // let every copy already issued land before the CTA goes away: the
+            // last phase issued on each tile
+            for (int w = 0; w < NW; ++w) {
+                const uint32_t rows_w =
+                    (k_issued > (uint32_t)w) ? (k_issued - 1u - (uint32_t)w) / NW + 1u : 0u;
+                for (int i = 0; i < tpw; ++i) {
+                    if (rows_w > (uint32_t)i) {
+                        const uint32_t uses = (rows_w - 1u - (uint32_t)i) / (uint32_t)tpw + 1u;
+                        (void)mbar_wait_bounded(&full[w * tpw + i], (uses - 1u) & 1u);
+                    }
                 }
             }
         }
@@ -156,8 +172,9 @@ ce_rows_kernel(const __grid_constant__ RowsArgs p) {
         if (!is_loaded(y)) continue;
         const uint32_t mine = k++;
         if ((int)(mine % (uint32_t)NW) != warp) continue;
-        const int s = (int)(mine % (uint32_t)p.stages);
-        const uint32_t ph = (mine / (uint32_t)p.stages) & 1u;
+        const uint32_t j = mine / NW;  // this warp's j-th kept row
+        const int s = warp * tpw + (int)(j % (uint32_t)tpw);
+        const uint32_t ph = (j / (uint32_t)tpw) & 1u;
         if (!flags[0] && !mbar_wait_bounded(&full[s], ph)) {
             atomicOr(p.err, CE_DEVERR_TIMEOUT);
             flags[0] = 1;
@@ -307,8 +324,9 @@ cudaError_t launch_rows_one(const Problem& pb, const RowsPlan& plan, cudaStream_
 
 template <typename T, bool GRAD>
 cudaError_t launch_rows_typed(const Problem& pb, const RowsPlan& plan, cudaStream_t s) {
-    if (plan.tile_kb == 32) return launch_rows_one<T, 8, 32 * 1024, GRAD>(pb, plan, s);
-    return launch_rows_one<T, 8, 16 * 1024, GRAD>(pb, plan, s);
+    if (plan.stages % kRowsWarps != 0) return cudaErrorInvalidValue;
+    if (plan.tile_kb == 32) return launch_rows_one<T, kRowsWarps, 32 * 1024, GRAD>(pb, plan, s);
+    return launch_rows_one<T, kRowsWarps, 16 * 1024, GRAD>(pb, plan, s);
 }
 
 }  // namespace
