@@ -37,7 +37,8 @@ struct Plan {
 bool plan_rows(int64_t row_bytes, const ce_options* o, RowsPlan* rp) {
     rp->tile_kb = (o && o->tune_tile_kb) ? o->tune_tile_kb : (row_bytes <= 16 * 1024 ? 16 : 32);
     if (row_bytes > (int64_t)rp->tile_kb * 1024) return false;
-    rp->stages = (o && o->tune_stages) ? o->tune_stages : (rp->tile_kb == 16 ? 12 : 6);
+    // one tile per warp: 96 KB (16 KB tiles, two CTAs per SM) or 192 KB (32 KB)
+    rp->stages = (o && o->tune_stages) ? o->tune_stages : 6;
     if (rp->stages % 6 != 0) return false;
     rp->ctas_per_sm_cap = o ? o->tune_ctas_per_sm : 0;
     return rp->stages * (size_t)rp->tile_kb * 1024 + 1024 <= kSmemLimit;
@@ -45,11 +46,11 @@ bool plan_rows(int64_t row_bytes, const ce_options* o, RowsPlan* rp) {
 
 // Row-streaming kernel: tiles of threads*64 bytes, `stages` of them in flight.
 // Row-streaming kernel: tiles of 16 or 32 KB consumed by 256 or 512 threads,
-// `stages` of them in flight.  Defaults from sweeps on the (4,4096,128000)
-// bf16 workload.
+// `stages` of them in flight.  Defaults from sweeps over V = 32000 .. 256000
+// bf16 (32 KB x 5 was best or within 2% of best at every width).
 bool plan_stream(const ce_options* o, StreamPlan* sp) {
     sp->threads = (o && o->tune_threads) ? o->tune_threads : 256;
-    sp->tile_kb = (o && o->tune_tile_kb) ? o->tune_tile_kb : 16;
+    sp->tile_kb = (o && o->tune_tile_kb) ? o->tune_tile_kb : 32;
     sp->stages = (o && o->tune_stages) ? o->tune_stages : (sp->tile_kb == 32 ? 5 : 12);
     sp->ctas_per_sm_cap = o ? o->tune_ctas_per_sm : 0;
     sp->l2_keep = (o && o->tune_l2_keep == 2) ? 0 : 1;
