@@ -163,6 +163,31 @@ ce_status ce_fwd_only(const void* logits, ce_dtype dtype, ce_layout layout, int6
                       void* workspace, size_t workspace_bytes, const ce_options* opts,
                       void* stream);
 
+/* Backward only, from the logsumexp a forward-only pass saved: for callers
+ * that learn the upstream gradient after the forward (autograd).  Writes
+ *   grad_j = g * (exp(x_j - lse) - a/V) - g * (1-a) * [j == target]
+ * for every kept row (CSDN "Ascend CANN ops-nn cross-entropy fusion",
+ * section "Backward", pitfall 3; smoothing over all V classes) and zeros for
+ * ignored or out-of-range rows; g = dloss[0] / n_non_ignore (reduce_loss) or
+ * dloss[row] (otherwise; NULL means 1).
+ *   logits, targets, sizes, strides, label_smoothing, ignore_idx: as given to
+ *                  ce_fwd_only; the logits must be unchanged since then.
+ *   lse            float32 per flattened row, from ce_fwd_only's lse_out.
+ *   n_non_ignore   int64 count from ce_fwd_only's n_non_ignore_out; required
+ *                  when reduce_loss.
+ *   grad           gradient in the logits dtype with its own strides
+ *                  (grad_strides[2] == 1): either the logits themselves (same
+ *                  strides; the TENPU in-place staging) or memory that does
+ *                  not overlap them.
+ * One read of the logits and one write of the gradient per element; no
+ * workspace.  Returns CE_OK once the kernel is enqueued on `stream`. */
+ce_status ce_bwd(const void* logits, ce_dtype dtype, ce_layout layout, int64_t dim0, int64_t dim1,
+                 int64_t V, const int64_t strides[3], const int64_t* targets,
+                 const int64_t target_strides[2], const float* lse, float label_smoothing,
+                 int64_t ignore_idx, int reduce_loss, const float* dloss,
+                 const int64_t* n_non_ignore, void* grad, const int64_t grad_strides[3],
+                 void* stream);
+
 /* ce_fwd_bwd without a workspace argument: the pass keeps its scratch in a
  * fixed 2 MiB array of device memory that the library itself reserves on
  * every GPU where it is loaded (held until the process exits).  The pages have

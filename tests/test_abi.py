@@ -143,3 +143,24 @@ def test_overlapping_rows_rejected_for_in_place_gradient(lib):
     # a transposed (SQ, B, V) storage read as (B, SQ, V) passes the host checks
     # and fails later only for want of a GPU
     assert _call(lib, d0=2, d1=3, strides=(4096, 2 * 4096, 1)) not in (1, 2, 3, 4)
+
+
+def test_bwd_host_validation(lib):
+    def call(**kw):
+        a = dict(logits=0x1000, dtype=1, d0=2, d1=3, V=4096, st=(3 * 4096, 4096, 1), tgt=0x2000,
+                 ts=(3, 1), lse=0x3000, a=0.0, reduce=0, dloss=None, n=None, grad=0x9000,
+                 gst=(3 * 4096, 4096, 1))
+        a.update(kw)
+        return lib.ce_bwd(ctypes.c_void_p(a["logits"]), a["dtype"], 0, a["d0"], a["d1"], a["V"],
+                          _lib.i64_array(a["st"]), ctypes.c_void_p(a["tgt"]),
+                          _lib.i64_array(a["ts"]), ctypes.c_void_p(a["lse"]), a["a"], -100,
+                          a["reduce"], ctypes.c_void_p(a["dloss"]), ctypes.c_void_p(a["n"]),
+                          ctypes.c_void_p(a["grad"]), _lib.i64_array(a["gst"]), None)
+    assert call(lse=0) == 1
+    assert call(grad=0) == 1
+    assert call(reduce=1) == 1                       # the mean needs the forward's count
+    assert call(gst=(3 * 4096, 4096, 2)) == 3
+    assert call(gst=(0, 4096, 1)) == 3               # gradient rows may not share memory
+    assert call(grad=0x1000, gst=(4096, 2 * 4096, 1)) == 3  # in place means the same strides
+    assert call(dtype=9) == 2
+    assert call(d0=0) == 0                            # nothing to do

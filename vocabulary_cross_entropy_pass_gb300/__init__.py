@@ -6,11 +6,14 @@ entry points keep the C names:
 
   ce_fwd_bwd(logits, targets, ...)   loss; the gradient overwrites logits
   ce_fwd_only(logits, targets, ...)  loss (and optionally lse); logits kept
+  ce_bwd(logits, targets, lse, ...)  gradient from a saved lse
   ce_workspace_bytes(...), ce_get_error(...), ce_status_string(...),
-  ce_plan_path(...)
+  ce_plan_path(...), ce_fwd_bwd_noalloc(...)
 
 whose arguments follow the TENPU "Parallel Cross Entropy (Triton)" interface
-(Ascend/TransformerEngineNPU issue #29, section 1).
+(Ascend/TransformerEngineNPU issue #29, section 1), and
+``parallel_cross_entropy`` wraps ce_fwd_only + ce_bwd in a
+torch.autograd.Function with that interface's argument list.
 
 Importing the package does not load the library; the first call does, and
 raises if it is missing.  There is no CPU fallback.
@@ -25,7 +28,7 @@ from . import _lib
 from ._lib import (CE_PATH_AUTO, CE_PATH_CLUSTER, CE_PATH_ROW, CE_PATH_STREAM,
                    CE_PATH_TWO_STAGE, CE_PATH_WARP, CEError, ce_options, make_options)
 
-__all__ = ["ce_fwd_bwd", "ce_fwd_bwd_noalloc", "ce_fwd_only", "ce_workspace_bytes", "ce_get_error", "ce_status_string",
+__all__ = ["ce_fwd_bwd", "ce_fwd_bwd_noalloc", "ce_fwd_only", "ce_bwd", "parallel_cross_entropy", "ce_workspace_bytes", "ce_get_error", "ce_status_string",
            "ce_plan_path", "CEError", "make_options", "ce_options",
            "CE_PATH_AUTO", "CE_PATH_ROW", "CE_PATH_CLUSTER", "CE_PATH_TWO_STAGE", "CE_PATH_STREAM", "CE_PATH_WARP"]
 
@@ -216,3 +219,79 @@ def ce_get_error(workspace: torch.Tensor, stream=None) -> tuple[int, int]:
 def ce_status_string(status: int) -> str:
     return _lib.load().ce_status_string(int(status)).decode()
 
+
+
+def ce_bwd(logits: torch.Tensor, targets: torch.Tensor, lse: torch.Tensor,
+           label_smoothing: float = 0.0, ignore_idx: int = -100, reduce_loss: bool = False,
+           dloss: torch.Tensor | None = None, n_non_ignore: torch.Tensor | None = None,
+           grad: torch.Tensor | None = None, layout: str = "bsv", stream=None) -> torch.Tensor:
+    """Gradient of the cross-entropy from the ``lse`` a forward-only pass saved.
+    ``grad`` may be ``logits`` itself (in place) or a separate tensor of the
+    same shape and dtype (allocated when None).  ``n_non_ignore`` (int64 CUDA
+    tensor from the forward) is needed for reduce_loss."""
+    _check(logits, targets)
+    lib = _lib.load()
+    d0, d1, V, st = _dims(logits)
+    ts = _tstrides(targets, d0, d1)
+    if grad is None:
+        grad = torch.empty_like(logits)
+    if grad.shape != logits.shape or grad.dtype != logits.dtype or not grad.is_cuda:
+        raise ValueError("grad must match logits in shape and dtype, on the GPU")
+    gst = _dims(grad)[3]
+    for tens, name in ((lse, "lse"), (dloss, "dloss")):
+        if tens is not None and (tens.dtype != torch.float32 or not tens.is_cuda):
+            raise TypeError(f"{name} must be a float32 CUDA tensor")
+    rc = lib.ce_bwd(ctypes.c_void_p(logits.data_ptr()), _DTYPE[logits.dtype], _LAYOUT[layout], d0,
+                    d1, V, _lib.i64_array(st), ctypes.c_void_p(targets.data_ptr()),
+                    _lib.i64_array(ts), ctypes.c_void_p(lse.data_ptr()), float(label_smoothing),
+                    int(ignore_idx), int(bool(reduce_loss)),
+                    ctypes.c_void_p(dloss.data_ptr() if dloss is not None else None),
+                    ctypes.c_void_p(n_non_ignore.data_ptr() if n_non_ignore is not None else None),
+                    ctypes.c_void_p(grad.data_ptr()), _lib.i64_array(gst),
+                    _stream(logits.device, stream))
+    _raise(rc, "ce_bwd")
+    return grad
+
+
+class _ParallelCrossEntropy(torch.autograd.Function):
+    """Forward: ce_fwd_only (loss, lse and the kept-row count saved).
+    Backward: ce_bwd with the upstream gradient, into a new tensor or, with
+    ``inplace_grad``, over the logits (the in-place staging of TENPU #29
+    section 6: the caller gives up the logits)."""
+
+    @staticmethod
+    def forward(ctx, inp, target, label_smoothing, reduce_loss, ignore_idx, layout, inplace_grad):
+        x = inp if inp.stride(-1) == 1 else inp.contiguous()
+        d0, d1, V, _ = _dims(x)
+        lse = torch.empty(d0 * d1, dtype=torch.float32, device=x.device)
+        n = torch.empty(1, dtype=torch.int64, device=x.device)
+        loss = ce_fwd_only(x, target, label_smoothing=label_smoothing, ignore_idx=ignore_idx,
+                           reduce_loss=reduce_loss, layout=layout, lse_out=lse,
+                           n_non_ignore_out=n)
+        ctx.save_for_backward(x, target, lse, n)
+        ctx.cfg = (label_smoothing, reduce_loss, ignore_idx, layout, inplace_grad)
+        return loss.view(()) if reduce_loss else loss.view(target.shape)
+
+    @staticmethod
+    def backward(ctx, grad_out):
+        x, target, lse, n = ctx.saved_tensors
+        a, reduce_loss, ignore_idx, layout, inplace_grad = ctx.cfg
+        dl = grad_out.detach().to(torch.float32).contiguous().reshape(-1)
+        g = ce_bwd(x, target, lse, label_smoothing=a, ignore_idx=ignore_idx,
+                   reduce_loss=reduce_loss, dloss=dl, n_non_ignore=n,
+                   grad=x if inplace_grad else None, layout=layout)
+        return g, None, None, None, None, None, None
+
+
+def parallel_cross_entropy(inp: torch.Tensor, target: torch.Tensor, label_smoothing: float = 0.0,
+                           reduce_loss: bool = False, dist_process_group=None,
+                           ignore_idx: int = -100, layout: str = "bsv",
+                           inplace_grad: bool = False) -> torch.Tensor:
+    """Cross-entropy with autograd, argument list of TENPU #29 section 1.
+    Returns the per-token loss (shape of ``target``) or the mean over kept
+    tokens (``reduce_loss``); ``backward`` fills ``inp.grad`` through ce_bwd.
+    One GPU only: ``dist_process_group`` must be None."""
+    if dist_process_group is not None:
+        raise NotImplementedError("vocabulary-parallel process groups are not supported: one GPU")
+    return _ParallelCrossEntropy.apply(inp, target, label_smoothing, reduce_loss, ignore_idx,
+                                       layout, inplace_grad)

@@ -323,6 +323,57 @@ ce_status ce_fwd_only(const void* logits, ce_dtype dtype, ce_layout layout, int6
                     static_cast<cudaStream_t>(stream));
 }
 
+ce_status ce_bwd(const void* logits, ce_dtype dtype, ce_layout layout, int64_t dim0, int64_t dim1,
+                 int64_t V, const int64_t strides[3], const int64_t* targets,
+                 const int64_t target_strides[2], const float* lse, float label_smoothing,
+                 int64_t ignore_idx, int reduce_loss, const float* dloss,
+                 const int64_t* n_non_ignore, void* grad, const int64_t grad_strides[3],
+                 void* stream) {
+    if (dtype < CE_F32 || dtype > CE_F16) return CE_ERR_UNSUPPORTED_DTYPE;
+    if (layout != CE_LAYOUT_BSV && layout != CE_LAYOUT_SBV) return CE_ERR_INVALID_ARG;
+    if (!strides || !target_strides || !grad_strides) return CE_ERR_INVALID_ARG;
+    if (dim0 < 0 || dim1 < 0 || V < 1 || V > 0x7fffffffLL) return CE_ERR_INVALID_ARG;
+    if (!(label_smoothing >= 0.f && label_smoothing <= 1.f)) return CE_ERR_INVALID_ARG;
+    const int64_t N = dim0 * dim1;
+    if (N > 0 && (!logits || !targets || !lse || !grad)) return CE_ERR_INVALID_ARG;
+    if (N > 0 && reduce_loss && !n_non_ignore) return CE_ERR_INVALID_ARG;
+    if (strides[2] != 1 || strides[0] < 0 || strides[1] < 0) return CE_ERR_BAD_STRIDE;
+    if (grad_strides[2] != 1 || grad_strides[0] < 0 || grad_strides[1] < 0) return CE_ERR_BAD_STRIDE;
+    if (target_strides[0] < 0 || target_strides[1] < 0) return CE_ERR_BAD_STRIDE;
+    if (!rows_disjoint(dim0, dim1, V, grad_strides[0], grad_strides[1])) return CE_ERR_BAD_STRIDE;
+    if (grad == logits && (grad_strides[0] != strides[0] || grad_strides[1] != strides[1]))
+        return CE_ERR_BAD_STRIDE;
+    if (N == 0) return CE_OK;
+    BwdProblem bp;
+    memset(&bp, 0, sizeof bp);
+    const int es = elem_size(dtype);
+    bp.logits = static_cast<const char*>(logits);
+    bp.grad = static_cast<char*>(grad);
+    bp.dtype = dtype;
+    bp.dim1 = dim1;
+    bp.N = N;
+    bp.V = V;
+    bp.s0 = strides[0];
+    bp.s1 = strides[1];
+    bp.gs0 = grad_strides[0];
+    bp.gs1 = grad_strides[1];
+    bp.targets = targets;
+    bp.ts0 = target_strides[0];
+    bp.ts1 = target_strides[1];
+    bp.ignore_idx = ignore_idx;
+    bp.lse = lse;
+    bp.a = label_smoothing;
+    bp.reduce = reduce_loss ? 1 : 0;
+    bp.dloss = dloss;
+    bp.n_dev = n_non_ignore;
+    bp.vec_ok = reinterpret_cast<uintptr_t>(logits) % 16 == 0 &&
+                reinterpret_cast<uintptr_t>(grad) % 16 == 0 && (V * es) % 16 == 0 &&
+                (strides[0] * es) % 16 == 0 && (strides[1] * es) % 16 == 0 &&
+                (grad_strides[0] * es) % 16 == 0 && (grad_strides[1] * es) % 16 == 0;
+    if (launch_bwd(bp, static_cast<cudaStream_t>(stream)) != cudaSuccess) return CE_ERR_LAUNCH;
+    return CE_OK;
+}
+
 ce_status ce_get_error(const void* workspace, void* stream, uint32_t* host_err) {
     if (!workspace || !host_err) return CE_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -75,6 +75,23 @@ struct SplitPlan {
     int64_t chunk;             // elements per chunk (ceil(V/K))
 };
 
+// The backward from a saved logsumexp.
+struct BwdProblem {
+    const char* logits;
+    char* grad;
+    int dtype;
+    int64_t dim1, N, V;
+    int64_t s0, s1, gs0, gs1;  // element strides of logits and gradient rows
+    const int64_t* targets;
+    int64_t ts0, ts1, ignore_idx;
+    const float* lse;
+    float a;
+    int reduce;
+    const float* dloss;
+    const int64_t* n_dev;
+    bool vec_ok;               // every row of both tensors 16-byte aligned
+};
+
 int elem_size(int dtype);
 bool fused_aligned(const Problem& p);
 int fused_capacity(int dtype, int threads);  // elements one CTA can hold
@@ -87,6 +104,7 @@ cudaError_t launch_reduce_mean(const Problem& p, float* loss_out, cudaStream_t s
 cudaError_t launch_fused(const Problem& p, const FusedPlan& plan, cudaStream_t s);
 cudaError_t launch_stream(const Problem& p, const StreamPlan& plan, cudaStream_t s);
 cudaError_t launch_rows(const Problem& p, const RowsPlan& plan, cudaStream_t s);
+cudaError_t launch_bwd(const BwdProblem& bp, cudaStream_t s);
 cudaError_t launch_split(const Problem& p, const SplitPlan& plan, float4* partials,
                          cudaStream_t s);
 
