@@ -188,6 +188,57 @@ ce_status ce_bwd(const void* logits, ce_dtype dtype, ce_layout layout, int64_t d
                  const int64_t* n_non_ignore, void* grad, const int64_t grad_strides[3],
                  void* stream);
 
+/* Vocabulary-parallel cross-entropy (mindspore/hyper-parallel #269, section
+ * 3.1: each tensor-parallel rank holds a ceil(V/tp) slice of the vocabulary;
+ * per-row (max, sum-exp) statistics of the slice, a MAX all-reduce and a SUM
+ * all-reduce of the rescaled sums and a gather of the target logit -- TENPU
+ * #29 section 6's m_d_Xy gather -- then a backward without collectives).  The
+ * three calls below are the three steps; a caller with one GPU runs them over
+ * vocabulary shards held as separate tensors, a caller with several ranks
+ * would all-gather the partials between steps 1 and 2.
+ *
+ * Step 1: statistics of one shard.
+ *   shard_logits   (dim0, dim1, V_shard) columns [vocab_offset, vocab_offset +
+ *                  V_shard) of the vocabulary; strides as for ce_fwd_bwd.
+ *   targets        global vocabulary indices, as for ce_fwd_bwd.
+ *   partials       float32 [dim0*dim1][4], 16-byte aligned: per flattened row
+ *                  {max, sum of exp(x - max), sum of x, target logit if the
+ *                  target lies in this shard else 0}; ignored rows get
+ *                  {-inf, 0, 0, 0}. */
+ce_status ce_vp_partials(const void* shard_logits, ce_dtype dtype, int64_t dim0, int64_t dim1,
+                         int64_t V_shard, const int64_t strides[3], const int64_t* targets,
+                         const int64_t target_strides[2], int64_t vocab_offset, int64_t ignore_idx,
+                         float* partials, void* stream);
+
+/* Step 2: combine the partials of all shards, in shard order.
+ *   partials       num_shards consecutive blocks of [dim0*dim1][4] (shard k's
+ *                  block k), 1 <= num_shards <= 64.
+ *   shard_offsets  HOST array of num_shards + 1 increasing column offsets:
+ *                  shard k covers [shard_offsets[k], shard_offsets[k+1]);
+ *                  shard_offsets[0] = 0, shard_offsets[num_shards] = V.
+ *   loss_out, reduce_loss, n_non_ignore_out, workspace: as for ce_fwd_bwd
+ *                  (workspace of ce_workspace_bytes(dim0, dim1, V, dtype, NULL)).
+ *   lse_out        float32 logsumexp per flattened row (required: step 3 needs
+ *                  it); NaN for ignored or out-of-range rows.
+ * Out-of-range targets set CE_DEVERR_TARGET_RANGE in the workspace. */
+ce_status ce_vp_combine(const float* partials, int num_shards, const int64_t* shard_offsets,
+                        int64_t dim0, int64_t dim1, const int64_t* targets,
+                        const int64_t target_strides[2], float label_smoothing, int64_t ignore_idx,
+                        int reduce_loss, float* loss_out, float* lse_out,
+                        int64_t* n_non_ignore_out, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
+/* Step 3: the gradient of one shard from the combined lse -- ce_bwd for the
+ * columns [vocab_offset, vocab_offset + V_shard) of a V_total vocabulary (the
+ * smoothing share is a / V_total; the one-hot term lands in the shard that
+ * holds the target).  Other arguments as for ce_bwd. */
+ce_status ce_vp_bwd(const void* shard_logits, ce_dtype dtype, int64_t dim0, int64_t dim1,
+                    int64_t V_shard, const int64_t strides[3], const int64_t* targets,
+                    const int64_t target_strides[2], int64_t vocab_offset, int64_t V_total,
+                    const float* lse, float label_smoothing, int64_t ignore_idx, int reduce_loss,
+                    const float* dloss, const int64_t* n_non_ignore, void* grad,
+                    const int64_t grad_strides[3], void* stream);
+
 /* ce_fwd_bwd without a workspace argument: the pass keeps its scratch in a
  * fixed 2 MiB array of device memory that the library itself reserves on
  * every GPU where it is loaded (held until the process exits).  The pages have

@@ -164,3 +164,29 @@ def test_bwd_host_validation(lib):
     assert call(grad=0x1000, gst=(4096, 2 * 4096, 1)) == 3  # in place means the same strides
     assert call(dtype=9) == 2
     assert call(d0=0) == 0                            # nothing to do
+
+
+def test_vocab_parallel_host_validation(lib):
+    def comb(offs, R=None, **kw):
+        R = len(offs) - 1 if R is None else R
+        a = dict(part=0x1000, d0=1, d1=4, tgt=0x2000, ts=(4, 1), a=0.0, reduce=0, loss=0x3000,
+                 lse=0x4000, n=None, ws=0x5000, wsb=1 << 20)
+        a.update(kw)
+        return lib.ce_vp_combine(ctypes.c_void_p(a["part"]), R, _lib.i64_array(offs), a["d0"],
+                                 a["d1"], ctypes.c_void_p(a["tgt"]), _lib.i64_array(a["ts"]),
+                                 a["a"], -100, a["reduce"], ctypes.c_void_p(a["loss"]),
+                                 ctypes.c_void_p(a["lse"]), ctypes.c_void_p(a["n"]),
+                                 ctypes.c_void_p(a["ws"]), a["wsb"], None)
+    assert comb([0, 10, 10, 30]) == 1          # empty shard: offsets must increase
+    assert comb([1, 10, 30]) == 1              # must start at column 0
+    assert comb(list(range(0, 66 * 10, 10))) == 1  # at most 64 shards
+    assert comb([0, 10, 30], lse=0) == 1       # step 3 needs the lse
+    assert comb([0, 10, 30], wsb=10) == 4
+    assert lib.ce_vp_partials(ctypes.c_void_p(0x1000), 1, 1, 4, 16, _lib.i64_array((64, 16, 1)),
+                              ctypes.c_void_p(0x2000), _lib.i64_array((4, 1)), 0, -100,
+                              ctypes.c_void_p(0x3008), None) == 1  # partials not 16-byte aligned
+    # the shard must lie inside the vocabulary
+    assert lib.ce_vp_bwd(ctypes.c_void_p(0x1000), 1, 1, 4, 16, _lib.i64_array((64, 16, 1)),
+                         ctypes.c_void_p(0x2000), _lib.i64_array((4, 1)), 40, 50,
+                         ctypes.c_void_p(0x3000), 0.0, -100, 0, None, None,
+                         ctypes.c_void_p(0x4000), _lib.i64_array((64, 16, 1)), None) == 1

@@ -28,7 +28,8 @@ from . import _lib
 from ._lib import (CE_PATH_AUTO, CE_PATH_CLUSTER, CE_PATH_ROW, CE_PATH_STREAM,
                    CE_PATH_TWO_STAGE, CE_PATH_WARP, CEError, ce_options, make_options)
 
-__all__ = ["ce_fwd_bwd", "ce_fwd_bwd_noalloc", "ce_fwd_only", "ce_bwd", "parallel_cross_entropy", "ce_workspace_bytes", "ce_get_error", "ce_status_string",
+__all__ = ["ce_fwd_bwd", "ce_fwd_bwd_noalloc", "ce_fwd_only", "ce_bwd", "parallel_cross_entropy",
+           "ce_vp_partials", "ce_vp_combine", "ce_vp_bwd", "vocab_parallel_cross_entropy", "ce_workspace_bytes", "ce_get_error", "ce_status_string",
            "ce_plan_path", "CEError", "make_options", "ce_options",
            "CE_PATH_AUTO", "CE_PATH_ROW", "CE_PATH_CLUSTER", "CE_PATH_TWO_STAGE", "CE_PATH_STREAM", "CE_PATH_WARP"]
 
@@ -295,3 +296,103 @@ def parallel_cross_entropy(inp: torch.Tensor, target: torch.Tensor, label_smooth
         raise NotImplementedError("vocabulary-parallel process groups are not supported: one GPU")
     return _ParallelCrossEntropy.apply(inp, target, label_smoothing, reduce_loss, ignore_idx,
                                        layout, inplace_grad)
+
+
+# ---------------------------------------------------------------- vocabulary parallel
+def ce_vp_partials(shard: torch.Tensor, targets: torch.Tensor, vocab_offset: int,
+                   partials: torch.Tensor | None = None, ignore_idx: int = -100,
+                   stream=None) -> torch.Tensor:
+    """Step 1: (max, sum-exp, sum, target logit) per row of one vocabulary
+    shard; returns a float32 (N, 4) tensor."""
+    _check(shard, targets)
+    lib = _lib.load()
+    d0, d1, V, st = _dims(shard)
+    ts = _tstrides(targets, d0, d1)
+    if partials is None:
+        partials = torch.empty(d0 * d1, 4, dtype=torch.float32, device=shard.device)
+    rc = lib.ce_vp_partials(ctypes.c_void_p(shard.data_ptr()), _DTYPE[shard.dtype], d0, d1, V,
+                            _lib.i64_array(st), ctypes.c_void_p(targets.data_ptr()),
+                            _lib.i64_array(ts), int(vocab_offset), int(ignore_idx),
+                            ctypes.c_void_p(partials.data_ptr()), _stream(shard.device, stream))
+    _raise(rc, "ce_vp_partials")
+    return partials
+
+
+def ce_vp_combine(partials: torch.Tensor, shard_offsets, targets: torch.Tensor,
+                  label_smoothing: float = 0.0, ignore_idx: int = -100, reduce_loss: bool = False,
+                  loss_out: torch.Tensor | None = None, lse_out: torch.Tensor | None = None,
+                  n_non_ignore_out: torch.Tensor | None = None,
+                  workspace: torch.Tensor | None = None, stream=None):
+    """Step 2: combine (R, N, 4) partials in shard order; returns (loss, lse)."""
+    lib = _lib.load()
+    R = partials.shape[0]
+    if targets.dim() != 2:
+        raise ValueError("targets must be (dim0, dim1)")
+    d0, d1 = targets.shape
+    ts = targets.stride()
+    dev = targets.device
+    V = int(shard_offsets[-1])
+    if loss_out is None:
+        loss_out = torch.empty(1 if reduce_loss else d0 * d1, dtype=torch.float32, device=dev)
+    if lse_out is None:
+        lse_out = torch.empty(d0 * d1, dtype=torch.float32, device=dev)
+    ws, wsb = _workspace(workspace, d0, d1, V, torch.float32, None, dev)
+    rc = lib.ce_vp_combine(ctypes.c_void_p(partials.contiguous().data_ptr()), R,
+                           _lib.i64_array(shard_offsets), d0, d1,
+                           ctypes.c_void_p(targets.data_ptr()), _lib.i64_array(ts),
+                           float(label_smoothing), int(ignore_idx), int(bool(reduce_loss)),
+                           ctypes.c_void_p(loss_out.data_ptr()), ctypes.c_void_p(lse_out.data_ptr()),
+                           ctypes.c_void_p(n_non_ignore_out.data_ptr()
+                                           if n_non_ignore_out is not None else None),
+                           ctypes.c_void_p(ws.data_ptr()), wsb, _stream(dev, stream))
+    _raise(rc, "ce_vp_combine")
+    return loss_out, lse_out
+
+
+def ce_vp_bwd(shard: torch.Tensor, targets: torch.Tensor, vocab_offset: int, V_total: int,
+              lse: torch.Tensor, label_smoothing: float = 0.0, ignore_idx: int = -100,
+              reduce_loss: bool = False, dloss: torch.Tensor | None = None,
+              n_non_ignore: torch.Tensor | None = None, grad: torch.Tensor | None = None,
+              stream=None) -> torch.Tensor:
+    """Step 3: the gradient of one shard (in place when ``grad`` is ``shard``)."""
+    _check(shard, targets)
+    lib = _lib.load()
+    d0, d1, V, st = _dims(shard)
+    ts = _tstrides(targets, d0, d1)
+    if grad is None:
+        grad = torch.empty_like(shard)
+    gst = _dims(grad)[3]
+    rc = lib.ce_vp_bwd(ctypes.c_void_p(shard.data_ptr()), _DTYPE[shard.dtype], d0, d1, V,
+                       _lib.i64_array(st), ctypes.c_void_p(targets.data_ptr()), _lib.i64_array(ts),
+                       int(vocab_offset), int(V_total), ctypes.c_void_p(lse.data_ptr()),
+                       float(label_smoothing), int(ignore_idx), int(bool(reduce_loss)),
+                       ctypes.c_void_p(dloss.data_ptr() if dloss is not None else None),
+                       ctypes.c_void_p(n_non_ignore.data_ptr() if n_non_ignore is not None else None),
+                       ctypes.c_void_p(grad.data_ptr()), _lib.i64_array(gst),
+                       _stream(shard.device, stream))
+    _raise(rc, "ce_vp_bwd")
+    return grad
+
+
+def vocab_parallel_cross_entropy(shards, targets: torch.Tensor, label_smoothing: float = 0.0,
+                                 ignore_idx: int = -100, reduce_loss: bool = False,
+                                 dloss: torch.Tensor | None = None, inplace_grad: bool = True):
+    """All three steps over vocabulary shards held by one GPU (shard k holds
+    the next block of columns).  Returns (loss, gradients per shard); with
+    ``inplace_grad`` the gradients overwrite the shards."""
+    offsets = [0]
+    for sh in shards:
+        offsets.append(offsets[-1] + sh.shape[-1])
+    N = targets.numel()
+    dev = targets.device
+    part = torch.empty(len(shards), N, 4, dtype=torch.float32, device=dev)
+    for k, sh in enumerate(shards):
+        ce_vp_partials(sh, targets, offsets[k], partials=part[k], ignore_idx=ignore_idx)
+    n = torch.empty(1, dtype=torch.int64, device=dev)
+    loss, lse = ce_vp_combine(part, offsets, targets, label_smoothing=label_smoothing,
+                              ignore_idx=ignore_idx, reduce_loss=reduce_loss, n_non_ignore_out=n)
+    grads = [ce_vp_bwd(sh, targets, offsets[k], offsets[-1], lse, label_smoothing=label_smoothing,
+                       ignore_idx=ignore_idx, reduce_loss=reduce_loss, dloss=dloss,
+                       n_non_ignore=n, grad=sh if inplace_grad else None)
+             for k, sh in enumerate(shards)]
+    return loss, grads

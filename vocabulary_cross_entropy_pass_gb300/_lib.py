@@ -34,7 +34,8 @@ STATUS = {
 
 # every function include/ce.h declares
 EXPORTS = ("ce_workspace_bytes", "ce_fwd_bwd", "ce_fwd_only", "ce_get_error", "ce_status_string",
-           "ce_plan_path", "ce_fwd_bwd_noalloc", "ce_bwd")
+           "ce_plan_path", "ce_fwd_bwd_noalloc", "ce_bwd", "ce_vp_partials", "ce_vp_combine",
+           "ce_vp_bwd")
 
 
 class ce_options(ctypes.Structure):
@@ -91,6 +92,14 @@ def load(path: str = LIB_PATH):
         lib.ce_bwd.restype = i32
         lib.ce_bwd.argtypes = [vp, i32, i32, i64, i64, i64, I64_3, vp, I64_3, vp, f32, i64, i32, vp,
                                vp, vp, I64_3, vp]
+        lib.ce_vp_partials.restype = i32
+        lib.ce_vp_partials.argtypes = [vp, i32, i64, i64, i64, I64_3, vp, I64_3, i64, i64, vp, vp]
+        lib.ce_vp_combine.restype = i32
+        lib.ce_vp_combine.argtypes = [vp, i32, I64_3, i64, i64, vp, I64_3, f32, i64, i32, vp, vp,
+                                      vp, vp, ctypes.c_size_t, vp]
+        lib.ce_vp_bwd.restype = i32
+        lib.ce_vp_bwd.argtypes = [vp, i32, i64, i64, i64, I64_3, vp, I64_3, i64, i64, vp, f32, i64,
+                                  i32, vp, vp, vp, I64_3, vp]
         lib.ce_get_error.restype = i32
         lib.ce_get_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
         lib.ce_status_string.restype = ctypes.c_char_p

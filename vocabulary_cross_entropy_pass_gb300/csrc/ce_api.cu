@@ -269,6 +269,62 @@ void fill_problem(Problem& pb, const void* logits, int dtype, int64_t dim0, int6
     pb.reduce = reduce ? 1 : 0;
 }
 
+// The backward of ce_bwd and ce_vp_bwd: the gradient of V columns of the
+// logits that start at vocabulary column vocab_offset of a V_total vocabulary.
+ce_status bwd_common(const void* logits, int dtype, int64_t dim0, int64_t dim1, int64_t V,
+                     int64_t vocab_offset, int64_t V_total, const int64_t* strides,
+                     const int64_t* targets, const int64_t* target_strides, const float* lse,
+                     float label_smoothing, int64_t ignore_idx, int reduce_loss, const float* dloss,
+                     const int64_t* n_non_ignore, void* grad, const int64_t* grad_strides,
+                     cudaStream_t stream) {
+    if (dtype < CE_F32 || dtype > CE_F16) return CE_ERR_UNSUPPORTED_DTYPE;
+    if (!strides || !target_strides || !grad_strides) return CE_ERR_INVALID_ARG;
+    if (dim0 < 0 || dim1 < 0 || V < 1 || vocab_offset < 0 || V_total < vocab_offset + V ||
+        V_total > 0x7fffffffLL)
+        return CE_ERR_INVALID_ARG;
+    if (!(label_smoothing >= 0.f && label_smoothing <= 1.f)) return CE_ERR_INVALID_ARG;
+    const int64_t N = dim0 * dim1;
+    if (N > 0 && (!logits || !targets || !lse || !grad)) return CE_ERR_INVALID_ARG;
+    if (N > 0 && reduce_loss && !n_non_ignore) return CE_ERR_INVALID_ARG;
+    if (strides[2] != 1 || strides[0] < 0 || strides[1] < 0) return CE_ERR_BAD_STRIDE;
+    if (grad_strides[2] != 1 || grad_strides[0] < 0 || grad_strides[1] < 0) return CE_ERR_BAD_STRIDE;
+    if (target_strides[0] < 0 || target_strides[1] < 0) return CE_ERR_BAD_STRIDE;
+    if (!rows_disjoint(dim0, dim1, V, grad_strides[0], grad_strides[1])) return CE_ERR_BAD_STRIDE;
+    if (grad == logits && (grad_strides[0] != strides[0] || grad_strides[1] != strides[1]))
+        return CE_ERR_BAD_STRIDE;
+    if (N == 0) return CE_OK;
+    BwdProblem bp;
+    memset(&bp, 0, sizeof bp);
+    const int es = elem_size(dtype);
+    bp.logits = static_cast<const char*>(logits);
+    bp.grad = static_cast<char*>(grad);
+    bp.dtype = dtype;
+    bp.dim1 = dim1;
+    bp.N = N;
+    bp.V = V;
+    bp.s0 = strides[0];
+    bp.s1 = strides[1];
+    bp.gs0 = grad_strides[0];
+    bp.gs1 = grad_strides[1];
+    bp.targets = targets;
+    bp.ts0 = target_strides[0];
+    bp.ts1 = target_strides[1];
+    bp.ignore_idx = ignore_idx;
+    bp.lse = lse;
+    bp.a = label_smoothing;
+    bp.reduce = reduce_loss ? 1 : 0;
+    bp.dloss = dloss;
+    bp.n_dev = n_non_ignore;
+    bp.vocab_offset = vocab_offset;
+    bp.V_total = V_total;
+    bp.vec_ok = reinterpret_cast<uintptr_t>(logits) % 16 == 0 &&
+                reinterpret_cast<uintptr_t>(grad) % 16 == 0 && (V * es) % 16 == 0 &&
+                (strides[0] * es) % 16 == 0 && (strides[1] * es) % 16 == 0 &&
+                (grad_strides[0] * es) % 16 == 0 && (grad_strides[1] * es) % 16 == 0;
+    if (launch_bwd(bp, stream) != cudaSuccess) return CE_ERR_LAUNCH;
+    return CE_OK;
+}
+
 }  // namespace
 }  // namespace gbce
 
@@ -329,49 +385,104 @@ ce_status ce_bwd(const void* logits, ce_dtype dtype, ce_layout layout, int64_t d
                  int64_t ignore_idx, int reduce_loss, const float* dloss,
                  const int64_t* n_non_ignore, void* grad, const int64_t grad_strides[3],
                  void* stream) {
-    if (dtype < CE_F32 || dtype > CE_F16) return CE_ERR_UNSUPPORTED_DTYPE;
     if (layout != CE_LAYOUT_BSV && layout != CE_LAYOUT_SBV) return CE_ERR_INVALID_ARG;
-    if (!strides || !target_strides || !grad_strides) return CE_ERR_INVALID_ARG;
-    if (dim0 < 0 || dim1 < 0 || V < 1 || V > 0x7fffffffLL) return CE_ERR_INVALID_ARG;
+    return bwd_common(logits, dtype, dim0, dim1, V, 0, V, strides, targets, target_strides, lse,
+                      label_smoothing, ignore_idx, reduce_loss, dloss, n_non_ignore, grad,
+                      grad_strides, static_cast<cudaStream_t>(stream));
+}
+
+ce_status ce_vp_partials(const void* shard_logits, ce_dtype dtype, int64_t dim0, int64_t dim1,
+                         int64_t V_shard, const int64_t strides[3], const int64_t* targets,
+                         const int64_t target_strides[2], int64_t vocab_offset, int64_t ignore_idx,
+                         float* partials, void* stream) {
+    if (dtype < CE_F32 || dtype > CE_F16) return CE_ERR_UNSUPPORTED_DTYPE;
+    if (!strides || !target_strides) return CE_ERR_INVALID_ARG;
+    if (dim0 < 0 || dim1 < 0 || V_shard < 1 || vocab_offset < 0) return CE_ERR_INVALID_ARG;
+    const int64_t N = dim0 * dim1;
+    if (N > 0 && (!shard_logits || !targets || !partials)) return CE_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(partials) % 16) return CE_ERR_INVALID_ARG;
+    if (strides[2] != 1 || strides[0] < 0 || strides[1] < 0) return CE_ERR_BAD_STRIDE;
+    if (target_strides[0] < 0 || target_strides[1] < 0) return CE_ERR_BAD_STRIDE;
+    if (N == 0) return CE_OK;
+    const int es = elem_size(dtype);
+    VpPartProblem vp;
+    vp.logits = static_cast<const char*>(shard_logits);
+    vp.dtype = dtype;
+    vp.s0 = strides[0];
+    vp.s1 = strides[1];
+    vp.dim1 = dim1;
+    vp.N = N;
+    vp.V = V_shard;
+    vp.vocab_offset = vocab_offset;
+    vp.targets = targets;
+    vp.ts0 = target_strides[0];
+    vp.ts1 = target_strides[1];
+    vp.ignore_idx = ignore_idx;
+    vp.part = reinterpret_cast<float4*>(partials);
+    vp.vec_ok = reinterpret_cast<uintptr_t>(shard_logits) % 16 == 0 && (V_shard * es) % 16 == 0 &&
+                (strides[0] * es) % 16 == 0 && (strides[1] * es) % 16 == 0;
+    if (launch_vp_partials(vp, static_cast<cudaStream_t>(stream)) != cudaSuccess) return CE_ERR_LAUNCH;
+    return CE_OK;
+}
+
+ce_status ce_vp_combine(const float* partials, int num_shards, const int64_t* shard_offsets,
+                        int64_t dim0, int64_t dim1, const int64_t* targets,
+                        const int64_t target_strides[2], float label_smoothing, int64_t ignore_idx,
+                        int reduce_loss, float* loss_out, float* lse_out,
+                        int64_t* n_non_ignore_out, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+    if (num_shards < 1 || num_shards > kVpMaxShards || !shard_offsets || !target_strides)
+        return CE_ERR_INVALID_ARG;
+    if (shard_offsets[0] != 0) return CE_ERR_INVALID_ARG;
+    for (int k = 0; k < num_shards; ++k)
+        if (shard_offsets[k + 1] <= shard_offsets[k]) return CE_ERR_INVALID_ARG;
+    const int64_t V = shard_offsets[num_shards];
+    if (dim0 < 0 || dim1 < 0 || V > 0x7fffffffLL) return CE_ERR_INVALID_ARG;
     if (!(label_smoothing >= 0.f && label_smoothing <= 1.f)) return CE_ERR_INVALID_ARG;
     const int64_t N = dim0 * dim1;
-    if (N > 0 && (!logits || !targets || !lse || !grad)) return CE_ERR_INVALID_ARG;
-    if (N > 0 && reduce_loss && !n_non_ignore) return CE_ERR_INVALID_ARG;
-    if (strides[2] != 1 || strides[0] < 0 || strides[1] < 0) return CE_ERR_BAD_STRIDE;
-    if (grad_strides[2] != 1 || grad_strides[0] < 0 || grad_strides[1] < 0) return CE_ERR_BAD_STRIDE;
+    if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 16) return CE_ERR_INVALID_ARG;
+    if (N > 0 && (!partials || !targets || !loss_out || !lse_out)) return CE_ERR_INVALID_ARG;
+    if (N == 0 && reduce_loss && !loss_out) return CE_ERR_INVALID_ARG;
     if (target_strides[0] < 0 || target_strides[1] < 0) return CE_ERR_BAD_STRIDE;
-    if (!rows_disjoint(dim0, dim1, V, grad_strides[0], grad_strides[1])) return CE_ERR_BAD_STRIDE;
-    if (grad == logits && (grad_strides[0] != strides[0] || grad_strides[1] != strides[1]))
-        return CE_ERR_BAD_STRIDE;
-    if (N == 0) return CE_OK;
-    BwdProblem bp;
-    memset(&bp, 0, sizeof bp);
-    const int es = elem_size(dtype);
-    bp.logits = static_cast<const char*>(logits);
-    bp.grad = static_cast<char*>(grad);
-    bp.dtype = dtype;
-    bp.dim1 = dim1;
-    bp.N = N;
-    bp.V = V;
-    bp.s0 = strides[0];
-    bp.s1 = strides[1];
-    bp.gs0 = grad_strides[0];
-    bp.gs1 = grad_strides[1];
-    bp.targets = targets;
-    bp.ts0 = target_strides[0];
-    bp.ts1 = target_strides[1];
-    bp.ignore_idx = ignore_idx;
-    bp.lse = lse;
-    bp.a = label_smoothing;
-    bp.reduce = reduce_loss ? 1 : 0;
-    bp.dloss = dloss;
-    bp.n_dev = n_non_ignore;
-    bp.vec_ok = reinterpret_cast<uintptr_t>(logits) % 16 == 0 &&
-                reinterpret_cast<uintptr_t>(grad) % 16 == 0 && (V * es) % 16 == 0 &&
-                (strides[0] * es) % 16 == 0 && (strides[1] * es) % 16 == 0 &&
-                (grad_strides[0] * es) % 16 == 0 && (grad_strides[1] * es) % 16 == 0;
-    if (launch_bwd(bp, static_cast<cudaStream_t>(stream)) != cudaSuccess) return CE_ERR_LAUNCH;
+    if (workspace_bytes < workspace_need(N, V, nullptr)) return CE_ERR_WORKSPACE_TOO_SMALL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    static const int64_t unit_strides[3] = {0, 0, 1};
+    Problem pb;
+    fill_problem(pb, nullptr, CE_F32, dim0, dim1, V, unit_strides, targets, target_strides,
+                 label_smoothing, ignore_idx, reduce_loss);
+    char* w = static_cast<char*>(workspace);
+    pb.err = reinterpret_cast<uint32_t*>(w + kWsErrOffset);
+    pb.n_dev = reinterpret_cast<int64_t*>(w + kWsCountOffset);
+    pb.ticket = reinterpret_cast<uint32_t*>(w + kWsTicketOffset);
+    pb.loss_rows = reduce_loss ? reinterpret_cast<float*>(w + kWsHeaderBytes) : loss_out;
+    if (launch_count(pb, n_non_ignore_out, s) != cudaSuccess) return CE_ERR_LAUNCH;
+    VpCombineProblem vc;
+    vc.part = reinterpret_cast<const float4*>(partials);
+    vc.R = num_shards;
+    vc.off = shard_offsets;
+    vc.dim1 = dim1;
+    vc.N = N;
+    vc.targets = targets;
+    vc.ts0 = target_strides[0];
+    vc.ts1 = target_strides[1];
+    vc.ignore_idx = ignore_idx;
+    vc.a = label_smoothing;
+    vc.loss = pb.loss_rows;
+    vc.lse = lse_out;
+    if (launch_vp_combine(vc, s) != cudaSuccess) return CE_ERR_LAUNCH;
+    if (reduce_loss && launch_reduce_mean(pb, loss_out, s) != cudaSuccess) return CE_ERR_LAUNCH;
     return CE_OK;
+}
+
+ce_status ce_vp_bwd(const void* shard_logits, ce_dtype dtype, int64_t dim0, int64_t dim1,
+                    int64_t V_shard, const int64_t strides[3], const int64_t* targets,
+                    const int64_t target_strides[2], int64_t vocab_offset, int64_t V_total,
+                    const float* lse, float label_smoothing, int64_t ignore_idx, int reduce_loss,
+                    const float* dloss, const int64_t* n_non_ignore, void* grad,
+                    const int64_t grad_strides[3], void* stream) {
+    return bwd_common(shard_logits, dtype, dim0, dim1, V_shard, vocab_offset, V_total, strides,
+                      targets, target_strides, lse, label_smoothing, ignore_idx, reduce_loss, dloss,
+                      n_non_ignore, grad, grad_strides, static_cast<cudaStream_t>(stream));
 }
 
 ce_status ce_get_error(const void* workspace, void* stream, uint32_t* host_err) {

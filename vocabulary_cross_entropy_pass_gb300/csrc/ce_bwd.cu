@@ -33,6 +33,7 @@ struct BwdArgs {
     int reduce;
     const float* dloss;
     const int64_t* n_dev;
+    int64_t voff, Vtot;    // vocabulary offset of column 0, and the size targets index
 };
 
 template <typename T>
@@ -52,7 +53,7 @@ __global__ void __launch_bounds__(kBwdThreads) ce_bwd_vec_kernel(const __grid_co
         uint4* dst = reinterpret_cast<uint4*>(p.grad + (i * p.gs0 + j * p.gs1) * ES);
         const int64_t v0 = c * p.chunk / VEC;
         const int64_t v1 = min(p.V, (c + 1) * p.chunk) / VEC;
-        if (y == p.ignore_idx || y < 0 || y >= p.V) {
+        if (y == p.ignore_idx || y < 0 || y >= p.Vtot) {
             const uint4 z = make_uint4(0, 0, 0, 0);
             for (int64_t v = v0 + threadIdx.x; v < v1; v += kBwdThreads) stg128_stream(dst + v, z);
             continue;
@@ -65,8 +66,9 @@ __global__ void __launch_bounds__(kBwdThreads) ce_bwd_vec_kernel(const __grid_co
         const float nll = -__ldg(p.lse + r) * kLog2e;
         const float bb = g * p.a_over_v;
         const float2 NL = make_float2(nll, nll), G2 = make_float2(g, g), NB = make_float2(-bb, -bb);
-        const int64_t vy = y / VEC;
-        const int ey = (int)(y % VEC);
+        const int64_t yl = y - p.voff;  // the target's column in these logits
+        const int64_t vy = (yl >= 0 && yl < p.V) ? yl / VEC : -1;
+        const int ey = (int)(yl >= 0 ? yl % VEC : 0);
         const float hit = g * (1.f - p.a);
         for (int64_t vb = v0 + threadIdx.x; vb < v1; vb += kBwdThreads * kBwdVecs) {
             uint4 raw[kBwdVecs];
@@ -113,7 +115,7 @@ __global__ void __launch_bounds__(kBwdThreads) ce_bwd_scalar_kernel(const __grid
         const char* src = p.logits + (i * p.s0 + j * p.s1) * ES;
         char* dst = p.grad + (i * p.gs0 + j * p.gs1) * ES;
         const int64_t e0 = c * p.chunk, e1 = min(p.V, (c + 1) * p.chunk);
-        if (y == p.ignore_idx || y < 0 || y >= p.V) {
+        if (y == p.ignore_idx || y < 0 || y >= p.Vtot) {
             for (int64_t e = e0 + threadIdx.x; e < e1; e += kBwdThreads) VT::store1(dst + e * ES, 0.f);
             continue;
         }
@@ -127,7 +129,7 @@ __global__ void __launch_bounds__(kBwdThreads) ce_bwd_scalar_kernel(const __grid
         for (int64_t e = e0 + threadIdx.x; e < e1; e += kBwdThreads) {
             const float x = VT::load1(src + e * ES);
             float o = fmaf(ex2_approx(fmaf(x, kLog2e, nll)), g, -bb);
-            if (e == y) o -= g * (1.f - p.a);
+            if (e + p.voff == y) o -= g * (1.f - p.a);
             VT::store1(dst + e * ES, o);
         }
     }
@@ -153,7 +155,9 @@ cudaError_t launch_bwd_typed(const BwdProblem& bp, cudaStream_t s) {
     a.ignore_idx = bp.ignore_idx;
     a.lse = bp.lse;
     a.a = bp.a;
-    a.a_over_v = bp.a / (float)bp.V;
+    a.voff = bp.vocab_offset;
+    a.Vtot = bp.V_total;
+    a.a_over_v = bp.a / (float)bp.V_total;
     a.reduce = bp.reduce;
     a.dloss = bp.dloss;
     a.n_dev = bp.n_dev;

@@ -90,6 +90,31 @@ struct BwdProblem {
     const float* dloss;
     const int64_t* n_dev;
     bool vec_ok;               // every row of both tensors 16-byte aligned
+    int64_t vocab_offset;      // global index of column 0 (a vocabulary shard), else 0
+    int64_t V_total;           // vocabulary size the targets index, else V
+};
+
+// Vocabulary-parallel partials of one shard.
+constexpr int kVpMaxShards = 64;
+struct VpPartProblem {
+    const char* logits;
+    int dtype;
+    int64_t s0, s1, dim1, N, V, vocab_offset;
+    const int64_t* targets;
+    int64_t ts0, ts1, ignore_idx;
+    float4* part;
+    bool vec_ok;
+};
+struct VpCombineProblem {
+    const float4* part;
+    int R;
+    const int64_t* off;        // host, R + 1 entries
+    int64_t dim1, N;
+    const int64_t* targets;
+    int64_t ts0, ts1, ignore_idx;
+    float a;
+    float* loss;
+    float* lse;
 };
 
 int elem_size(int dtype);
@@ -105,6 +130,8 @@ cudaError_t launch_fused(const Problem& p, const FusedPlan& plan, cudaStream_t s
 cudaError_t launch_stream(const Problem& p, const StreamPlan& plan, cudaStream_t s);
 cudaError_t launch_rows(const Problem& p, const RowsPlan& plan, cudaStream_t s);
 cudaError_t launch_bwd(const BwdProblem& bp, cudaStream_t s);
+cudaError_t launch_vp_partials(const VpPartProblem& vp, cudaStream_t s);
+cudaError_t launch_vp_combine(const VpCombineProblem& vc, cudaStream_t s);
 cudaError_t launch_split(const Problem& p, const SplitPlan& plan, float4* partials,
                          cudaStream_t s);
 

@@ -1,0 +1,205 @@
+// ce_vp.cu -- vocabulary-parallel cross-entropy, one shard at a time.
+//
+// mindspore/hyper-parallel #269 (section 3.1) describes the vocab-sharded
+// cross-entropy that tensor-parallel training runs when each rank holds a
+// ceil(V/tp) slice of the logits: per-row (max, sum-exp) statistics of the
+// slice, a MAX all-reduce and a SUM all-reduce of the rescaled sums plus a
+// gather of the target logit (the m_d_Xy gather of TENPU "Parallel Cross
+// Entropy (Triton)" #29, section 6), then a backward that needs no collective.
+// On one GPU the ranks become vocabulary shards (separate tensors) and the
+// collectives become a fixed-order combine over the gathered partials:
+//
+//   ce_vp_partials_kernel: per row of one shard, {m, d, S, x_y} (x_y when the
+//     global target falls in the shard, else 0); ignored rows get the empty
+//     partial {-inf, 0, 0, 0};
+//   ce_vp_combine_kernel:  per row, the partials of all shards in shard order
+//     -> lse = m + log d, loss = lse - (1-a) x_y - (a/V) S;
+//   the gradient of each shard: ce_bwd's kernels with the shard's vocabulary
+//     offset (ce_bwd.cu).
+#include "ce_device.cuh"
+#include "ce_internal.h"
+
+namespace gbce {
+namespace {
+
+constexpr int kVpThreads = 256;
+constexpr int kVpWarps = kVpThreads / 32;
+
+struct VpPartArgs {
+    const char* logits;
+    int64_t s0, s1, dim1, N, V;        // V: columns of this shard
+    int64_t vocab_offset;              // global index of the shard's column 0
+    const int64_t* targets;
+    int64_t ts0, ts1, ignore_idx;
+    float4* part;                      // [N]
+    bool vec_ok;
+};
+
+// One CTA per row: a running (max, sum-exp, sum) per thread over 16-byte
+// vectors (one rescale per vector whose max is new), then the CTA combine.
+template <typename T>
+__global__ void __launch_bounds__(kVpThreads) ce_vp_partials_kernel(const __grid_constant__ VpPartArgs p) {
+    using VT = Vec<T>;
+    constexpr int VEC = VT::kElems;
+    constexpr int ES = sizeof(T);
+    constexpr int PP = VEC / 2;
+    __shared__ float4 s_red[kVpWarps];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const float2 L2 = make_float2(kLog2e, kLog2e);
+    for (int64_t r = blockIdx.x; r < p.N; r += gridDim.x) {
+        const int64_t i = r / p.dim1, j = r - i * p.dim1;
+        const int64_t y = __ldg(p.targets + i * p.ts0 + j * p.ts1);
+        if (y == p.ignore_idx) {
+            if (threadIdx.x == 0) p.part[r] = make_float4(-INFINITY, 0.f, 0.f, 0.f);
+            continue;
+        }
+        const char* row = p.logits + (i * p.s0 + j * p.s1) * ES;
+        float m = -INFINITY;
+        float2 d2 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
+        if (p.vec_ok) {
+            const uint4* rv = reinterpret_cast<const uint4*>(row);
+            const int64_t nv = p.V / VEC;
+            for (int64_t v = threadIdx.x; v < nv; v += kVpThreads) {
+                const uint4 raw = __ldcs(rv + v);
+                const float vm = VT::vmax(raw);
+                if (vm > m) {
+                    if (m != -INFINITY) {
+                        const float c = ex2_approx((m - vm) * kLog2e);
+                        d2.x *= c;
+                        d2.y *= c;
+                    }
+                    m = vm;
+                }
+                const float nml = -m * kLog2e;
+                const float2 NM = make_float2(nml, nml);
+                float2 x[PP];
+                VT::unpack2(raw, x);
+#pragma unroll
+                for (int q = 0; q < PP; ++q) {
+                    const float2 e = __ffma2_rn(x[q], L2, NM);
+                    d2 = __fadd2_rn(d2, make_float2(ex2_approx(e.x), ex2_approx(e.y)));
+                    s2 = __fadd2_rn(s2, x[q]);
+                }
+            }
+        } else {
+            for (int64_t e = threadIdx.x; e < p.V; e += kVpThreads) {
+                const float x = VT::load1(row + e * ES);
+                if (x > m) {
+                    if (m != -INFINITY) d2.x *= ex2_approx((m - x) * kLog2e);
+                    m = x;
+                }
+                d2.x += ex2_approx(fmaf(x, kLog2e, -m * kLog2e));
+                s2.x += x;
+            }
+        }
+        Part q = warp_allreduce_part(Part{m, d2.x + d2.y, s2.x + s2.y});
+        if (lane == 0) s_red[warp] = make_float4(q.m, q.d, q.S, 0.f);
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            Part G = part_identity();
+            for (int w = 0; w < kVpWarps; ++w) G = part_combine(G, Part{s_red[w].x, s_red[w].y, s_red[w].z});
+            const int64_t yl = y - p.vocab_offset;
+            const float xy = (yl >= 0 && yl < p.V) ? VT::load1(row + yl * ES) : 0.f;
+            p.part[r] = make_float4(G.m, G.d, G.S, xy);
+        }
+        __syncthreads();
+    }
+}
+
+struct VpCombineArgs {
+    const float4* part;                // [R][N]
+    int R;
+    int64_t off[kVpMaxShards + 1];     // shard column offsets, off[R] = V total
+    int64_t dim1, N;
+    const int64_t* targets;
+    int64_t ts0, ts1, ignore_idx;
+    float a, a_over_v;
+    float* loss;                       // [N]
+    float* lse;                        // [N]
+};
+
+// One thread per row: combine the shards' partials in shard order.
+__global__ void __launch_bounds__(256) ce_vp_combine_kernel(const __grid_constant__ VpCombineArgs p) {
+    const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= p.N) return;
+    const int64_t i = r / p.dim1, j = r - i * p.dim1;
+    const int64_t y = __ldg(p.targets + i * p.ts0 + j * p.ts1);
+    const float nan = __int_as_float(0x7fc00000);
+    if (y == p.ignore_idx || y < 0 || y >= p.off[p.R]) {
+        p.loss[r] = (y == p.ignore_idx) ? 0.f : nan;
+        p.lse[r] = nan;
+        return;
+    }
+    Part G = part_identity();
+    float xy = 0.f;
+    for (int k = 0; k < p.R; ++k) {
+        const float4 w = p.part[(int64_t)k * p.N + r];
+        G = part_combine(G, Part{w.x, w.y, w.z});
+        if (y >= p.off[k] && y < p.off[k + 1]) xy = w.w;  // the target's owner
+    }
+    const float lse = G.m + logf(G.d);
+    p.lse[r] = lse;
+    p.loss[r] = lse - (1.f - p.a) * xy - p.a_over_v * G.S;
+}
+
+template <typename T>
+cudaError_t launch_vp_partials_typed(const VpPartArgs& a, cudaStream_t s) {
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int64_t grid = a.N;
+    if (grid > (int64_t)sms * 16) grid = (int64_t)sms * 16;
+    if (grid < 1) return cudaSuccess;
+    ce_vp_partials_kernel<T><<<(unsigned)grid, kVpThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_vp_partials(const VpPartProblem& vp, cudaStream_t s) {
+    VpPartArgs a;
+    a.logits = vp.logits;
+    a.s0 = vp.s0;
+    a.s1 = vp.s1;
+    a.dim1 = vp.dim1;
+    a.N = vp.N;
+    a.V = vp.V;
+    a.vocab_offset = vp.vocab_offset;
+    a.targets = vp.targets;
+    a.ts0 = vp.ts0;
+    a.ts1 = vp.ts1;
+    a.ignore_idx = vp.ignore_idx;
+    a.part = vp.part;
+    a.vec_ok = vp.vec_ok;
+    switch (vp.dtype) {
+        case CE_F32:
+            return launch_vp_partials_typed<float>(a, s);
+        case CE_BF16:
+            return launch_vp_partials_typed<__nv_bfloat16>(a, s);
+        default:
+            return launch_vp_partials_typed<__half>(a, s);
+    }
+}
+
+cudaError_t launch_vp_combine(const VpCombineProblem& vc, cudaStream_t s) {
+    VpCombineArgs a;
+    a.part = vc.part;
+    a.R = vc.R;
+    for (int k = 0; k <= vc.R; ++k) a.off[k] = vc.off[k];
+    a.dim1 = vc.dim1;
+    a.N = vc.N;
+    a.targets = vc.targets;
+    a.ts0 = vc.ts0;
+    a.ts1 = vc.ts1;
+    a.ignore_idx = vc.ignore_idx;
+    a.a = vc.a;
+    a.a_over_v = vc.a / (float)vc.off[vc.R];
+    a.loss = vc.loss;
+    a.lse = vc.lse;
+    if (vc.N < 1) return cudaSuccess;
+    const int64_t blocks = (vc.N + 255) / 256;
+    ce_vp_combine_kernel<<<(unsigned)blocks, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace gbce
