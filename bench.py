@@ -276,9 +276,43 @@ def run_ours(args, w, rank: int, world: int, dist) -> None:
     path, chunks = pkg.ce_plan_path(x, opts)
     torch.cuda.synchronize(dev)
 
-    def step(o=opts):
-        pkg.ce_fwd_bwd(x, t, label_smoothing=w.label_smoothing, ignore_idx=w.ignore_idx,
-                       reduce_loss=w.reduce_loss, loss_out=loss, workspace=ws, opts=o)
+    mode = args.mode
+    if mode == "fused":
+        def step(o=opts):
+            pkg.ce_fwd_bwd(x, t, label_smoothing=w.label_smoothing, ignore_idx=w.ignore_idx,
+                           reduce_loss=w.reduce_loss, loss_out=loss, workspace=ws, opts=o)
+    elif mode == "split":
+        # forward only (saves lse and the kept-row count), then the backward
+        lse = torch.empty(w.N, dtype=torch.float32, device=dev)
+        n_kept = torch.empty(1, dtype=torch.int64, device=dev)
+
+        def step(o=opts):
+            pkg.ce_fwd_only(x, t, label_smoothing=w.label_smoothing, ignore_idx=w.ignore_idx,
+                            reduce_loss=w.reduce_loss, loss_out=loss, lse_out=lse,
+                            n_non_ignore_out=n_kept, workspace=ws, opts=o)
+            pkg.ce_bwd(x, t, lse, label_smoothing=w.label_smoothing, ignore_idx=w.ignore_idx,
+                       reduce_loss=w.reduce_loss, n_non_ignore=n_kept, grad=x)
+    else:
+        # vocabulary shards held as separate tensors, the three steps per pass
+        R = args.vocab_shards
+        c = -(-w.V // R)
+        shards = [x[..., k * c:min(w.V, (k + 1) * c)].contiguous() for k in range(R)]
+        del x
+        offsets = [min(w.V, k * c) for k in range(R)] + [w.V]
+        part = torch.empty(R, w.N, 4, dtype=torch.float32, device=dev)
+        lse = torch.empty(w.N, dtype=torch.float32, device=dev)
+        n_kept = torch.empty(1, dtype=torch.int64, device=dev)
+
+        def step(o=opts):
+            for k, sh in enumerate(shards):
+                pkg.ce_vp_partials(sh, t, offsets[k], partials=part[k], ignore_idx=w.ignore_idx)
+            pkg.ce_vp_combine(part, offsets, t, label_smoothing=w.label_smoothing,
+                              ignore_idx=w.ignore_idx, reduce_loss=w.reduce_loss, loss_out=loss,
+                              lse_out=lse, n_non_ignore_out=n_kept, workspace=ws)
+            for k, sh in enumerate(shards):
+                pkg.ce_vp_bwd(sh, t, offsets[k], w.V, lse, label_smoothing=w.label_smoothing,
+                              ignore_idx=w.ignore_idx, reduce_loss=w.reduce_loss,
+                              n_non_ignore=n_kept, grad=sh)
 
     for _ in range(args.warmup):
         step()
@@ -317,7 +351,8 @@ def run_ours(args, w, rank: int, world: int, dist) -> None:
     sampler.stop()
     clocks = sampler.summary(t0, t1)
     total_ms = start.elapsed_time(end)
-    kernel_ms = sum(b.elapsed_time(e) for (b, e) in evs) / args.steps
+    kernel_ms = (sum(b.elapsed_time(e) for (b, e) in evs) / args.steps
+                 if args.mode in ("fused", "split") else None)
 
     def allmax(v):
         if dist is None:
@@ -327,6 +362,26 @@ def run_ours(args, w, rank: int, world: int, dist) -> None:
         return float(tt.item())
 
     ms, tok_s = aggregate(total_ms, w.N * args.steps, world, allmax)
+
+    if mode != "fused":
+        # one line for a secondary mode: whole-step bytes over whole-step time
+        if rank == 0:
+            nb = (2 if mode == "fused" else 3) * w.logits_bytes + 8 * w.N
+            line = {"metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": world,
+                    "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+                    "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                    "dtype": "f32", "data": "synthetic",
+                    "config": config_of(w, args) | {"mode": mode,
+                                                     "vocab_shards": args.vocab_shards
+                                                     if mode == "vp" else None},
+                    "roofline": {"bound": "hbm", "kernel": "whole step (two reads + one write)",
+                                 "achieved": nb / (ms / args.steps / 1e3) / 1e9,
+                                 "peak": measured_peaks()["hbm_gbs"], "unit": "GB/s",
+                                 "frac": nb / (ms / args.steps / 1e3) / 1e9
+                                 / measured_peaks()["hbm_gbs"], "traffic": None},
+                    "clocks": clocks}
+            print(json.dumps(line), flush=True)
+        return
 
     # end to end through the public call: pinned host -> device inputs, the
     # pass, the loss back to the host, every step
@@ -397,6 +452,10 @@ def main(argv=None) -> int:
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--ref-rows", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    # secondary passes: "split" = ce_fwd_only + ce_bwd (autograd order), "vp" = the
+    # vocabulary-parallel steps over --vocab-shards shards on one GPU
+    ap.add_argument("--mode", choices=["fused", "split", "vp"], default="fused")
+    ap.add_argument("--vocab-shards", type=int, default=8)
     # planner overrides, for tuning sweeps (defaults: the planner's choice)
     ap.add_argument("--force-path", type=int, default=0)
     ap.add_argument("--chunks", type=int, default=0)

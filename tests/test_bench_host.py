@@ -47,7 +47,7 @@ def _rank_main(rank, world, port, out):
 
 def test_aggregate_over_two_gloo_ranks():
     port = _free_port()
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
     mp.spawn(_rank_main, args=(2, port, out), nprocs=2, join=True)
     for r in (0, 1):

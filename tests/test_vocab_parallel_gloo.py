@@ -42,6 +42,6 @@ def test_two_rank_vocab_parallel_combine():
     s.bind(("127.0.0.1", 0))
     port = s.getsockname()[1]
     s.close()
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()
     mp.spawn(_rank, args=(2, port, 1001, out), nprocs=2, join=True)
     assert out[0] <= 1e-13 and out[1] <= 1e-13
