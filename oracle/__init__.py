@@ -45,7 +45,7 @@ def _bind(lib):
     c_i64, c_dbl, c_int, c_vp = ctypes.c_int64, ctypes.c_double, ctypes.c_int, ctypes.c_void_p
     lib.oracle_ce.restype = c_int
     lib.oracle_ce.argtypes = [c_vp, c_int, c_i64, c_i64, c_i64, c_i64, c_i64, c_vp, c_i64, c_i64,
-                              c_dbl, c_i64, c_int, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]
+                              c_dbl, c_i64, c_int, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]
     lib.oracle_round.restype = c_dbl
     lib.oracle_round.argtypes = [c_dbl, c_int]
     lib.oracle_round_array.restype = None
@@ -81,7 +81,7 @@ def _ptr(a: np.ndarray | None):
 def ce(logits: np.ndarray, dtype: int, dim0: int, dim1: int, V: int, strides=None,
        targets: np.ndarray | None = None, target_strides=None, label_smoothing: float = 0.0,
        ignore_idx: int = -100, reduce_loss: bool = False, dloss: np.ndarray | None = None,
-       want_grad: bool = True, lib=None) -> dict:
+       want_grad: bool = True, class_weights: np.ndarray | None = None, lib=None) -> dict:
     """Run the oracle on raw logits storage.
 
     ``logits`` is the flat storage (float32 for F32; uint16 bit patterns for BF16
@@ -100,6 +100,9 @@ def ce(logits: np.ndarray, dtype: int, dim0: int, dim1: int, V: int, strides=Non
     targets = np.ascontiguousarray(targets, dtype=np.int64)
     if dloss is not None:
         dloss = np.ascontiguousarray(dloss, dtype=np.float64)
+    if class_weights is not None:
+        class_weights = np.ascontiguousarray(class_weights, dtype=np.float64)
+        assert class_weights.shape == (V,)
     loss = np.zeros(1 if reduce_loss else N, dtype=np.float64)
     lse = np.zeros(N, dtype=np.float64)
     grad = np.zeros((N, V), dtype=np.float64) if want_grad else None
@@ -107,8 +110,8 @@ def ce(logits: np.ndarray, dtype: int, dim0: int, dim1: int, V: int, strides=Non
     err = np.zeros(1, dtype=np.uint32)
     rc = lib.oracle_ce(_ptr(logits), dtype, dim0, dim1, V, strides[0], strides[1], _ptr(targets),
                        target_strides[0], target_strides[1], float(label_smoothing), int(ignore_idx),
-                       int(bool(reduce_loss)), _ptr(dloss), _ptr(loss), _ptr(lse), _ptr(grad),
-                       _ptr(n), _ptr(err))
+                       int(bool(reduce_loss)), _ptr(dloss), _ptr(class_weights), _ptr(loss),
+                       _ptr(lse), _ptr(grad), _ptr(n), _ptr(err))
     if rc != 0:
         raise MemoryError("oracle_ce ran out of host memory")
     return {"loss": loss, "lse": lse, "grad": grad, "n": int(n[0]), "err": int(err[0])}

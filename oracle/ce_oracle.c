@@ -40,6 +40,9 @@
  *   - reduce_loss: dloss is the upstream gradient of the mean (one scalar),
  *     so each kept row is scaled by dloss/n; n == 0 gives a NaN mean and an
  *     all-zero gradient, as torch F.cross_entropy does.
+ *   - class weights (optional) follow torch F.cross_entropy(weight=...): each
+ *     class's term of the smoothed target is weighted, and the mean divides by
+ *     the summed weight of the kept rows' targets.
  *   - without reduce_loss, dloss holds one scale per row (NULL means 1).
  *   - rows are visited in the flattened (dim0, dim1) order r = i*dim1 + j for
  *     both layouts (B,SQ,V) and (SQ,B,V); targets use the same (dim0, dim1).
@@ -177,6 +180,37 @@ static void row_reference(const double* x, int64_t V, int64_t y, double a, doubl
     }
 }
 
+/* The same row with per-class weights w (the weighted cross-entropy of torch
+ * F.cross_entropy(weight=w), which hyper-parallel #269's comparison table lists
+ * as supported by PyTorch and Hyper): the smoothed target q_j is weighted by
+ * w_j,
+ *   loss = -sum_j q_j w_j log softmax_j
+ *        = (1-a) w_y (lse - x_y) + (a/V) sum_j w_j (lse - x_j),
+ *   grad_j = g (softmax_j ((1-a) w_y + (a/V) sum_k w_k) - q_j w_j). */
+static void row_reference_weighted(const double* x, const double* w, int64_t V, int64_t y,
+                                   double a, double g, double* loss, double* lse_out,
+                                   double* grad) {
+    double m = -INFINITY;
+    for (int64_t j = 0; j < V; ++j)
+        if (x[j] > m) m = x[j];
+    double d = 0.0, Sw = 0.0, W = 0.0;
+    for (int64_t j = 0; j < V; ++j) {
+        d += exp(x[j] - m);
+        Sw += w[j] * x[j];
+        W += w[j];
+    }
+    double lse = m + log(d);
+    *loss = (1.0 - a) * w[y] * (lse - x[y]) + (a / (double)V) * (W * lse - Sw);
+    if (lse_out) *lse_out = lse;
+    if (grad) {
+        double c = (1.0 - a) * w[y] + (a / (double)V) * W;
+        for (int64_t j = 0; j < V; ++j) {
+            double q = (j == y ? 1.0 - a : 0.0) + a / (double)V;
+            grad[j] = g * (exp(x[j] - lse) * c - q * w[j]);
+        }
+    }
+}
+
 /* ---------------------------------------------------------------------------
  * Vocabulary-split statistics and their combine, the exchange the pages run
  * across vocabulary-parallel ranks [HYPER-269 section 3.1; TENPU-29 section 6,
@@ -230,6 +264,7 @@ void oracle_combine(const double* parts, int K, double* out) {
  *   reduce      0: loss_out[r] per row;  1: loss_out[0] = mean over kept rows
  *   dloss       reduce: one scalar (upstream gradient of the mean);
  *               otherwise one scale per row; NULL means 1
+ *   class_weights  double[V] per-class weights, or NULL (all ones)
  *   loss_out    double[N] or double[1]
  *   lse_out     double[N] or NULL (NaN for rows that are ignored or in error)
  *   grad_out    double[N*V] in flattened row order (r*V + v), or NULL; the
@@ -241,13 +276,15 @@ void oracle_combine(const double* parts, int K, double* out) {
 int oracle_ce(const void* logits, int dtype, int64_t dim0, int64_t dim1, int64_t V,
               int64_t s0, int64_t s1, const int64_t* targets, int64_t ts0, int64_t ts1,
               double a, int64_t ignore_idx, int reduce, const double* dloss,
-              double* loss_out, double* lse_out, double* grad_out, int64_t* n_out,
-              uint32_t* err_out) {
+              const double* class_weights, double* loss_out, double* lse_out, double* grad_out,
+              int64_t* n_out, uint32_t* err_out) {
     const int64_t N = dim0 * dim1;
 
     /* Ignore mask, count and range check [TENPU-29 section 1, ignore_idx;
-     * section 7, n_non_ignore]. */
+     * section 7, n_non_ignore].  With class weights the mean divides by the
+     * summed weight of the kept rows' targets instead of their count. */
     int64_t n = 0;
+    double wsum = 0.0;
     uint32_t err = 0;
     for (int64_t r = 0; r < N; ++r) {
         int64_t i = r / dim1, j = r % dim1;
@@ -255,7 +292,9 @@ int oracle_ce(const void* logits, int dtype, int64_t dim0, int64_t dim1, int64_t
         if (y == ignore_idx) continue;
         ++n;
         if (y < 0 || y >= V) err |= ORACLE_ERR_TARGET_RANGE;
+        else if (class_weights) wsum += class_weights[y];
     }
+    const double denom = class_weights ? wsum : (double)n;
 
     /* Per-row losses, kept in row order so the mean is summed sequentially. */
     double* row_loss = (double*)malloc((size_t)(N > 0 ? N : 1) * sizeof(double));
@@ -274,13 +313,16 @@ int oracle_ce(const void* logits, int dtype, int64_t dim0, int64_t dim1, int64_t
             /* per-row scale of the gradient */
             double g;
             if (reduce)
-                g = (dloss ? dloss[0] : 1.0) / (double)n;
+                g = (dloss ? dloss[0] : 1.0) / denom;
             else
                 g = dloss ? dloss[r] : 1.0;
             double* row = (double*)malloc((size_t)V * sizeof(double));
             for (int64_t v = 0; v < V; ++v)
                 row[v] = oracle_decode(logits, dtype, i * s0 + j * s1 + v);
-            row_reference(row, V, y, a, g, &loss, &lse, grow);
+            if (class_weights)
+                row_reference_weighted(row, class_weights, V, y, a, g, &loss, &lse, grow);
+            else
+                row_reference(row, V, y, a, g, &loss, &lse, grow);
             free(row);
         }
         if (lse_out) lse_out[r] = lse;
@@ -292,7 +334,7 @@ int oracle_ce(const void* logits, int dtype, int64_t dim0, int64_t dim1, int64_t
         sum_loss += row_loss[r];
     }
     free(row_loss);
-    if (reduce) loss_out[0] = sum_loss / (double)n; /* 0/0 = NaN when all rows are ignored */
+    if (reduce) loss_out[0] = sum_loss / denom; /* 0/0 = NaN when all rows are ignored */
     if (n_out) *n_out = n;
     if (err_out) *err_out = err;
     return 0;

@@ -324,4 +324,92 @@ def pin_rounding_is_nearest_even(lib):
     assert np.array_equal(got, probes.astype(np.float32).astype(np.float64))
 
 
+# ---------------------------------------------------------------- class weights
+def _ce_w(lib, x32, t, w, a=0.0, reduce=False, dloss=None):
+    N, V = x32.shape
+    return oracle.ce(np.ascontiguousarray(x32, dtype=np.float32), F32, 1, N, V,
+                     targets=np.asarray(t, dtype=np.int64).reshape(1, N), label_smoothing=a,
+                     reduce_loss=reduce, dloss=dloss, class_weights=w, lib=lib)
+
+
+def _brute_loss_weighted(x, y, a, w):
+    """-sum_j q_j w_j log softmax_j, explicit softmax -> log -> weighted sum."""
+    V = len(x)
+    m = max(x)
+    e = [math.exp(v - m) for v in x]
+    s = math.fsum(e)
+    logp = [math.log(v / s) for v in e]
+    q = [(1.0 - a if j == y else 0.0) + a / V for j in range(V)]
+    return -math.fsum(qj * wj * lj for qj, wj, lj in zip(q, w, logp))
+
+
+def pin_class_weights_torch_float64(lib):
+    rng = np.random.default_rng(21)
+    N, V = 30, 97
+    x = (rng.standard_normal((N, V)) * 2).astype(np.float32)
+    t = rng.integers(0, V, N)
+    t[[2, 11]] = -100
+    w = rng.uniform(0.2, 3.0, V)
+    for a in (0.0, 0.15):
+        xt = torch.tensor(x, dtype=torch.float64, requires_grad=True)
+        wt = torch.tensor(w)
+        tt = torch.tensor(t)
+        dl = rng.uniform(0.5, 2.0, N)
+        lt = torch.nn.functional.cross_entropy(xt, tt, weight=wt, reduction="none",
+                                               label_smoothing=a, ignore_index=-100)
+        lt.backward(torch.tensor(dl))
+        r = _ce_w(lib, x, t, w, a=a, dloss=dl)
+        assert np.allclose(r["loss"], lt.detach().numpy(), rtol=1e-12, atol=1e-12)
+        assert np.allclose(r["grad"], xt.grad.numpy(), rtol=1e-10, atol=1e-14)
+        xt.grad = None
+        lm = torch.nn.functional.cross_entropy(xt, tt, weight=wt, reduction="mean",
+                                               label_smoothing=a, ignore_index=-100)
+        lm.backward(torch.tensor(0.8, dtype=torch.float64))
+        r = _ce_w(lib, x, t, w, a=a, reduce=True, dloss=np.array([0.8]))
+        assert abs(r["loss"][0] - lm.item()) <= 1e-12 * abs(lm.item())
+        assert np.allclose(r["grad"], xt.grad.numpy(), rtol=1e-10, atol=1e-15)
+
+
+def pin_class_weights_brute_force_and_fd(lib):
+    rng = np.random.default_rng(22)
+    h = 1e-5
+    for V, a in ((5, 0.0), (9, 0.3)):
+        x = (rng.standard_normal((V, V)) * 2).astype(np.float32)
+        w = rng.uniform(0.1, 2.0, V)
+        t = np.arange(V)
+        r = _ce_w(lib, x, t, w, a=a)
+        for k in range(V):
+            row = [float(v) for v in x[k]]
+            ref = _brute_loss_weighted(row, k, a, w)
+            assert abs(r["loss"][k] - ref) <= 1e-12 * max(1.0, abs(ref))
+            for j in range(V):
+                up = row.copy(); up[j] += h
+                dn = row.copy(); dn[j] -= h
+                fd = (_brute_loss_weighted(up, k, a, w) - _brute_loss_weighted(dn, k, a, w)) / (2 * h)
+                assert abs(r["grad"][k, j] - fd) < 1e-8
+
+
+def pin_class_weights_closed_forms(lib):
+    rng = np.random.default_rng(23)
+    V = 64
+    w = rng.uniform(0.5, 1.5, V)
+    x = np.full((3, V), 1.5, dtype=np.float32)
+    t = np.array([0, 17, 63])
+    for a in (0.0, 0.2):
+        r = _ce_w(lib, x, t, w, a=a)
+        # uniform logits: every lse - x_j = log V
+        expect = math.log(V) * ((1 - a) * w[t] + a / V * w.sum())
+        assert np.allclose(r["loss"], expect, rtol=1e-13)
+        # mean divides by the targets' summed weight
+        rm = _ce_w(lib, x, t, w, a=a, reduce=True)
+        assert abs(rm["loss"][0] - expect.sum() / w[t].sum()) <= 1e-13 * expect.sum()
+    # all-ones weights: the unweighted pass
+    xr = (rng.standard_normal((4, V)) * 2).astype(np.float32)
+    tr = rng.integers(0, V, 4)
+    a1 = _ce_w(lib, xr, tr, np.ones(V), a=0.1, reduce=True)
+    a0 = _ce(lib, xr, tr, a=0.1, reduce=True)
+    assert abs(a1["loss"][0] - a0["loss"][0]) <= 1e-14 * abs(a0["loss"][0])
+    assert np.allclose(a1["grad"], a0["grad"], rtol=1e-13, atol=1e-17)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

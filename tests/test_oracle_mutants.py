@@ -20,18 +20,23 @@ MUTANTS = {
                             "        d += exp(x[j]);\n        S += x[j];\n    }\n    double lse"),
     "smoothing_over_v_minus_1": ("+ a / (double)V; /* smoothed target */",
                                  "+ a / (double)(V - 1); /* smoothed target */"),
-    "target_off_by_one": ("(j == y ? 1.0 - a : 0.0)", "(j == y + 1 ? 1.0 - a : 0.0)"),
+    "target_off_by_one": ("double q = (j == y ? 1.0 - a : 0.0) + a / (double)V; /* smoothed",
+                          "double q = (j == y + 1 ? 1.0 - a : 0.0) + a / (double)V; /* smoothed"),
     "rows_in_wrong_order": ("        int64_t i = r / dim1, j = r % dim1;\n        int64_t y = targets[i * ts0 + j * ts1];\n        double* grow",
                             "        int64_t i = r % dim0, j = r / dim0;\n        int64_t y = targets[i * ts0 + j * ts1];\n        double* grow"),
     "count_includes_ignored": ("        if (y == ignore_idx) continue;\n        ++n;",
                                "        ++n;"),
-    "mean_not_divided_by_n": ("g = (dloss ? dloss[0] : 1.0) / (double)n;",
+    "mean_not_divided_by_n": ("g = (dloss ? dloss[0] : 1.0) / denom;",
                               "g = (dloss ? dloss[0] : 1.0);"),
     "ties_away_from_zero": ("double r = nearbyint(v / q) * q;", "double r = round(v / q) * q;"),
     "combine_skips_rescale": ("if (p[1] > 0.0) d += p[1] * exp(p[0] - m);",
                               "if (p[1] > 0.0) d += p[1];"),
     "grad_missing_scale": ("grad[j] = g * (exp(x[j] - lse) - q);", "grad[j] = exp(x[j] - lse) - q;"),
     "fp16_subnormal_decode": ("v = ldexp((double)f, -24);", "v = ldexp((double)f, -25);"),
+    "weighted_target_weight_dropped": ("*loss = (1.0 - a) * w[y] * (lse - x[y])",
+                                       "*loss = (1.0 - a) * (lse - x[y])"),
+    "weighted_mean_over_count": ("const double denom = class_weights ? wsum : (double)n;",
+                                 "const double denom = (double)n;"),
 }
 
 
