@@ -117,7 +117,12 @@ typedef struct {
                                keep the row for the second (evict-last), 2 = evict-first */
     int tune_tile_kb;       /* stream and warp paths: 0 = default, else the ring tile size
                                (16 or 32 KB) */
-    int reserved[3];        /* must be zero */
+    const float* class_weights; /* NULL, or device float32[V]: per-class weights as in
+                               torch F.cross_entropy(weight=...): the smoothed target's
+                               class j term is weighted by w_j and the mean divides by
+                               the summed weight of the kept rows' targets.  Runs on the
+                               two-stage path (ce_fwd_bwd, ce_fwd_only; not ce_bwd) */
+    int reserved[2];        /* must be zero */
 } ce_options;
 
 /* Bytes of device workspace a call with these sizes needs (either entry

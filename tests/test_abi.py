@@ -93,7 +93,7 @@ def test_host_validation_rejects_before_launch(lib):
     assert _call(lib, wsb=100) == 4
     assert _call(lib, grad=0x9000) == 1        # the gradient must go in place
     o = _lib.make_options()
-    o.reserved[2] = 1
+    o.reserved[1] = 1
     assert _call(lib, opts=ctypes.byref(o)) == 1
     o = _lib.make_options(tune_threads=300)
     assert _call(lib, opts=ctypes.byref(o)) == 1

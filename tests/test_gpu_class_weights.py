@@ -1,0 +1,67 @@
+"""Per-class weights (torch F.cross_entropy(weight=...) semantics) on the GPU
+against the CPU oracle: per-row losses, the weighted mean, the gradient."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import vocabulary_cross_entropy_pass_gb300 as pkg
+from tests import harness
+from vocabulary_cross_entropy_pass_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda")
+
+
+@pytest.mark.parametrize("name", ["c1_bsv4096_f32", "c2_sbv8192_bf16", "c3h_bsv32000_f16_spiked",
+                                  "c5_bsv128000_bf16_ls"])
+def test_class_weighted_pass(name):
+    w = wl.WORKLOADS[name]
+    rng = np.random.default_rng(31)
+    cw = rng.uniform(0.1, 3.0, w.V).astype(np.float32)
+    x = wl.logits(w)
+    t = wl.targets(w)
+    rngd = np.random.default_rng(32)
+    dl = np.array([1.3]) if w.reduce_loss else rngd.uniform(0.5, 2.0, w.N).astype(np.float32)
+    ref = oracle.ce(harness.storage_np(x), harness.CODE[w.dtype], w.dim0, w.dim1, w.V,
+                    targets=t.numpy().ravel(), label_smoothing=w.label_smoothing,
+                    reduce_loss=w.reduce_loss, dloss=dl.astype(np.float64),
+                    class_weights=cw.astype(np.float64))
+    xd, td = x.to(DEV), t.to(DEV)
+    cwd = torch.tensor(cw, device=DEV)
+    n = torch.zeros(1, dtype=torch.int64, device=DEV)
+    loss = pkg.ce_fwd_bwd(xd, td, label_smoothing=w.label_smoothing, reduce_loss=w.reduce_loss,
+                          dloss=torch.tensor(dl, dtype=torch.float32, device=DEV),
+                          layout=w.layout, n_non_ignore_out=n, class_weights=cwd)
+    assert int(n.item()) == ref["n"]
+    harness.check_loss(loss.cpu().numpy(), ref["loss"], w.dtype, name)
+    g = xd.float().cpu().numpy().reshape(w.N, w.V).astype(np.float64)
+    excess, _ = harness.grad_errors(g, ref["grad"], w.dtype)
+    assert excess <= 0.0
+    # forward only gives the same losses
+    lf = pkg.ce_fwd_only(x.to(DEV), td, label_smoothing=w.label_smoothing,
+                         reduce_loss=w.reduce_loss, layout=w.layout, class_weights=cwd)
+    harness.check_loss(lf.cpu().numpy(), ref["loss"], w.dtype, name)
+
+
+def test_unit_weights_equal_unweighted():
+    w = wl.WORKLOADS["c2_sbv8192_bf16"]
+    x = wl.logits(w).to(DEV)
+    t = wl.targets(w).to(DEV)
+    a = x.clone()
+    la = pkg.ce_fwd_bwd(a, t, label_smoothing=0.1, reduce_loss=True, force_path=3)
+    b = x.clone()
+    lb = pkg.ce_fwd_bwd(b, t, label_smoothing=0.1, reduce_loss=True,
+                        class_weights=torch.ones(w.V, device=DEV))
+    harness.check_loss(lb.cpu().numpy(), la.cpu().numpy().astype(np.float64), "bf16")
+    excess, _ = harness.grad_errors(b.float().cpu().numpy().astype(np.float64).reshape(w.N, w.V),
+                                    a.float().cpu().numpy().astype(np.float64).reshape(w.N, w.V),
+                                    "bf16")
+    assert excess <= 0.0
+
+
+def test_weights_refuse_other_paths():
+    x = torch.zeros(1, 4, 4096, dtype=torch.bfloat16, device=DEV)
+    t = torch.zeros(1, 4, dtype=torch.int64, device=DEV)
+    with pytest.raises(pkg.CEError):
+        pkg.ce_fwd_bwd(x, t, force_path=4, class_weights=torch.ones(4096, device=DEV))

@@ -72,9 +72,14 @@ def _check(logits, targets):
         raise ValueError("the vocabulary dimension must be contiguous (call .contiguous())")
 
 
-def _options(opts, force_path, num_vocab_chunks):
+def _options(opts, force_path, num_vocab_chunks, class_weights=None):
     if opts is None:
         opts = make_options(force_path=force_path, num_vocab_chunks=num_vocab_chunks)
+    if class_weights is not None:
+        if class_weights.dtype != torch.float32 or not class_weights.is_cuda or \
+                class_weights.dim() != 1 or not class_weights.is_contiguous():
+            raise TypeError("class_weights must be a contiguous float32 CUDA vector of length V")
+        opts.class_weights = class_weights.data_ptr()
     return opts
 
 
@@ -118,17 +123,19 @@ def ce_fwd_bwd(logits: torch.Tensor, targets: torch.Tensor, label_smoothing: flo
                layout: str = "bsv", loss_out: torch.Tensor | None = None,
                n_non_ignore_out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
                force_path: int = CE_PATH_AUTO, num_vocab_chunks: int = 0, opts=None,
-               stream=None) -> torch.Tensor:
+               stream=None, class_weights: torch.Tensor | None = None) -> torch.Tensor:
     """Loss of every row (or the mean); the gradient overwrites ``logits``.
 
     ``dloss``: float32 CUDA tensor, one value (reduce_loss) or one per row;
-    None means 1.  Returns ``loss_out`` (allocated when None).
+    None means 1.  ``class_weights``: optional float32 CUDA vector of length V
+    (torch F.cross_entropy(weight=...) semantics).  Returns ``loss_out``
+    (allocated when None).
     """
     _check(logits, targets)
     lib = _lib.load()
     d0, d1, V, st = _dims(logits)
     ts = _tstrides(targets, d0, d1)
-    opts = _options(opts, force_path, num_vocab_chunks)
+    opts = _options(opts, force_path, num_vocab_chunks, class_weights)
     dev = logits.device
     if loss_out is None:
         loss_out = torch.empty(1 if reduce_loss else d0 * d1, dtype=torch.float32, device=dev)
@@ -154,13 +161,13 @@ def ce_fwd_only(logits: torch.Tensor, targets: torch.Tensor, label_smoothing: fl
                 loss_out: torch.Tensor | None = None, lse_out: torch.Tensor | None = None,
                 n_non_ignore_out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
                 force_path: int = CE_PATH_AUTO, num_vocab_chunks: int = 0, opts=None,
-                stream=None) -> torch.Tensor:
+                stream=None, class_weights: torch.Tensor | None = None) -> torch.Tensor:
     """Loss of every row (or the mean); ``logits`` is left untouched."""
     _check(logits, targets)
     lib = _lib.load()
     d0, d1, V, st = _dims(logits)
     ts = _tstrides(targets, d0, d1)
-    opts = _options(opts, force_path, num_vocab_chunks)
+    opts = _options(opts, force_path, num_vocab_chunks, class_weights)
     dev = logits.device
     if loss_out is None:
         loss_out = torch.empty(1 if reduce_loss else d0 * d1, dtype=torch.float32, device=dev)

@@ -49,7 +49,8 @@ class ce_options(ctypes.Structure):
         ("tune_ctas_per_sm", ctypes.c_int),
         ("tune_l2_keep", ctypes.c_int),
         ("tune_tile_kb", ctypes.c_int),
-        ("reserved", ctypes.c_int * 3),
+        ("class_weights", ctypes.c_void_p),
+        ("reserved", ctypes.c_int * 2),
     ]
 
 
@@ -116,7 +117,7 @@ def i64_array(vals):
 
 def make_options(force_path: int = 0, num_vocab_chunks: int = 0, event_begin=None, event_end=None,
                  tune_threads: int = 0, tune_stages: int = 0, tune_ctas_per_sm: int = 0,
-                 tune_l2_keep: int = 0, tune_tile_kb: int = 0):
+                 tune_l2_keep: int = 0, tune_tile_kb: int = 0, class_weights=None):
     o = ce_options()
     o.force_path = force_path
     o.num_vocab_chunks = num_vocab_chunks
@@ -127,4 +128,5 @@ def make_options(force_path: int = 0, num_vocab_chunks: int = 0, event_begin=Non
     o.tune_ctas_per_sm = tune_ctas_per_sm
     o.tune_l2_keep = tune_l2_keep
     o.tune_tile_kb = tune_tile_kb
+    o.class_weights = class_weights  # device address (int) or None
     return o

@@ -62,7 +62,7 @@ int round_up_int(int64_t x, int64_t m) { return (int)((x + m - 1) / m * m); }
 
 bool opts_clean(const ce_options* o) {
     if (!o) return true;
-    for (int i = 0; i < 3; ++i)
+    for (int i = 0; i < 2; ++i)
         if (o->reserved[i] != 0) return false;
     if (o->tune_tile_kb != 0 && o->tune_tile_kb != 16 && o->tune_tile_kb != 32) return false;
     if (o->force_path < 0 || o->force_path > CE_PATH_WARP) return false;
@@ -122,6 +122,17 @@ Plan make_plan(const Problem& p, const ce_options* o) {
     memset(&pl, 0, sizeof pl);
     const int force = o ? o->force_path : CE_PATH_AUTO;
     const bool aligned = fused_aligned(p) && p.V <= 0x7fffffffLL;
+    if (o && o->class_weights) {
+        // the class-weighted pass runs on the two-stage kernels only
+        if (force != CE_PATH_AUTO && force != CE_PATH_TWO_STAGE) {
+            pl.path = -2;
+            return pl;
+        }
+        pl.path = CE_PATH_TWO_STAGE;
+        pl.split.chunks = split_chunks(p.V, o);
+        pl.split.chunk = (p.V + pl.split.chunks - 1) / pl.split.chunks;
+        return pl;
+    }
     const int K = o ? o->num_vocab_chunks : 0;
     // Rows wider than one CTA's registers go through the stream kernel unless
     // a vocabulary split is asked for.
@@ -203,6 +214,9 @@ ce_status run_pass(Problem& pb, const ce_options* o, float* loss_out, int64_t* n
     pb.err = reinterpret_cast<uint32_t*>(w + kWsErrOffset);
     pb.n_dev = reinterpret_cast<int64_t*>(w + kWsCountOffset);
     pb.ticket = reinterpret_cast<uint32_t*>(w + kWsTicketOffset);
+    pb.cw = o ? o->class_weights : nullptr;
+    pb.wdenom = reinterpret_cast<double*>(w + kWsWeightDenomOffset);
+    pb.wsum = reinterpret_cast<double*>(w + kWsWeightSumOffset);
     // the stream and warp kernels compute the mean themselves (their last CTA)
     const bool mean_in_kernel =
         pb.reduce && (pl.path == CE_PATH_STREAM || pl.path == CE_PATH_WARP) && pb.N > 0;

@@ -6,7 +6,7 @@
 //   were unreliable there; here one CTA counts on the device with a
 //   fixed-order integer reduction, before the gradient pass needs dloss/n.
 // ce_mean_kernel: reduce_loss -- the mean of the per-row losses over the kept
-//   rows, summed in a fixed order (fixed per-thread strides, then a fixed
+//   rows (or over their summed class weight), summed in a fixed order (fixed per-thread strides, then a fixed
 //   butterfly and a fixed cross-warp order), so the result is bitwise the same
 //   on every run.
 #include "ce_device.cuh"
@@ -20,48 +20,68 @@ constexpr int kAuxThreads = 1024;
 __global__ void __launch_bounds__(kAuxThreads)
 ce_count_kernel(const int64_t* __restrict__ targets, int64_t ts0, int64_t ts1, int64_t dim1,
                 int64_t N, int64_t V, int64_t ignore_idx, int64_t* n_ws, int64_t* n_out,
-                uint32_t* err, uint32_t* ticket) {
+                uint32_t* err, uint32_t* ticket, const float* __restrict__ cw, double* wdenom,
+                double* wsum) {
     // the pass launched after this kernel may start now: it waits for this
     // kernel's results itself (griddepcontrol.wait) before it reads them
     griddep_launch_dependents();
     __shared__ long long s_n[kAuxThreads / 32];
     __shared__ unsigned s_e[kAuxThreads / 32];
+    __shared__ double s_wd[kAuxThreads / 32], s_ws[kAuxThreads / 32];
     long long n = 0;
     unsigned e = 0;
+    double wd = 0.0, ws = 0.0;
     for (int64_t r = threadIdx.x; r < N; r += kAuxThreads) {
         const int64_t i = r / dim1, j = r - i * dim1;
         const int64_t y = targets[i * ts0 + j * ts1];
         if (y == ignore_idx) continue;
         ++n;
-        if (y < 0 || y >= V) e |= CE_DEVERR_TARGET_RANGE;
+        if (y < 0 || y >= V)
+            e |= CE_DEVERR_TARGET_RANGE;
+        else if (cw)
+            wd += (double)cw[y];
     }
+    if (cw)
+        for (int64_t v = threadIdx.x; v < V; v += kAuxThreads) ws += (double)cw[v];
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
         n += __shfl_xor_sync(kFull, n, off);
         e |= __shfl_xor_sync(kFull, e, off);
+        wd += __shfl_xor_sync(kFull, wd, off);
+        ws += __shfl_xor_sync(kFull, ws, off);
     }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (lane == 0) {
         s_n[warp] = n;
         s_e[warp] = e;
+        s_wd[warp] = wd;
+        s_ws[warp] = ws;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
         long long tn = 0;
         unsigned te = 0;
+        double twd = 0.0, tws = 0.0;
         for (int w = 0; w < kAuxThreads / 32; ++w) {
             tn += s_n[w];
             te |= s_e[w];
+            twd += s_wd[w];
+            tws += s_ws[w];
         }
         *n_ws = tn;
         if (n_out) *n_out = tn;
         *err = te;     // starts the error word of this pass
         *ticket = 0u;  // no CTA of the pass has finished yet
+        if (cw) {
+            *wdenom = twd;
+            *wsum = tws;
+        }
     }
 }
 
 __global__ void __launch_bounds__(kAuxThreads)
-ce_mean_kernel(const float* __restrict__ loss_rows, int64_t N, const int64_t* n_dev, float* out) {
+ce_mean_kernel(const float* __restrict__ loss_rows, int64_t N, const int64_t* n_dev,
+               const double* wdenom, float* out) {
     __shared__ double s_sum[kAuxThreads / 32];
     double acc = 0.0;
     for (int64_t r = threadIdx.x; r < N; r += kAuxThreads) acc += (double)loss_rows[r];
@@ -73,8 +93,9 @@ ce_mean_kernel(const float* __restrict__ loss_rows, int64_t N, const int64_t* n_
     if (threadIdx.x == 0) {
         double t = 0.0;
         for (int w = 0; w < kAuxThreads / 32; ++w) t += s_sum[w];
-        const long long n = *n_dev;
-        out[0] = (float)(t / (double)n);  // 0/0 = NaN when every row is ignored
+        // the mean over kept rows, or over their summed class weight
+        const double den = wdenom ? *wdenom : (double)(*n_dev);
+        out[0] = (float)(t / den);  // 0/0 = NaN when every row is ignored
     }
 }
 
@@ -82,7 +103,8 @@ ce_mean_kernel(const float* __restrict__ loss_rows, int64_t N, const int64_t* n_
 
 cudaError_t launch_count(const Problem& p, int64_t* n_out, cudaStream_t s) {
     ce_count_kernel<<<1, kAuxThreads, 0, s>>>(p.targets, p.ts0, p.ts1, p.dim1, p.N, p.V,
-                                              p.ignore_idx, p.n_dev, n_out, p.err, p.ticket);
+                                              p.ignore_idx, p.n_dev, n_out, p.err, p.ticket, p.cw,
+                                              p.wdenom, p.wsum);
     return cudaGetLastError();
 }
 
@@ -92,7 +114,8 @@ void set_pdl_attr(cudaLaunchAttribute* attr) {
 }
 
 cudaError_t launch_reduce_mean(const Problem& p, float* loss_out, cudaStream_t s) {
-    ce_mean_kernel<<<1, kAuxThreads, 0, s>>>(p.loss_rows, p.N, p.n_dev, loss_out);
+    ce_mean_kernel<<<1, kAuxThreads, 0, s>>>(p.loss_rows, p.N, p.n_dev, p.cw ? p.wdenom : nullptr,
+                                             loss_out);
     return cudaGetLastError();
 }
 

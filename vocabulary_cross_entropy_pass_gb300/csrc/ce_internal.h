@@ -14,11 +14,15 @@ namespace gbce {
 //   [0, 4)      uint32 device error word
 //   [8, 16)     int64 n_non_ignore of the last pass
 //   [16, 20)    uint32 count of CTAs done (the stream kernel's in-kernel mean)
+//   [24, 32)    double summed class weight of the kept rows' targets (weighted pass)
+//   [32, 40)    double summed class weight over the vocabulary (weighted pass)
 //   [256, ...)  float per-row losses (N) -- used when reduce_loss
 //   [...]       float4 per-(row, chunk) partials of the two-stage path
 constexpr size_t kWsErrOffset = 0;
 constexpr size_t kWsCountOffset = 8;
 constexpr size_t kWsTicketOffset = 16;
+constexpr size_t kWsWeightDenomOffset = 24;
+constexpr size_t kWsWeightSumOffset = 32;
 constexpr size_t kWsHeaderBytes = 256;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -42,6 +46,9 @@ struct Problem {
     int64_t* n_dev;            // device count
     uint32_t* ticket;          // CTAs-done counter, zeroed by the count kernel
     float* mean_out;           // stream path with reduce_loss: the mean, written in-kernel
+    const float* cw;           // class weights [V] or NULL
+    double* wdenom;            // summed weight of kept targets (weighted pass)
+    double* wsum;              // summed weight over the vocabulary (weighted pass)
 };
 
 // Plan of the fused (row / cluster) kernel.

@@ -11,8 +11,9 @@
 //
 // This path takes any alignment and any row strides (scalar element loads);
 // the row and cluster paths need 16-byte aligned rows.  It reads the logits
-// twice, so it is the fallback, and the forced second implementation of the
-// vocabulary-split workloads.
+// twice, so it is the fallback, the forced second implementation of the
+// vocabulary-split workloads, and the path of the class-weighted pass
+// (weights as in torch F.cross_entropy(weight=...)).
 #include "ce_device.cuh"
 #include "ce_internal.h"
 
@@ -35,6 +36,9 @@ struct SplitArgs {
     float* lse_out;
     const int64_t* n_dev;
     float4* part;  // [N][K]
+    const float* cw;         // class weights [V] (weighted pass) or NULL
+    const double* wdenom;    // summed weight of the kept rows' targets
+    const double* wsum;      // summed weight over the vocabulary
 };
 
 __device__ __forceinline__ void row_of(const SplitArgs& p, int64_t r, int64_t& y, int64_t& off) {
@@ -43,7 +47,8 @@ __device__ __forceinline__ void row_of(const SplitArgs& p, int64_t r, int64_t& y
     off = i * p.s0 + j * p.s1;
 }
 
-template <typename T>
+// WT: the class-weighted pass, whose third statistic is sum_j w_j x_j.
+template <typename T, bool WT>
 __global__ void __launch_bounds__(kSplitThreads) ce_split_stats_kernel(const __grid_constant__ SplitArgs p) {
     using VT = Vec<T>;
     __shared__ float s_red[kSplitWarps];
@@ -73,7 +78,7 @@ __global__ void __launch_bounds__(kSplitThreads) ce_split_stats_kernel(const __g
     for (int64_t v = k0 + threadIdx.x; v < k1; v += kSplitThreads) {
         const float x = VT::load1(row + v * (int64_t)sizeof(T));
         d += ex2_approx(fmaf(x, kLog2e, -ml));
-        S += x;
+        S = WT ? fmaf(__ldg(p.cw + v), x, S) : S + x;
     }
     d = warp_allsum(d);
     S = warp_allsum(S);
@@ -90,7 +95,7 @@ __global__ void __launch_bounds__(kSplitThreads) ce_split_stats_kernel(const __g
     }
 }
 
-template <typename T, bool GRAD>
+template <typename T, bool GRAD, bool WT>
 __global__ void __launch_bounds__(kSplitThreads) ce_split_grad_kernel(const __grid_constant__ SplitArgs p) {
     using VT = Vec<T>;
     __shared__ float s_lse, s_S, s_xy;
@@ -128,7 +133,13 @@ __global__ void __launch_bounds__(kSplitThreads) ce_split_grad_kernel(const __gr
         s_S = G.S;
         s_xy = pr[y / p.chunk].w;
         if (k == 0) {
-            p.loss[r] = lse - (1.f - p.a) * pr[y / p.chunk].w - p.a_over_v * G.S;
+            float loss;
+            if (WT)  // (1-a) w_y (lse - x_y) + (a/V) (W lse - sum_j w_j x_j)
+                loss = (1.f - p.a) * __ldg(p.cw + y) * (lse - pr[y / p.chunk].w) +
+                       p.a_over_v * ((float)(*p.wsum) * lse - G.S);
+            else
+                loss = lse - (1.f - p.a) * pr[y / p.chunk].w - p.a_over_v * G.S;
+            p.loss[r] = loss;
             if (p.lse_out) p.lse_out[r] = lse;
         }
     }
@@ -137,11 +148,24 @@ __global__ void __launch_bounds__(kSplitThreads) ce_split_grad_kernel(const __gr
     const float lse = s_lse;
     float g;
     if (p.reduce)
-        g = (p.dloss ? p.dloss[0] : 1.f) / (float)(*p.n_dev);
+        g = (p.dloss ? p.dloss[0] : 1.f) / (WT ? (float)(*p.wdenom) : (float)(*p.n_dev));
     else
         g = p.dloss ? p.dloss[r] : 1.f;
-    const float bb = g * p.a_over_v;
     const float lsel = lse * kLog2e;
+    if (WT) {
+        // g (softmax_j ((1-a) w_y + (a/V) W) - (a/V) w_j) - g (1-a) w_y [j == y]
+        const float wy = __ldg(p.cw + y);
+        const float c = g * ((1.f - p.a) * wy + p.a_over_v * (float)(*p.wsum));
+        const float ga = g * p.a_over_v;
+        for (int64_t v = k0 + threadIdx.x; v < k1; v += kSplitThreads) {
+            const float x = VT::load1(row + v * (int64_t)sizeof(T));
+            float o = fmaf(ex2_approx(fmaf(x, kLog2e, -lsel)), c, -ga * __ldg(p.cw + v));
+            if (v == y) o -= g * (1.f - p.a) * wy;
+            VT::store1(row + v * (int64_t)sizeof(T), o);
+        }
+        return;
+    }
+    const float bb = g * p.a_over_v;
     for (int64_t v = k0 + threadIdx.x; v < k1; v += kSplitThreads) {
         const float x = VT::load1(row + v * (int64_t)sizeof(T));
         float o = fmaf(ex2_approx(fmaf(x, kLog2e, -lsel)), g, -bb);
@@ -174,15 +198,29 @@ cudaError_t launch_split_typed(const Problem& pb, const SplitPlan& plan, float4*
     a.lse_out = pb.lse_out;
     a.n_dev = pb.n_dev;
     a.part = partials;
+    a.cw = pb.cw;
+    a.wdenom = pb.wdenom;
+    a.wsum = pb.wsum;
     const int64_t blocks = pb.N * plan.chunks;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    ce_split_stats_kernel<T><<<(unsigned)blocks, kSplitThreads, 0, s>>>(a);
+    const bool wt = pb.cw != nullptr;
+    if (wt)
+        ce_split_stats_kernel<T, true><<<(unsigned)blocks, kSplitThreads, 0, s>>>(a);
+    else
+        ce_split_stats_kernel<T, false><<<(unsigned)blocks, kSplitThreads, 0, s>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if (pb.grad)
-        ce_split_grad_kernel<T, true><<<(unsigned)blocks, kSplitThreads, 0, s>>>(a);
-    else
-        ce_split_grad_kernel<T, false><<<(unsigned)pb.N, kSplitThreads, 0, s>>>(a);
+    if (pb.grad) {
+        if (wt)
+            ce_split_grad_kernel<T, true, true><<<(unsigned)blocks, kSplitThreads, 0, s>>>(a);
+        else
+            ce_split_grad_kernel<T, true, false><<<(unsigned)blocks, kSplitThreads, 0, s>>>(a);
+    } else {
+        if (wt)
+            ce_split_grad_kernel<T, false, true><<<(unsigned)pb.N, kSplitThreads, 0, s>>>(a);
+        else
+            ce_split_grad_kernel<T, false, false><<<(unsigned)pb.N, kSplitThreads, 0, s>>>(a);
+    }
     return cudaGetLastError();
 }
 
