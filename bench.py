@@ -281,6 +281,14 @@ def run_ours(args, w, rank: int, world: int, dist) -> None:
         def step(o=opts):
             pkg.ce_fwd_bwd(x, t, label_smoothing=w.label_smoothing, ignore_idx=w.ignore_idx,
                            reduce_loss=w.reduce_loss, loss_out=loss, workspace=ws, opts=o)
+    elif mode == "weighted":
+        # per-class weights (torch F.cross_entropy(weight=...)): the two-stage kernels
+        cw = torch.empty(w.V, dtype=torch.float32, device=dev).uniform_(0.1, 3.0)
+
+        def step(o=opts):
+            pkg.ce_fwd_bwd(x, t, label_smoothing=w.label_smoothing, ignore_idx=w.ignore_idx,
+                           reduce_loss=w.reduce_loss, loss_out=loss, workspace=ws,
+                           class_weights=cw)
     elif mode == "split":
         # forward only (saves lse and the kept-row count), then the backward
         lse = torch.empty(w.N, dtype=torch.float32, device=dev)
@@ -375,6 +383,8 @@ def run_ours(args, w, rank: int, world: int, dist) -> None:
                                                      "vocab_shards": args.vocab_shards
                                                      if mode == "vp" else None},
                     "roofline": {"bound": "hbm", "kernel": "whole step (two reads + one write)",
+                                 "note": "weighted mode: the class weights are read from L2"
+                                 if mode == "weighted" else None,
                                  "achieved": nb / (ms / args.steps / 1e3) / 1e9,
                                  "peak": measured_peaks()["hbm_gbs"], "unit": "GB/s",
                                  "frac": nb / (ms / args.steps / 1e3) / 1e9
@@ -453,8 +463,9 @@ def main(argv=None) -> int:
     ap.add_argument("--ref-rows", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     # secondary passes: "split" = ce_fwd_only + ce_bwd (autograd order), "vp" = the
-    # vocabulary-parallel steps over --vocab-shards shards on one GPU
-    ap.add_argument("--mode", choices=["fused", "split", "vp"], default="fused")
+    # vocabulary-parallel steps over --vocab-shards shards on one GPU, "weighted" =
+    # the class-weighted pass
+    ap.add_argument("--mode", choices=["fused", "split", "vp", "weighted"], default="fused")
     ap.add_argument("--vocab-shards", type=int, default=8)
     # planner overrides, for tuning sweeps (defaults: the planner's choice)
     ap.add_argument("--force-path", type=int, default=0)

@@ -49,7 +49,7 @@ def test_oversized_problems_are_rejected_on_the_host():
                                       _lib.i64_array((d1, 1)), 0.0, -100, 1, None, loss,
                                       ctypes.c_void_p(0x1000), None, ctypes.byref(opts), None)
     assert call(600_000, 4096) == 4                 # per-row losses alone exceed 2 MiB
-    assert call(5_000, 128000, force_path=3) == 4   # two-stage partials exceed 2 MiB
+    assert call(20_000, 128000, force_path=3) == 4  # two-stage partials exceed 2 MiB
     assert call(8, 4096, tune_threads=300) == 1     # ordinary argument checks still apply
 
 

@@ -47,11 +47,23 @@ __device__ __forceinline__ void row_of(const SplitArgs& p, int64_t r, int64_t& y
     off = i * p.s0 + j * p.s1;
 }
 
-// WT: the class-weighted pass, whose third statistic is sum_j w_j x_j.
-template <typename T, bool WT>
+// Per-thread running statistics of one element (scalar path) or of one
+// 16-byte vector (vector path): a new maximum rescales the sum first.
+__device__ __forceinline__ void stats_push(float x, float& m, float& d) {
+    if (x > m) {
+        if (m != -INFINITY) d *= ex2_approx((m - x) * kLog2e);
+        m = x;
+    }
+    d += ex2_approx(fmaf(x, kLog2e, -m * kLog2e));
+}
+
+// Stage 1.  WT: the class-weighted pass, whose third statistic is
+// sum_j w_j x_j.  VECOK: rows 16-byte aligned, read in 16-byte vectors.
+template <typename T, bool WT, bool VECOK>
 __global__ void __launch_bounds__(kSplitThreads) ce_split_stats_kernel(const __grid_constant__ SplitArgs p) {
     using VT = Vec<T>;
-    __shared__ float s_red[kSplitWarps];
+    constexpr int VEC = VT::kElems;
+    constexpr int ES = sizeof(T);
     __shared__ float4 s_part[kSplitWarps];
     const int64_t b = blockIdx.x;
     const int64_t r = b / p.K;
@@ -61,44 +73,58 @@ __global__ void __launch_bounds__(kSplitThreads) ce_split_stats_kernel(const __g
     if (y == p.ignore_idx || y < 0 || y >= p.V) return;
     const int64_t k0 = (int64_t)k * p.chunk;
     const int64_t k1 = min(p.V, k0 + p.chunk);
-    const char* row = p.logits + off * (int64_t)sizeof(T);
+    const char* row = p.logits + off * (int64_t)ES;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
-    float m = -INFINITY;
-    for (int64_t v = k0 + threadIdx.x; v < k1; v += kSplitThreads)
-        m = fmaxf(m, VT::load1(row + v * (int64_t)sizeof(T)));
-    m = warp_allmax(m);
-    if (lane == 0) s_red[warp] = m;
-    __syncthreads();
-    m = -INFINITY;
-    for (int w = 0; w < kSplitWarps; ++w) m = fmaxf(m, s_red[w]);
-    const float ml = (m == -INFINITY) ? 0.f : m * kLog2e;
-
-    float d = 0.f, S = 0.f;
-    for (int64_t v = k0 + threadIdx.x; v < k1; v += kSplitThreads) {
-        const float x = VT::load1(row + v * (int64_t)sizeof(T));
-        d += ex2_approx(fmaf(x, kLog2e, -ml));
-        S = WT ? fmaf(__ldg(p.cw + v), x, S) : S + x;
+    float m = -INFINITY, d = 0.f, S = 0.f;
+    if (VECOK) {
+        // chunk boundaries are multiples of the vector length
+        const uint4* rv = reinterpret_cast<const uint4*>(row);
+        for (int64_t v = k0 / VEC + threadIdx.x; v < k1 / VEC; v += kSplitThreads) {
+            const uint4 raw = __ldcs(rv + v);
+            const float vm = VT::vmax(raw);
+            if (vm > m) {
+                if (m != -INFINITY) d *= ex2_approx((m - vm) * kLog2e);
+                m = vm;
+            }
+            const float nml = -m * kLog2e;
+            float x[VEC];
+            VT::unpack(raw, x);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                d += ex2_approx(fmaf(x[e], kLog2e, nml));
+                S = WT ? fmaf(__ldg(p.cw + v * VEC + e), x[e], S) : S + x[e];
+            }
+        }
+    } else {
+        for (int64_t v = k0 + threadIdx.x; v < k1; v += kSplitThreads) {
+            const float x = VT::load1(row + v * ES);
+            stats_push(x, m, d);
+            S = WT ? fmaf(__ldg(p.cw + v), x, S) : S + x;
+        }
     }
-    d = warp_allsum(d);
-    S = warp_allsum(S);
-    if (lane == 0) s_part[warp] = make_float4(0.f, d, S, 0.f);
+    Part q = warp_allreduce_part(Part{m, d, S});
+    if (lane == 0) s_part[warp] = make_float4(q.m, q.d, q.S, 0.f);
     __syncthreads();
     if (threadIdx.x == 0) {
-        float td = 0.f, tS = 0.f;
-        for (int w = 0; w < kSplitWarps; ++w) {
-            td += s_part[w].y;
-            tS += s_part[w].z;
-        }
-        const float xy = (y >= k0 && y < k1) ? VT::load1(row + y * (int64_t)sizeof(T)) : 0.f;
-        p.part[r * p.K + k] = make_float4(m, td, tS, xy);
+        Part G = part_identity();
+        for (int w = 0; w < kSplitWarps; ++w)
+            G = part_combine(G, Part{s_part[w].x, s_part[w].y, s_part[w].z});
+        const float xy = (y >= k0 && y < k1) ? VT::load1(row + y * ES) : 0.f;
+        p.part[r * p.K + k] = make_float4(G.m, G.d, G.S, xy);
     }
 }
 
-template <typename T, bool GRAD, bool WT>
+// Stage 2: the row's K partials combined by one warp in a fixed order (lane
+// l takes partials l, l+32, ... in turn, then a butterfly), then the loss and
+// the gradient of this CTA's chunk.
+template <typename T, bool GRAD, bool WT, bool VECOK>
 __global__ void __launch_bounds__(kSplitThreads) ce_split_grad_kernel(const __grid_constant__ SplitArgs p) {
     using VT = Vec<T>;
-    __shared__ float s_lse, s_S, s_xy;
+    constexpr int VEC = VT::kElems;
+    constexpr int ES = sizeof(T);
+    constexpr int PP = VEC / 2;
+    __shared__ float s_lse, s_S;
     const int kper = GRAD ? p.K : 1;  // without a gradient one CTA per row
     const int64_t b = blockIdx.x;
     const int64_t r = b / kper;
@@ -107,12 +133,20 @@ __global__ void __launch_bounds__(kSplitThreads) ce_split_grad_kernel(const __gr
     row_of(p, r, y, off);
     const int64_t k0 = (int64_t)k * p.chunk;
     const int64_t k1 = min(p.V, k0 + p.chunk);
-    char* row = p.logits + off * (int64_t)sizeof(T);
+    char* row = p.logits + off * (int64_t)ES;
 
     if (y == p.ignore_idx || y < 0 || y >= p.V) {
-        if (GRAD)
-            for (int64_t v = k0 + threadIdx.x; v < k1; v += kSplitThreads)
-                VT::store1(row + v * (int64_t)sizeof(T), 0.f);
+        if (GRAD) {
+            if (VECOK) {
+                const uint4 z = make_uint4(0, 0, 0, 0);
+                uint4* rv = reinterpret_cast<uint4*>(row);
+                for (int64_t v = k0 / VEC + threadIdx.x; v < k1 / VEC; v += kSplitThreads)
+                    stg128_stream(rv + v, z);
+            } else {
+                for (int64_t v = k0 + threadIdx.x; v < k1; v += kSplitThreads)
+                    VT::store1(row + v * ES, 0.f);
+            }
+        }
         if (k == 0 && threadIdx.x == 0) {
             p.loss[r] = (y == p.ignore_idx) ? 0.f : __int_as_float(0x7fc00000);
             if (p.lse_out) p.lse_out[r] = __int_as_float(0x7fc00000);
@@ -120,27 +154,30 @@ __global__ void __launch_bounds__(kSplitThreads) ce_split_grad_kernel(const __gr
         return;
     }
 
-    if (threadIdx.x == 0) {
-        // combine the K partials in chunk order
-        Part G = part_identity();
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x < 32) {
         const float4* pr = p.part + r * p.K;
-        for (int q = 0; q < p.K; ++q) {
+        Part G = part_identity();
+        for (int q = lane; q < p.K; q += 32) {
             const float4 w = pr[q];
             G = part_combine(G, Part{w.x, w.y, w.z});
         }
-        const float lse = G.m + logf(G.d);
-        s_lse = lse;
-        s_S = G.S;
-        s_xy = pr[y / p.chunk].w;
-        if (k == 0) {
-            float loss;
-            if (WT)  // (1-a) w_y (lse - x_y) + (a/V) (W lse - sum_j w_j x_j)
-                loss = (1.f - p.a) * __ldg(p.cw + y) * (lse - pr[y / p.chunk].w) +
-                       p.a_over_v * ((float)(*p.wsum) * lse - G.S);
-            else
-                loss = lse - (1.f - p.a) * pr[y / p.chunk].w - p.a_over_v * G.S;
-            p.loss[r] = loss;
-            if (p.lse_out) p.lse_out[r] = lse;
+        G = warp_allreduce_part(G);
+        if (lane == 0) {
+            const float lse = G.m + logf(G.d);
+            const float xy = pr[y / p.chunk].w;
+            s_lse = lse;
+            s_S = G.S;
+            if (k == 0) {
+                float loss;
+                if (WT)  // (1-a) w_y (lse - x_y) + (a/V) (W lse - sum_j w_j x_j)
+                    loss = (1.f - p.a) * __ldg(p.cw + y) * (lse - xy) +
+                           p.a_over_v * ((float)(*p.wsum) * lse - G.S);
+                else
+                    loss = lse - (1.f - p.a) * xy - p.a_over_v * G.S;
+                p.loss[r] = loss;
+                if (p.lse_out) p.lse_out[r] = lse;
+            }
         }
     }
     if (!GRAD) return;
@@ -151,26 +188,51 @@ __global__ void __launch_bounds__(kSplitThreads) ce_split_grad_kernel(const __gr
         g = (p.dloss ? p.dloss[0] : 1.f) / (WT ? (float)(*p.wdenom) : (float)(*p.n_dev));
     else
         g = p.dloss ? p.dloss[r] : 1.f;
-    const float lsel = lse * kLog2e;
-    if (WT) {
-        // g (softmax_j ((1-a) w_y + (a/V) W) - (a/V) w_j) - g (1-a) w_y [j == y]
-        const float wy = __ldg(p.cw + y);
-        const float c = g * ((1.f - p.a) * wy + p.a_over_v * (float)(*p.wsum));
-        const float ga = g * p.a_over_v;
-        for (int64_t v = k0 + threadIdx.x; v < k1; v += kSplitThreads) {
-            const float x = VT::load1(row + v * (int64_t)sizeof(T));
-            float o = fmaf(ex2_approx(fmaf(x, kLog2e, -lsel)), c, -ga * __ldg(p.cw + v));
-            if (v == y) o -= g * (1.f - p.a) * wy;
-            VT::store1(row + v * (int64_t)sizeof(T), o);
+    const float nll = -lse * kLog2e;
+    // gradient = c * softmax - b_j, minus the one-hot term at the target:
+    //   unweighted c = g, b_j = g a/V;  weighted c = g ((1-a) w_y + (a/V) W),
+    //   b_j = g (a/V) w_j, one-hot term g (1-a) w_y
+    const float wy = WT ? __ldg(p.cw + y) : 1.f;
+    const float c = WT ? g * ((1.f - p.a) * wy + p.a_over_v * (float)(*p.wsum)) : g;
+    const float ga = g * p.a_over_v;
+    const float hit = g * (1.f - p.a) * wy;
+    if (VECOK) {
+        const float2 L2 = make_float2(kLog2e, kLog2e), NL = make_float2(nll, nll);
+        const float2 C2 = make_float2(c, c), NB = make_float2(-ga, -ga);
+        uint4* rv = reinterpret_cast<uint4*>(row);
+        for (int64_t v = k0 / VEC + threadIdx.x; v < k1 / VEC; v += kSplitThreads) {
+            const uint4 raw = __ldcs(rv + v);
+            float2 x[PP], o[PP];
+            VT::unpack2(raw, x);
+#pragma unroll
+            for (int q = 0; q < PP; ++q) {
+                const float2 e = __ffma2_rn(x[q], L2, NL);
+                const float2 pe = make_float2(ex2_approx(e.x), ex2_approx(e.y));
+                if (WT) {
+                    const float w0 = __ldg(p.cw + v * VEC + 2 * q), w1 = __ldg(p.cw + v * VEC + 2 * q + 1);
+                    o[q] = __ffma2_rn(pe, C2, make_float2(-ga * w0, -ga * w1));
+                } else {
+                    o[q] = __ffma2_rn(pe, C2, NB);
+                }
+            }
+            if (v == y / VEC) {
+                const int ey = (int)(y % VEC);
+#pragma unroll
+                for (int q = 0; q < PP; ++q) {
+                    if (2 * q == ey) o[q].x -= hit;
+                    if (2 * q + 1 == ey) o[q].y -= hit;
+                }
+            }
+            stg128_stream(rv + v, VT::pack2(o));
         }
-        return;
-    }
-    const float bb = g * p.a_over_v;
-    for (int64_t v = k0 + threadIdx.x; v < k1; v += kSplitThreads) {
-        const float x = VT::load1(row + v * (int64_t)sizeof(T));
-        float o = fmaf(ex2_approx(fmaf(x, kLog2e, -lsel)), g, -bb);
-        if (v == y) o -= g * (1.f - p.a);
-        VT::store1(row + v * (int64_t)sizeof(T), o);
+    } else {
+        for (int64_t v = k0 + threadIdx.x; v < k1; v += kSplitThreads) {
+            const float x = VT::load1(row + v * ES);
+            const float bj = WT ? ga * __ldg(p.cw + v) : ga;
+            float o = fmaf(ex2_approx(fmaf(x, kLog2e, nll)), c, -bj);
+            if (v == y) o -= hit;
+            VT::store1(row + v * ES, o);
+        }
     }
 }
 
@@ -204,30 +266,38 @@ cudaError_t launch_split_typed(const Problem& pb, const SplitPlan& plan, float4*
     const int64_t blocks = pb.N * plan.chunks;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const bool wt = pb.cw != nullptr;
-    if (wt)
-        ce_split_stats_kernel<T, true><<<(unsigned)blocks, kSplitThreads, 0, s>>>(a);
+    // 16-byte vectors when every row and chunk boundary is 16-byte aligned
+    const bool vec = reinterpret_cast<uintptr_t>(pb.logits) % 16 == 0 &&
+                     (pb.s0 * (int64_t)sizeof(T)) % 16 == 0 && (pb.s1 * (int64_t)sizeof(T)) % 16 == 0 &&
+                     (pb.V * (int64_t)sizeof(T)) % 16 == 0 &&
+                     (plan.chunk * (int64_t)sizeof(T)) % 16 == 0;
+    const unsigned gs = (unsigned)blocks, gr = (unsigned)(pb.grad ? blocks : pb.N);
+#define CE_SPLIT_LAUNCH(W, VK)                                                     \
+    do {                                                                           \
+        ce_split_stats_kernel<T, W, VK><<<gs, kSplitThreads, 0, s>>>(a);           \
+        cudaError_t e_ = cudaGetLastError();                                       \
+        if (e_ != cudaSuccess) return e_;                                          \
+        if (pb.grad)                                                               \
+            ce_split_grad_kernel<T, true, W, VK><<<gr, kSplitThreads, 0, s>>>(a);  \
+        else                                                                       \
+            ce_split_grad_kernel<T, false, W, VK><<<gr, kSplitThreads, 0, s>>>(a); \
+    } while (0)
+    if (wt && vec)
+        CE_SPLIT_LAUNCH(true, true);
+    else if (wt)
+        CE_SPLIT_LAUNCH(true, false);
+    else if (vec)
+        CE_SPLIT_LAUNCH(false, true);
     else
-        ce_split_stats_kernel<T, false><<<(unsigned)blocks, kSplitThreads, 0, s>>>(a);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    if (pb.grad) {
-        if (wt)
-            ce_split_grad_kernel<T, true, true><<<(unsigned)blocks, kSplitThreads, 0, s>>>(a);
-        else
-            ce_split_grad_kernel<T, true, false><<<(unsigned)blocks, kSplitThreads, 0, s>>>(a);
-    } else {
-        if (wt)
-            ce_split_grad_kernel<T, false, true><<<(unsigned)pb.N, kSplitThreads, 0, s>>>(a);
-        else
-            ce_split_grad_kernel<T, false, false><<<(unsigned)pb.N, kSplitThreads, 0, s>>>(a);
-    }
+        CE_SPLIT_LAUNCH(false, false);
+#undef CE_SPLIT_LAUNCH
     return cudaGetLastError();
 }
 
 }  // namespace
 
 int split_auto_chunks(int64_t V) {
-    int64_t k = (V + 4095) / 4096;  // about 16 elements per thread
+    int64_t k = (V + 16383) / 16384;  // 64 elements per thread
     if (k < 1) k = 1;
     if (k > 4096) k = 4096;
     return (int)k;
