@@ -340,6 +340,84 @@ int oracle_ce(const void* logits, int dtype, int64_t dim0, int64_t dim1, int64_t
     return 0;
 }
 
+/* ---------------------------------------------------------------------------
+ * lm_head + cross-entropy, the chunked-loss pipeline of the TorchTitan
+ * ChunkedLossWrapper that hyper-parallel #269 describes (background: a
+ * sequence-chunked lm_head + CE to bound the O(B*L*V) logits memory), in the
+ * dataflow of a training step where hidden states, weights, logits and the
+ * logits gradient are tensors of the storage dtype:
+ *   logits = round_T(hidden . weight^T)          (double sum, one rounding)
+ *   loss, dlogits_exact = the cross-entropy pass of oracle_ce on those logits
+ *   dlogits = round_T(dlogits_exact)             (the pass writes dtype T)
+ *   grad_hidden = dlogits . weight               (double, not rounded)
+ *   grad_weight = dlogits^T . hidden             (double, not rounded)
+ *   hidden [N][H], weight [V][H] row-major storage of `dtype`; targets [N].
+ *   loss_out: N values or 1 (reduce); grad_hidden [N][H], grad_weight [V][H]
+ *   doubles, either may be NULL.
+ * Returns 0, or -1 when host memory runs out.
+ * ------------------------------------------------------------------------- */
+int oracle_linear_ce(const void* hidden, const void* weight, int dtype, int64_t N, int64_t H,
+                     int64_t V, const int64_t* targets, double a, int64_t ignore_idx, int reduce,
+                     const double* dloss, double* loss_out, double* grad_hidden,
+                     double* grad_weight, int64_t* n_out, uint32_t* err_out) {
+    /* logits rounded to the storage dtype, stored as that dtype's bits so the
+     * pass below reads them exactly as a GPU tensor of that dtype */
+    const size_t es = dtype == ORACLE_F32 ? 4 : 2;
+    unsigned char* lg = (unsigned char*)malloc((size_t)(N > 0 ? N : 1) * (size_t)V * es);
+    double* dl = (double*)malloc((size_t)(N > 0 ? N : 1) * (size_t)V * sizeof(double));
+    if (!lg || !dl) {
+        free(lg);
+        free(dl);
+        return -1;
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < N; ++r) {
+        for (int64_t v = 0; v < V; ++v) {
+            double acc = 0.0;
+            for (int64_t h = 0; h < H; ++h)
+                acc += oracle_decode(hidden, dtype, r * H + h) * oracle_decode(weight, dtype, v * H + h);
+            uint32_t bits = oracle_encode(acc, dtype);
+            if (es == 4)
+                memcpy(lg + ((size_t)r * V + v) * 4, &bits, 4);
+            else {
+                uint16_t b16 = (uint16_t)bits;
+                memcpy(lg + ((size_t)r * V + v) * 2, &b16, 2);
+            }
+        }
+    }
+    int rc = oracle_ce(lg, dtype, 1, N, V, N * V, V, targets, N, 1, a, ignore_idx, reduce, dloss,
+                       NULL, loss_out, NULL, dl, n_out, err_out);
+    free(lg);
+    if (rc != 0) {
+        free(dl);
+        return rc;
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < N * V; ++i) dl[i] = oracle_round(dl[i], dtype);
+    if (grad_hidden) {
+#pragma omp parallel for schedule(static)
+        for (int64_t r = 0; r < N; ++r)
+            for (int64_t h = 0; h < H; ++h) {
+                double acc = 0.0;
+                for (int64_t v = 0; v < V; ++v)
+                    acc += dl[r * V + v] * oracle_decode(weight, dtype, v * H + h);
+                grad_hidden[r * H + h] = acc;
+            }
+    }
+    if (grad_weight) {
+#pragma omp parallel for schedule(static)
+        for (int64_t v = 0; v < V; ++v)
+            for (int64_t h = 0; h < H; ++h) {
+                double acc = 0.0;
+                for (int64_t r = 0; r < N; ++r)
+                    acc += dl[r * V + v] * oracle_decode(hidden, dtype, r * H + h);
+                grad_weight[v * H + h] = acc;
+            }
+    }
+    free(dl);
+    return 0;
+}
+
 /* Number of OpenMP threads the oracle runs on (1 when built without OpenMP). */
 int oracle_num_threads(void) {
 #ifdef _OPENMP

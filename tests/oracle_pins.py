@@ -412,4 +412,45 @@ def pin_class_weights_closed_forms(lib):
     assert np.allclose(a1["grad"], a0["grad"], rtol=1e-13, atol=1e-17)
 
 
+# ---------------------------------------------------------------- lm_head + CE
+def pin_linear_ce_identity_weight_is_plain_ce(lib):
+    """weight = identity (V = H): the logits are the hidden states themselves."""
+    rng = np.random.default_rng(24)
+    N, V = 7, 48
+    h = (rng.standard_normal((N, V)) * 2).astype(np.float32)
+    W = np.eye(V, dtype=np.float32)
+    t = rng.integers(0, V, N)
+    t[3] = -100
+    for a, red in ((0.0, False), (0.2, True)):
+        lin = oracle.linear_ce(h, W, F32, N, V, V, t, label_smoothing=a, reduce_loss=red, lib=lib)
+        ce = _ce(lib, h, t, a=a, reduce=red)
+        assert np.array_equal(lin["loss"], ce["loss"])
+        g32 = oracle.round_to(ce["grad"], F32, lib=lib)
+        assert np.array_equal(lin["grad_hidden"], g32)
+        assert np.array_equal(lin["grad_weight"], g32.T @ h.astype(np.float64))
+
+
+def pin_linear_ce_torch_float64(lib):
+    """The same dataflow in torch float64: logits and the logits gradient
+    rounded to float32 where the pass holds float32 tensors."""
+    rng = np.random.default_rng(25)
+    N, H, V = 9, 24, 61
+    h = rng.standard_normal((N, H)).astype(np.float32)
+    W = (rng.standard_normal((V, H)) * 0.5).astype(np.float32)
+    t = rng.integers(0, V, N)
+    t[0] = -100
+    for a in (0.0, 0.1):
+        h64, W64 = torch.tensor(h, dtype=torch.float64), torch.tensor(W, dtype=torch.float64)
+        logits = (h64 @ W64.T).to(torch.float32).to(torch.float64).requires_grad_(True)
+        loss = torch.nn.functional.cross_entropy(logits, torch.tensor(t), reduction="mean",
+                                                 label_smoothing=a, ignore_index=-100)
+        loss.backward(torch.tensor(1.3, dtype=torch.float64))
+        dl = logits.grad.to(torch.float32).to(torch.float64)
+        r = oracle.linear_ce(h, W, F32, N, H, V, t, label_smoothing=a, reduce_loss=True,
+                             dloss=np.array([1.3]), lib=lib)
+        assert abs(r["loss"][0] - loss.item()) <= 1e-12 * abs(loss.item())
+        assert np.allclose(r["grad_hidden"], (dl @ W64).numpy(), rtol=1e-11, atol=1e-15)
+        assert np.allclose(r["grad_weight"], (dl.T @ h64).numpy(), rtol=1e-11, atol=1e-15)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

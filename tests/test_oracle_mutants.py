@@ -35,6 +35,10 @@ MUTANTS = {
     "fp16_subnormal_decode": ("v = ldexp((double)f, -24);", "v = ldexp((double)f, -25);"),
     "weighted_target_weight_dropped": ("*loss = (1.0 - a) * w[y] * (lse - x[y])",
                                        "*loss = (1.0 - a) * (lse - x[y])"),
+    "linear_grad_weight_wrong_column": ("acc += dl[r * V + v] * oracle_decode(hidden, dtype, r * H + h);",
+                                        "acc += dl[r * V + v] * oracle_decode(hidden, dtype, r * H + (H - 1 - h));"),
+    "linear_logits_unrounded_grad": ("for (int64_t i = 0; i < N * V; ++i) dl[i] = oracle_round(dl[i], dtype);",
+                                     "for (int64_t i = 0; i < N * V; ++i) dl[i] = dl[i] * 1.0000001;"),
     "weighted_mean_over_count": ("const double denom = class_weights ? wsum : (double)n;",
                                  "const double denom = (double)n;"),
 }
