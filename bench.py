@@ -289,6 +289,25 @@ def run_ours(args, w, rank: int, world: int, dist) -> None:
             pkg.ce_fwd_bwd(x, t, label_smoothing=w.label_smoothing, ignore_idx=w.ignore_idx,
                            reduce_loss=w.reduce_loss, loss_out=loss, workspace=ws,
                            class_weights=cw)
+    elif mode == "linear":
+        # lm_head (hidden . W^T) + cross-entropy + both gradients, chunked over rows
+        del x
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(w.seed)
+        hid = (torch.randn(w.N, args.hidden, device=dev, generator=gen)).to(torch.bfloat16)
+        wmat = (torch.randn(w.V, args.hidden, device=dev, generator=gen)
+                / args.hidden ** 0.5 * 2).to(torch.bfloat16)
+        gh = torch.empty_like(hid)
+        gw = torch.zeros(w.V, args.hidden, dtype=torch.float32, device=dev)
+        lws = torch.empty(pkg._lib.load().ce_linear_workspace_bytes(
+            w.N, args.hidden, w.V, 1, args.chunk_rows), dtype=torch.uint8, device=dev)
+        t1 = t.reshape(-1)
+
+        def step(o=opts):
+            pkg.ce_linear_fwd_bwd(hid, wmat, t1, label_smoothing=w.label_smoothing,
+                                  ignore_idx=w.ignore_idx, reduce_loss=w.reduce_loss,
+                                  grad_hidden=gh, grad_weight=gw, chunk_rows=args.chunk_rows,
+                                  loss_out=loss, workspace=lws)
     elif mode == "split":
         # forward only (saves lse and the kept-row count), then the backward
         lse = torch.empty(w.N, dtype=torch.float32, device=dev)
@@ -371,6 +390,27 @@ def run_ours(args, w, rank: int, world: int, dist) -> None:
 
     ms, tok_s = aggregate(total_ms, w.N * args.steps, world, allmax)
 
+    if mode == "linear":
+        # tensor-bound: three GEMMs of 2 N V H flops each per step
+        if rank == 0:
+            flops = 6.0 * w.N * w.V * args.hidden
+            with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+                pk = json.load(f)
+            peak = float(pk.get("bf16_tflops_sustained", pk.get("bf16_tflops", 1700.0)))
+            ach = flops / (ms / args.steps / 1e3) / 1e12
+            line = {"metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": world,
+                    "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+                    "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                    "dtype": "bf16", "data": "synthetic",
+                    "config": config_of(w, args) | {"mode": "linear", "hidden": args.hidden,
+                                                     "chunk_rows": args.chunk_rows},
+                    "roofline": {"bound": "tensor", "kernel": "whole step (3 GEMMs + CE)",
+                                 "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                                 "frac": ach / peak, "traffic": None,
+                                 "peak_source": "measured bf16_tflops_sustained"},
+                    "clocks": clocks}
+            print(json.dumps(line), flush=True)
+        return
     if mode != "fused":
         # one line for a secondary mode: whole-step bytes over whole-step time
         if rank == 0:
@@ -464,8 +504,11 @@ def main(argv=None) -> int:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     # secondary passes: "split" = ce_fwd_only + ce_bwd (autograd order), "vp" = the
     # vocabulary-parallel steps over --vocab-shards shards on one GPU, "weighted" =
-    # the class-weighted pass
-    ap.add_argument("--mode", choices=["fused", "split", "vp", "weighted"], default="fused")
+    # the class-weighted pass, "linear" = lm_head + cross-entropy chunked over rows
+    ap.add_argument("--mode", choices=["fused", "split", "vp", "weighted", "linear"],
+                    default="fused")
+    ap.add_argument("--hidden", type=int, default=4096)      # linear mode: H
+    ap.add_argument("--chunk-rows", type=int, default=4096)  # linear mode: rows per chunk
     ap.add_argument("--vocab-shards", type=int, default=8)
     # planner overrides, for tuning sweeps (defaults: the planner's choice)
     ap.add_argument("--force-path", type=int, default=0)

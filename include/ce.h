@@ -244,6 +244,34 @@ ce_status ce_vp_bwd(const void* shard_logits, ce_dtype dtype, int64_t dim0, int6
                     const float* dloss, const int64_t* n_non_ignore, void* grad,
                     const int64_t grad_strides[3], void* stream);
 
+/* lm_head + cross-entropy, chunked over token rows (the sequence-chunked
+ * lm_head + loss of the TorchTitan ChunkedLossWrapper that hyper-parallel
+ * #269 describes: the full (N, V) logits never exist).  For each chunk of
+ * chunk_rows rows: logits = hidden . weight^T (a cuBLAS GEMM into the
+ * workspace), the cross-entropy pass of this library on them (gradient in
+ * place, scaled with the kept-row count of the whole batch), then
+ * grad_hidden = dlogits . weight and grad_weight += dlogits^T . hidden (cuBLAS
+ * GEMMs, fp32 accumulation).
+ *   hidden       (N, H) row-major, dtype; weight (V, H) row-major, dtype.
+ *   targets      int64 [N], contiguous.
+ *   loss_out     one value (reduce_loss) or N values.
+ *   grad_hidden  (N, H) row-major, dtype, written; or NULL.
+ *   grad_weight  (V, H) row-major float32, ACCUMULATED into (zero it first for
+ *                a fresh gradient); or NULL.
+ *   workspace    ce_linear_workspace_bytes(N, H, V, dtype, chunk_rows) bytes,
+ *                256-byte aligned; it holds one chunk of logits and cuBLAS's
+ *                workspace.  cuBLAS creates one handle per host thread and
+ *                device on first use (its own small allocation).
+ * Returns CE_OK once every kernel and GEMM is enqueued on `stream`. */
+size_t ce_linear_workspace_bytes(int64_t N, int64_t H, int64_t V, ce_dtype dtype,
+                                 int64_t chunk_rows);
+ce_status ce_linear_fwd_bwd(const void* hidden, const void* weight, ce_dtype dtype, int64_t N,
+                            int64_t H, int64_t V, const int64_t* targets, float label_smoothing,
+                            int64_t ignore_idx, int reduce_loss, const float* dloss,
+                            float* loss_out, void* grad_hidden, float* grad_weight,
+                            int64_t* n_non_ignore_out, int64_t chunk_rows, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
 /* ce_fwd_bwd without a workspace argument: the pass keeps its scratch in a
  * fixed 2 MiB array of device memory that the library itself reserves on
  * every GPU where it is loaded (held until the process exits).  The pages have

@@ -48,7 +48,7 @@ def _bind(lib):
                               c_dbl, c_i64, c_int, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]
     lib.oracle_linear_ce.restype = c_int
     lib.oracle_linear_ce.argtypes = [c_vp, c_vp, c_int, c_i64, c_i64, c_i64, c_vp, c_dbl, c_i64,
-                                     c_int, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]
+                                     c_int, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]
     lib.oracle_round.restype = c_dbl
     lib.oracle_round.argtypes = [c_dbl, c_int]
     lib.oracle_round_array.restype = None
@@ -135,14 +135,17 @@ def linear_ce(hidden: np.ndarray, weight: np.ndarray, dtype: int, N: int, H: int
     loss = np.zeros(1 if reduce_loss else N, dtype=np.float64)
     gh = np.zeros((N, H), dtype=np.float64) if want_grad else None
     gw = np.zeros((V, H), dtype=np.float64) if want_grad else None
+    dl = np.zeros((N, V), dtype=np.float64) if want_grad else None
     n = np.zeros(1, dtype=np.int64)
     err = np.zeros(1, dtype=np.uint32)
     rc = lib.oracle_linear_ce(_ptr(hidden), _ptr(weight), dtype, N, H, V, _ptr(targets),
                               float(label_smoothing), int(ignore_idx), int(bool(reduce_loss)),
-                              _ptr(dloss), _ptr(loss), _ptr(gh), _ptr(gw), _ptr(n), _ptr(err))
+                              _ptr(dloss), _ptr(loss), _ptr(gh), _ptr(gw), _ptr(dl), _ptr(n),
+                              _ptr(err))
     if rc != 0:
         raise MemoryError("oracle_linear_ce ran out of host memory")
-    return {"loss": loss, "grad_hidden": gh, "grad_weight": gw, "n": int(n[0]), "err": int(err[0])}
+    return {"loss": loss, "grad_hidden": gh, "grad_weight": gw, "dlogits": dl, "n": int(n[0]),
+            "err": int(err[0])}
 
 
 def round_to(values, dtype: int, lib=None) -> np.ndarray:

@@ -353,13 +353,14 @@ int oracle_ce(const void* logits, int dtype, int64_t dim0, int64_t dim1, int64_t
  *   grad_weight = dlogits^T . hidden             (double, not rounded)
  *   hidden [N][H], weight [V][H] row-major storage of `dtype`; targets [N].
  *   loss_out: N values or 1 (reduce); grad_hidden [N][H], grad_weight [V][H]
- *   doubles, either may be NULL.
+ *   doubles, either may be NULL; dlogits_out [N][V] (the rounded logits
+ *   gradient) or NULL.
  * Returns 0, or -1 when host memory runs out.
  * ------------------------------------------------------------------------- */
 int oracle_linear_ce(const void* hidden, const void* weight, int dtype, int64_t N, int64_t H,
                      int64_t V, const int64_t* targets, double a, int64_t ignore_idx, int reduce,
                      const double* dloss, double* loss_out, double* grad_hidden,
-                     double* grad_weight, int64_t* n_out, uint32_t* err_out) {
+                     double* grad_weight, double* dlogits_out, int64_t* n_out, uint32_t* err_out) {
     /* logits rounded to the storage dtype, stored as that dtype's bits so the
      * pass below reads them exactly as a GPU tensor of that dtype */
     const size_t es = dtype == ORACLE_F32 ? 4 : 2;
@@ -394,6 +395,7 @@ int oracle_linear_ce(const void* hidden, const void* weight, int dtype, int64_t 
     }
 #pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < N * V; ++i) dl[i] = oracle_round(dl[i], dtype);
+    if (dlogits_out) memcpy(dlogits_out, dl, (size_t)N * (size_t)V * sizeof(double));
     if (grad_hidden) {
 #pragma omp parallel for schedule(static)
         for (int64_t r = 0; r < N; ++r)

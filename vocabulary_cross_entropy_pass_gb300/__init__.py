@@ -29,7 +29,8 @@ from ._lib import (CE_PATH_AUTO, CE_PATH_CLUSTER, CE_PATH_ROW, CE_PATH_STREAM,
                    CE_PATH_TWO_STAGE, CE_PATH_WARP, CEError, ce_options, make_options)
 
 __all__ = ["ce_fwd_bwd", "ce_fwd_bwd_noalloc", "ce_fwd_only", "ce_bwd", "parallel_cross_entropy",
-           "ce_vp_partials", "ce_vp_combine", "ce_vp_bwd", "vocab_parallel_cross_entropy", "ce_workspace_bytes", "ce_get_error", "ce_status_string",
+           "ce_vp_partials", "ce_vp_combine", "ce_vp_bwd", "vocab_parallel_cross_entropy",
+           "ce_linear_fwd_bwd", "ce_workspace_bytes", "ce_get_error", "ce_status_string",
            "ce_plan_path", "CEError", "make_options", "ce_options",
            "CE_PATH_AUTO", "CE_PATH_ROW", "CE_PATH_CLUSTER", "CE_PATH_TWO_STAGE", "CE_PATH_STREAM", "CE_PATH_WARP"]
 
@@ -403,3 +404,61 @@ def vocab_parallel_cross_entropy(shards, targets: torch.Tensor, label_smoothing:
                        n_non_ignore=n, grad=sh if inplace_grad else None)
              for k, sh in enumerate(shards)]
     return loss, grads
+
+
+# ---------------------------------------------------------------- lm_head + cross-entropy
+def ce_linear_fwd_bwd(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor,
+                      label_smoothing: float = 0.0, ignore_idx: int = -100,
+                      reduce_loss: bool = False, dloss: torch.Tensor | None = None,
+                      grad_hidden: torch.Tensor | bool | None = True,
+                      grad_weight: torch.Tensor | bool | None = True, chunk_rows: int = 4096,
+                      loss_out: torch.Tensor | None = None,
+                      n_non_ignore_out: torch.Tensor | None = None,
+                      workspace: torch.Tensor | None = None, stream=None):
+    """lm_head (hidden (N, H) . weight (V, H)^T) + cross-entropy, chunk_rows
+    rows at a time: the (N, V) logits never exist.  ``grad_hidden``: a (N, H)
+    tensor of the input dtype to write, True to allocate one, None to skip;
+    ``grad_weight``: a float32 (V, H) tensor accumulated into, True to
+    allocate a zeroed one, None to skip.  Returns (loss, grad_hidden,
+    grad_weight)."""
+    if not (hidden.is_cuda and weight.is_cuda and targets.is_cuda):
+        raise ValueError("hidden, weight and targets must be CUDA tensors (there is no CPU path)")
+    if hidden.dtype not in _DTYPE or weight.dtype != hidden.dtype:
+        raise TypeError("hidden and weight must share a float32/bfloat16/float16 dtype")
+    if hidden.dim() != 2 or weight.dim() != 2 or hidden.shape[1] != weight.shape[1]:
+        raise ValueError("hidden (N, H) and weight (V, H) expected")
+    hidden = hidden.contiguous()
+    weight = weight.contiguous()
+    t = targets.reshape(-1).contiguous()
+    if t.dtype != torch.int64 or t.numel() != hidden.shape[0]:
+        raise ValueError("targets must be int64 with one entry per hidden row")
+    lib = _lib.load()
+    N, H = hidden.shape
+    V = weight.shape[0]
+    dev = hidden.device
+    if grad_hidden is True:
+        grad_hidden = torch.empty_like(hidden)
+    if grad_weight is True:
+        grad_weight = torch.zeros(V, H, dtype=torch.float32, device=dev)
+    if grad_weight is not None and grad_weight is not False and grad_weight.dtype != torch.float32:
+        raise TypeError("grad_weight accumulates in float32")
+    gh = grad_hidden if isinstance(grad_hidden, torch.Tensor) else None
+    gw = grad_weight if isinstance(grad_weight, torch.Tensor) else None
+    if loss_out is None:
+        loss_out = torch.empty(1 if reduce_loss else N, dtype=torch.float32, device=dev)
+    need = int(lib.ce_linear_workspace_bytes(N, H, V, _DTYPE[hidden.dtype], int(chunk_rows)))
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    rc = lib.ce_linear_fwd_bwd(
+        ctypes.c_void_p(hidden.data_ptr()), ctypes.c_void_p(weight.data_ptr()),
+        _DTYPE[hidden.dtype], N, H, V, ctypes.c_void_p(t.data_ptr()), float(label_smoothing),
+        int(ignore_idx), int(bool(reduce_loss)),
+        ctypes.c_void_p(dloss.data_ptr() if dloss is not None else None),
+        ctypes.c_void_p(loss_out.data_ptr()),
+        ctypes.c_void_p(gh.data_ptr() if gh is not None else None),
+        ctypes.c_void_p(gw.data_ptr() if gw is not None else None),
+        ctypes.c_void_p(n_non_ignore_out.data_ptr() if n_non_ignore_out is not None else None),
+        int(chunk_rows), ctypes.c_void_p(workspace.data_ptr()),
+        workspace.numel() * workspace.element_size(), _stream(dev, stream))
+    _raise(rc, "ce_linear_fwd_bwd")
+    return loss_out, gh, gw

@@ -35,7 +35,7 @@ STATUS = {
 # every function include/ce.h declares
 EXPORTS = ("ce_workspace_bytes", "ce_fwd_bwd", "ce_fwd_only", "ce_get_error", "ce_status_string",
            "ce_plan_path", "ce_fwd_bwd_noalloc", "ce_bwd", "ce_vp_partials", "ce_vp_combine",
-           "ce_vp_bwd")
+           "ce_vp_bwd", "ce_linear_workspace_bytes", "ce_linear_fwd_bwd")
 
 
 class ce_options(ctypes.Structure):
@@ -101,6 +101,11 @@ def load(path: str = LIB_PATH):
         lib.ce_vp_bwd.restype = i32
         lib.ce_vp_bwd.argtypes = [vp, i32, i64, i64, i64, I64_3, vp, I64_3, i64, i64, vp, f32, i64,
                                   i32, vp, vp, vp, I64_3, vp]
+        lib.ce_linear_workspace_bytes.restype = ctypes.c_size_t
+        lib.ce_linear_workspace_bytes.argtypes = [i64, i64, i64, i32, i64]
+        lib.ce_linear_fwd_bwd.restype = i32
+        lib.ce_linear_fwd_bwd.argtypes = [vp, vp, i32, i64, i64, i64, vp, f32, i64, i32, vp, vp, vp,
+                                          vp, vp, i64, vp, ctypes.c_size_t, vp]
         lib.ce_get_error.restype = i32
         lib.ce_get_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
         lib.ce_status_string.restype = ctypes.c_char_p

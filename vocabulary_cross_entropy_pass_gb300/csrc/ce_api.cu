@@ -206,6 +206,13 @@ ce_status check_common(const void* logits, int dtype, int layout, int64_t dim0, 
     return CE_OK;
 }
 
+cudaError_t launch_planned(const Problem& pb, const Plan& pl, float4* parts, cudaStream_t s) {
+    if (pl.path == CE_PATH_TWO_STAGE) return launch_split(pb, pl.split, parts, s);
+    if (pl.path == CE_PATH_STREAM) return launch_stream(pb, pl.stream, s);
+    if (pl.path == CE_PATH_WARP) return launch_rows(pb, pl.rows, s);
+    return launch_fused(pb, pl.fused, s);
+}
+
 ce_status run_pass(Problem& pb, const ce_options* o, float* loss_out, int64_t* n_out,
                    void* ws, cudaStream_t s) {
     Plan pl = make_plan(pb, o);
@@ -230,18 +237,7 @@ ce_status run_pass(Problem& pb, const ce_options* o, float* loss_out, int64_t* n
     cudaEvent_t eb = o ? static_cast<cudaEvent_t>(o->event_begin) : nullptr;
     cudaEvent_t ee = o ? static_cast<cudaEvent_t>(o->event_end) : nullptr;
     if (eb && cudaEventRecord(eb, s) != cudaSuccess) return CE_ERR_LAUNCH;
-    if (pb.N > 0) {
-        cudaError_t e;
-        if (pl.path == CE_PATH_TWO_STAGE)
-            e = launch_split(pb, pl.split, parts, s);
-        else if (pl.path == CE_PATH_STREAM)
-            e = launch_stream(pb, pl.stream, s);
-        else if (pl.path == CE_PATH_WARP)
-            e = launch_rows(pb, pl.rows, s);
-        else
-            e = launch_fused(pb, pl.fused, s);
-        if (e != cudaSuccess) return CE_ERR_LAUNCH;
-    }
+    if (pb.N > 0 && launch_planned(pb, pl, parts, s) != cudaSuccess) return CE_ERR_LAUNCH;
     if (ee && cudaEventRecord(ee, s) != cudaSuccess) return CE_ERR_LAUNCH;
     if (pb.reduce && !mean_in_kernel && launch_reduce_mean(pb, loss_out, s) != cudaSuccess)
         return CE_ERR_LAUNCH;
@@ -340,6 +336,33 @@ ce_status bwd_common(const void* logits, int dtype, int64_t dim0, int64_t dim1, 
 }
 
 }  // namespace
+
+// The main kernel(s) of one pass, planned as ce_fwd_bwd would, for a caller
+// that has already run the count kernel (pb.n_dev, pb.err set) and wants the
+// per-row losses in pb.loss_rows (no in-kernel mean).  `partials` holds the
+// two-stage partials when that path is planned.
+cudaError_t launch_main_pass(Problem& pb, const ce_options* o, float4* partials, size_t partial_bytes,
+                             cudaStream_t s) {
+    Plan pl = make_plan(pb, o);
+    if (pl.path < 0) return cudaErrorInvalidValue;
+    if (pl.path == CE_PATH_TWO_STAGE &&
+        (size_t)pb.N * (size_t)pl.split.chunks * sizeof(float4) > partial_bytes)
+        return cudaErrorInvalidValue;
+    pb.mean_out = nullptr;
+    if (pb.N == 0) return cudaSuccess;
+    return launch_planned(pb, pl, partials, s);
+}
+
+size_t partial_bytes_for(int64_t N, int64_t V) {
+    return align_up((size_t)N * (size_t)split_chunks(V, nullptr) * sizeof(float4), 256);
+}
+
+void problem_init(Problem& pb, const void* logits, int dtype, int64_t dim0, int64_t dim1, int64_t V,
+                  const int64_t* strides, const int64_t* targets, const int64_t* tstrides, float a,
+                  int64_t ignore_idx, int reduce) {
+    fill_problem(pb, logits, dtype, dim0, dim1, V, strides, targets, tstrides, a, ignore_idx, reduce);
+}
+
 }  // namespace gbce
 
 using namespace gbce;

@@ -142,4 +142,12 @@ cudaError_t launch_vp_combine(const VpCombineProblem& vc, cudaStream_t s);
 cudaError_t launch_split(const Problem& p, const SplitPlan& plan, float4* partials,
                          cudaStream_t s);
 
+// Used by the lm_head + cross-entropy orchestration (ce_linear.cu).
+cudaError_t launch_main_pass(Problem& pb, const ce_options* o, float4* partials, size_t partial_bytes,
+                             cudaStream_t s);
+size_t partial_bytes_for(int64_t N, int64_t V);
+void problem_init(Problem& pb, const void* logits, int dtype, int64_t dim0, int64_t dim1, int64_t V,
+                  const int64_t* strides, const int64_t* targets, const int64_t* tstrides, float a,
+                  int64_t ignore_idx, int reduce);
+
 }  // namespace gbce

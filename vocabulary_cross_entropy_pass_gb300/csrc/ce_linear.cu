@@ -1,0 +1,162 @@
+// ce_linear.cu -- lm_head + cross-entropy, chunked over token rows.
+//
+// hyper-parallel #269 (background, and its TorchTitan comparison) describes
+// the ChunkedLossWrapper: the lm_head projection and the cross-entropy run a
+// chunk of the sequence at a time so that the full (B*L, V) logits never
+// exist, bounding their O(B*L*V) peak memory.  Here, for each chunk of rows:
+//
+//   1. logits_c = hidden_c . weight^T       cuBLAS GEMM (tensor cores), into a
+//                                           chunk buffer of the workspace;
+//   2. the cross-entropy pass of this library on that buffer (loss per row,
+//      gradient written in place over the chunk's logits), scaled with the
+//      kept-row count of the whole batch (counted once, up front);
+//   3. grad_hidden_c = dlogits_c . weight    cuBLAS GEMM;
+//      grad_weight  += dlogits_c^T . hidden_c cuBLAS GEMM, float32 accumulation.
+//
+// The three products are plain library GEMMs; the pass between them is this
+// library's kernels.  At a hidden size in the thousands the GEMMs dominate
+// (about 6*H flops per logit against a few bytes of logits traffic), so the
+// chunk buffer's round trip through memory costs little.
+#include <cublas_v2.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "ce_internal.h"
+
+namespace gbce {
+namespace {
+
+constexpr size_t kCublasWorkspaceBytes = (size_t)32 << 20;
+constexpr int kLinMaxDevices = 64;
+
+// One cuBLAS handle per host thread and device (handles are not shared
+// between threads that may run at the same time).
+cublasHandle_t thread_handle(int dev) {
+    thread_local cublasHandle_t handles[kLinMaxDevices] = {};
+    if (dev < 0 || dev >= kLinMaxDevices) return nullptr;
+    if (!handles[dev] && cublasCreate(&handles[dev]) != CUBLAS_STATUS_SUCCESS) handles[dev] = nullptr;
+    return handles[dev];
+}
+
+cudaDataType_t cuda_type(int dtype) {
+    return dtype == CE_F32 ? CUDA_R_32F : (dtype == CE_BF16 ? CUDA_R_16BF : CUDA_R_16F);
+}
+
+struct LinLayout {
+    size_t rows_off, chunk_off, part_off, cublas_off, total;
+};
+
+LinLayout lin_layout(int64_t N, int64_t V, int es, int64_t chunk_rows) {
+    LinLayout L;
+    L.rows_off = kWsHeaderBytes;
+    L.chunk_off = L.rows_off + align_up((size_t)N * sizeof(float), 256);
+    L.part_off = L.chunk_off + align_up((size_t)chunk_rows * (size_t)V * es, 256);
+    L.cublas_off = L.part_off + partial_bytes_for(chunk_rows, V);
+    L.total = L.cublas_off + kCublasWorkspaceBytes;
+    return L;
+}
+
+}  // namespace
+}  // namespace gbce
+
+using namespace gbce;
+
+extern "C" {
+
+size_t ce_linear_workspace_bytes(int64_t N, int64_t H, int64_t V, ce_dtype dtype,
+                                 int64_t chunk_rows) {
+    if (N < 0 || H < 1 || V < 1 || chunk_rows < 1 || (int)dtype < CE_F32 || (int)dtype > CE_F16)
+        return 0;
+    return lin_layout(N, V, elem_size(dtype), chunk_rows).total;
+}
+
+ce_status ce_linear_fwd_bwd(const void* hidden, const void* weight, ce_dtype dtype, int64_t N,
+                            int64_t H, int64_t V, const int64_t* targets, float label_smoothing,
+                            int64_t ignore_idx, int reduce_loss, const float* dloss,
+                            float* loss_out, void* grad_hidden, float* grad_weight,
+                            int64_t* n_non_ignore_out, int64_t chunk_rows, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+    if ((int)dtype < CE_F32 || (int)dtype > CE_F16) return CE_ERR_UNSUPPORTED_DTYPE;
+    if (N < 0 || H < 1 || V < 1 || V > 0x7fffffffLL || H > 0x7fffffffLL || chunk_rows < 1)
+        return CE_ERR_INVALID_ARG;
+    if (!(label_smoothing >= 0.f && label_smoothing <= 1.f)) return CE_ERR_INVALID_ARG;
+    if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256) return CE_ERR_INVALID_ARG;
+    if (N > 0 && (!hidden || !weight || !targets || !loss_out)) return CE_ERR_INVALID_ARG;
+    if (N == 0 && reduce_loss && !loss_out) return CE_ERR_INVALID_ARG;
+    const int es = elem_size(dtype);
+    if (chunk_rows > N && N > 0) chunk_rows = N;
+    const LinLayout L = lin_layout(N, V, es, chunk_rows);
+    if (workspace_bytes < L.total) return CE_ERR_WORKSPACE_TOO_SMALL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* w = static_cast<char*>(workspace);
+
+    // kept-row count and range check over the whole batch
+    static const int64_t no_strides[3] = {0, 0, 1};
+    const int64_t t_strides[2] = {N, 1};
+    Problem all;
+    problem_init(all, hidden, dtype, 1, N, V, no_strides, targets, t_strides, label_smoothing,
+                 ignore_idx, reduce_loss);
+    all.err = reinterpret_cast<uint32_t*>(w + kWsErrOffset);
+    all.n_dev = reinterpret_cast<int64_t*>(w + kWsCountOffset);
+    all.ticket = reinterpret_cast<uint32_t*>(w + kWsTicketOffset);
+    all.loss_rows = reduce_loss ? reinterpret_cast<float*>(w + L.rows_off) : loss_out;
+    if (launch_count(all, n_non_ignore_out, s) != cudaSuccess) return CE_ERR_LAUNCH;
+    if (N == 0) {
+        if (reduce_loss && launch_reduce_mean(all, loss_out, s) != cudaSuccess) return CE_ERR_LAUNCH;
+        return CE_OK;
+    }
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CE_ERR_LAUNCH;
+    cublasHandle_t h = thread_handle(dev);
+    if (!h) return CE_ERR_LAUNCH;
+    if (cublasSetStream(h, s) != CUBLAS_STATUS_SUCCESS) return CE_ERR_LAUNCH;
+    if (cublasSetWorkspace(h, w + L.cublas_off, kCublasWorkspaceBytes) != CUBLAS_STATUS_SUCCESS)
+        return CE_ERR_LAUNCH;
+    const cudaDataType_t ty = cuda_type(dtype);
+    const float one = 1.f, zero = 0.f;
+    char* chunk = w + L.chunk_off;
+    const char* hid = static_cast<const char*>(hidden);
+
+    for (int64_t r0 = 0; r0 < N; r0 += chunk_rows) {
+        const int64_t rows = (N - r0 < chunk_rows) ? N - r0 : chunk_rows;
+        // 1. logits of the chunk, row-major (rows, V): column-major C[V, rows] = W^T-op . h
+        if (cublasGemmEx(h, CUBLAS_OP_T, CUBLAS_OP_N, (int)V, (int)rows, (int)H, &one, weight, ty,
+                         (int)H, hid + (size_t)r0 * H * es, ty, (int)H, &zero, chunk, ty, (int)V,
+                         CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
+            return CE_ERR_LAUNCH;
+        // 2. the cross-entropy pass over the chunk, gradient in place
+        const int64_t c_strides[3] = {rows * V, V, 1};
+        const int64_t ct_strides[2] = {rows, 1};
+        Problem pb;
+        problem_init(pb, chunk, dtype, 1, rows, V, c_strides, targets + r0, ct_strides,
+                     label_smoothing, ignore_idx, reduce_loss);
+        pb.err = all.err;
+        pb.n_dev = all.n_dev;
+        pb.ticket = all.ticket;
+        pb.dloss = reduce_loss ? dloss : (dloss ? dloss + r0 : nullptr);
+        pb.loss_rows = all.loss_rows + r0;
+        pb.grad = grad_hidden != nullptr || grad_weight != nullptr;
+        if (launch_main_pass(pb, nullptr, reinterpret_cast<float4*>(w + L.part_off),
+                             L.cublas_off - L.part_off, s) != cudaSuccess)
+            return CE_ERR_LAUNCH;
+        // 3. gradients through the projection
+        if (grad_hidden &&
+            cublasGemmEx(h, CUBLAS_OP_N, CUBLAS_OP_N, (int)H, (int)rows, (int)V, &one, weight, ty,
+                         (int)H, chunk, ty, (int)V, &zero,
+                         static_cast<char*>(grad_hidden) + (size_t)r0 * H * es, ty, (int)H,
+                         CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
+            return CE_ERR_LAUNCH;
+        if (grad_weight &&
+            cublasGemmEx(h, CUBLAS_OP_N, CUBLAS_OP_T, (int)H, (int)V, (int)rows, &one,
+                         hid + (size_t)r0 * H * es, ty, (int)H, chunk, ty, (int)V, &one, grad_weight,
+                         CUDA_R_32F, (int)H, CUBLAS_COMPUTE_32F,
+                         CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
+            return CE_ERR_LAUNCH;
+    }
+    if (reduce_loss && launch_reduce_mean(all, loss_out, s) != cudaSuccess) return CE_ERR_LAUNCH;
+    return CE_OK;
+}
+
+}  // extern "C"
