@@ -101,41 +101,58 @@ ce_rows_kernel(const __grid_constant__ RowsArgs p) {
     const int tpw = p.stages / NW;  // tiles per consumer warp
 
     // ------------------------------------------------------------ producer warp
+    // Rows are examined 32 at a time, one per lane; a ballot gives the kept
+    // ones, which lane 0 copies in order, and the warp zero-fills the others.
     if (warp == NW) {
         const uint64_t pol = l2_evict_first();
         uint32_t k = 0;         // kept rows seen
         uint32_t k_issued = 0;  // kept rows whose copy was issued (a prefix of them)
-        for (int64_t r = blockIdx.x; r < p.N; r += gridDim.x) {
-            const int64_t y = row_target(r);
-            char* row = row_ptr(r);
-            if (!is_loaded(y)) {
-                // ignored (loss 0) or out of range (loss NaN): zero gradient, no read
+        for (int64_t q0 = 0;; q0 += 32) {
+            const int64_t r = (int64_t)blockIdx.x + (q0 + lane) * (int64_t)gridDim.x;
+            const bool valid = r < p.N;
+            const int64_t y = valid ? row_target(r) : p.ignore_idx;
+            const bool kept = valid && is_loaded(y);
+            const unsigned vmask = __ballot_sync(kFull, valid);
+            if (vmask == 0u) break;
+            unsigned kmask = __ballot_sync(kFull, kept);
+            unsigned zmask = vmask & ~kmask;
+            while (zmask) {  // ignored (loss 0) or out of range (loss NaN): zero gradient, no read
+                const int l = __ffs(zmask) - 1;
+                zmask &= zmask - 1;
+                const int64_t rl = __shfl_sync(kFull, r, l);
+                const int64_t yl = __shfl_sync(kFull, y, l);
+                char* row = row_ptr(rl);
                 if (GRAD) {
                     const uint4 z = make_uint4(0, 0, 0, 0);
                     for (int v = lane; v < nvec; v += 32) stg128_stream(row + (size_t)v * 16, z);
                 }
                 if (lane == 0) {
-                    p.loss[r] = (y == p.ignore_idx) ? 0.f : __int_as_float(0x7fc00000);
-                    if (p.lse_out) p.lse_out[r] = __int_as_float(0x7fc00000);
-                }
-                continue;
-            }
-            if (lane == 0 && !flags[0]) {
-                // kept row k goes to warp k % NW, whose j-th row uses its tile j % TPW
-                const uint32_t j = k / NW;
-                const int tile = (int)(k % NW) * tpw + (int)(j % (uint32_t)tpw);
-                const uint32_t ph = (j / (uint32_t)tpw) & 1u;
-                if (!mbar_wait_bounded(&empty[tile], ph ^ 1u)) {
-                    griddep_wait();  // the count kernel starts the error word
-                    atomicOr(p.err, CE_DEVERR_TIMEOUT);
-                    flags[0] = 1;
-                } else {
-                    mbar_arrive_expect_tx(&full[tile], p.row_bytes);
-                    tma_load_1d(ring + (size_t)tile * TB, row, p.row_bytes, &full[tile], pol);
-                    k_issued = k + 1;
+                    p.loss[rl] = (yl == p.ignore_idx) ? 0.f : __int_as_float(0x7fc00000);
+                    if (p.lse_out) p.lse_out[rl] = __int_as_float(0x7fc00000);
                 }
             }
-            ++k;
+            while (kmask) {
+                const int l = __ffs(kmask) - 1;
+                kmask &= kmask - 1;
+                const int64_t rl = __shfl_sync(kFull, r, l);
+                if (lane == 0 && !flags[0]) {
+                    // kept row k goes to warp k % NW, whose j-th row uses its tile j % TPW
+                    const uint32_t j = k / NW;
+                    const int tile = (int)(k % NW) * tpw + (int)(j % (uint32_t)tpw);
+                    const uint32_t ph = (j / (uint32_t)tpw) & 1u;
+                    if (!mbar_wait_bounded(&empty[tile], ph ^ 1u)) {
+                        griddep_wait();  // the count kernel starts the error word
+                        atomicOr(p.err, CE_DEVERR_TIMEOUT);
+                        flags[0] = 1;
+                    } else {
+                        mbar_arrive_expect_tx(&full[tile], p.row_bytes);
+                        tma_load_1d(ring + (size_t)tile * TB, row_ptr(rl), p.row_bytes, &full[tile],
+                                    pol);
+                        k_issued = k + 1;
+                    }
+                }
+                ++k;
+            }
         }
         __syncwarp();
         if (lane == 0 && flags[0]) {
@@ -167,11 +184,21 @@ ce_rows_kernel(const __grid_constant__ RowsArgs p) {
     if (p.reduce) g_reduce = (p.dloss ? __ldg(p.dloss) : 1.f) / (float)(*p.n_dev);
     uint32_t k = 0;  // kept rows seen by the whole CTA
     const float2 L2 = make_float2(kLog2e, kLog2e);
-    for (int64_t r = blockIdx.x; r < p.N; r += gridDim.x) {
-        const int64_t y = row_target(r);
-        if (!is_loaded(y)) continue;
+    for (int64_t q0 = 0;; q0 += 32) {
+      // 32 rows at a time, one per lane; this warp takes kept rows k = warp (mod NW)
+      const int64_t rq = (int64_t)blockIdx.x + (q0 + lane) * (int64_t)gridDim.x;
+      const bool valid = rq < p.N;
+      const int64_t yq = valid ? row_target(rq) : p.ignore_idx;
+      const unsigned vmask = __ballot_sync(kFull, valid);
+      if (vmask == 0u) break;
+      unsigned kmask = __ballot_sync(kFull, valid && is_loaded(yq));
+      while (kmask) {
+        const int l = __ffs(kmask) - 1;
+        kmask &= kmask - 1;
         const uint32_t mine = k++;
         if ((int)(mine % (uint32_t)NW) != warp) continue;
+        const int64_t r = __shfl_sync(kFull, rq, l);
+        const int64_t y = __shfl_sync(kFull, yq, l);
         const uint32_t j = mine / NW;  // this warp's j-th kept row
         const int s = warp * tpw + (int)(j % (uint32_t)tpw);
         const uint32_t ph = (j / (uint32_t)tpw) & 1u;
@@ -240,6 +267,7 @@ ce_rows_kernel(const __grid_constant__ RowsArgs p) {
         }
         __syncwarp();
         if (lane == 0) mbar_arrive_rows(&empty[s]);
+      }
     }
 
     // reduce_loss: the last CTA to finish sums the per-row losses in a fixed order
