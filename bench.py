@@ -265,7 +265,8 @@ def run_ours(args, w, rank: int, world: int, dist) -> None:
     t_host = wl.targets(w).pin_memory()
     x = x_host.to(dev, non_blocking=True)
     t = t_host.to(dev, non_blocking=True)
-    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    # one mean, or one loss per row
+    loss = torch.empty(1 if w.reduce_loss else w.N, dtype=torch.float32, device=dev)
     tune = dict(force_path=args.force_path, num_vocab_chunks=args.chunks,
                 tune_threads=args.tune_threads, tune_stages=args.tune_stages,
                 tune_ctas_per_sm=args.tune_ctas_per_sm, tune_l2_keep=args.tune_l2_keep,
@@ -445,7 +446,7 @@ def run_ours(args, w, rank: int, world: int, dist) -> None:
     copy_stream = torch.cuda.Stream(dev)
     copied = [torch.cuda.Event() for _ in range(2)]
     done = [torch.cuda.Event() for _ in range(2)]
-    loss_host = torch.empty(max(e2e_steps, 2), dtype=torch.float32, pin_memory=True)
+    loss_host = torch.empty(max(e2e_steps, 2), loss.numel(), dtype=torch.float32, pin_memory=True)
 
     def e2e_round(k):
         b = k % 2
@@ -458,7 +459,7 @@ def run_ours(args, w, rank: int, world: int, dist) -> None:
         pkg.ce_fwd_bwd(xs[b], ts_[b], label_smoothing=w.label_smoothing, ignore_idx=w.ignore_idx,
                        reduce_loss=w.reduce_loss, loss_out=loss, workspace=ws, opts=opts,
                        stream=stream)
-        loss_host[k:k + 1].copy_(loss, non_blocking=True)
+        loss_host[k].copy_(loss, non_blocking=True)
         done[b].record(stream)
 
     # warm-up: the first write into a freshly allocated device buffer and the
@@ -511,7 +512,7 @@ def run_ours(args, w, rank: int, world: int, dist) -> None:
                      "algorithmic_bytes": nbytes},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_tok_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": 4, "steps": e2e_steps,
+                "d2h_bytes_per_step": 4 * loss.numel(), "steps": e2e_steps,
                 "ms_per_step": e2e_ms / e2e_steps,
                 "how": "ce_fwd_bwd per step on inputs copied from pinned host memory "
                        "(two device buffers: the copy of step k+1 overlaps the pass of "
