@@ -121,7 +121,12 @@ typedef struct {
                                torch F.cross_entropy(weight=...): the smoothed target's
                                class j term is weighted by w_j and the mean divides by
                                the summed weight of the kept rows' targets.  Runs on the
-                               two-stage path (ce_fwd_bwd, ce_fwd_only; not ce_bwd) */
+                               stream path when the rows and this vector are 16-byte
+                               aligned and no vocabulary split is asked for (256
+                               consuming threads), else on the two-stage path;
+                               CE_PATH_ROW, CE_PATH_CLUSTER and CE_PATH_WARP are refused
+                               with CE_ERR_UNSUPPORTED_PATH (ce_fwd_bwd, ce_fwd_only;
+                               not ce_bwd) */
     int reserved[2];        /* must be zero */
 } ce_options;
 

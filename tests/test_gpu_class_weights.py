@@ -13,9 +13,18 @@ pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda")
 
 
+# (force_path, tile_kb, weight offset in floats): the planner's choice (the
+# stream kernel when rows and weights are 16-byte aligned), its 16 KB-tile
+# shape, the two-stage kernels forced, and weights 4 bytes off alignment
+# (the planner falls back to the two-stage kernels)
+ROUTES = [(0, 0, 0), (0, 16, 0), (3, 0, 0), (0, 0, 1)]
+
+
+@pytest.mark.parametrize("route", ROUTES, ids=["auto", "tile16", "two_stage", "unaligned_w"])
 @pytest.mark.parametrize("name", ["c1_bsv4096_f32", "c2_sbv8192_bf16", "c3h_bsv32000_f16_spiked",
                                   "c5_bsv128000_bf16_ls"])
-def test_class_weighted_pass(name):
+def test_class_weighted_pass(name, route):
+    force, tile_kb, woff = route
     w = wl.WORKLOADS[name]
     rng = np.random.default_rng(31)
     cw = rng.uniform(0.1, 3.0, w.V).astype(np.float32)
@@ -28,11 +37,16 @@ def test_class_weighted_pass(name):
                     reduce_loss=w.reduce_loss, dloss=dl.astype(np.float64),
                     class_weights=cw.astype(np.float64))
     xd, td = x.to(DEV), t.to(DEV)
-    cwd = torch.tensor(cw, device=DEV)
+    cwd = torch.zeros(w.V + woff, device=DEV)[woff:]
+    cwd.copy_(torch.tensor(cw))
+    opts = pkg.make_options(force_path=force, tune_tile_kb=tile_kb)
+    want = 3 if (force == 3 or woff) else 4
+    assert pkg.ce_plan_path(xd, opts=pkg.make_options(
+        force_path=force, tune_tile_kb=tile_kb, class_weights=cwd.data_ptr()))[0] == want
     n = torch.zeros(1, dtype=torch.int64, device=DEV)
     loss = pkg.ce_fwd_bwd(xd, td, label_smoothing=w.label_smoothing, reduce_loss=w.reduce_loss,
                           dloss=torch.tensor(dl, dtype=torch.float32, device=DEV),
-                          layout=w.layout, n_non_ignore_out=n, class_weights=cwd)
+                          layout=w.layout, n_non_ignore_out=n, class_weights=cwd, opts=opts)
     assert int(n.item()) == ref["n"]
     harness.check_loss(loss.cpu().numpy(), ref["loss"], w.dtype, name)
     g = xd.float().cpu().numpy().reshape(w.N, w.V).astype(np.float64)
@@ -40,7 +54,8 @@ def test_class_weighted_pass(name):
     assert excess <= 0.0
     # forward only gives the same losses
     lf = pkg.ce_fwd_only(x.to(DEV), td, label_smoothing=w.label_smoothing,
-                         reduce_loss=w.reduce_loss, layout=w.layout, class_weights=cwd)
+                         reduce_loss=w.reduce_loss, layout=w.layout, class_weights=cwd,
+                         opts=pkg.make_options(force_path=force, tune_tile_kb=tile_kb))
     harness.check_loss(lf.cpu().numpy(), ref["loss"], w.dtype, name)
 
 
@@ -60,8 +75,17 @@ def test_unit_weights_equal_unweighted():
     assert excess <= 0.0
 
 
-def test_weights_refuse_other_paths():
+@pytest.mark.parametrize("force", [1, 2, 5])
+def test_weights_refuse_other_paths(force):
     x = torch.zeros(1, 4, 4096, dtype=torch.bfloat16, device=DEV)
     t = torch.zeros(1, 4, dtype=torch.int64, device=DEV)
     with pytest.raises(pkg.CEError):
-        pkg.ce_fwd_bwd(x, t, force_path=4, class_weights=torch.ones(4096, device=DEV))
+        pkg.ce_fwd_bwd(x, t, force_path=force, class_weights=torch.ones(4096, device=DEV))
+
+
+def test_weights_stream_refuses_512_threads():
+    x = torch.zeros(1, 4, 4096, dtype=torch.bfloat16, device=DEV)
+    t = torch.zeros(1, 4, dtype=torch.int64, device=DEV)
+    with pytest.raises(pkg.CEError):
+        pkg.ce_fwd_bwd(x, t, class_weights=torch.ones(4096, device=DEV),
+                       opts=pkg.make_options(force_path=4, tune_threads=512))

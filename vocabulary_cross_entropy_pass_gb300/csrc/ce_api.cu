@@ -123,7 +123,15 @@ Plan make_plan(const Problem& p, const ce_options* o) {
     const int force = o ? o->force_path : CE_PATH_AUTO;
     const bool aligned = fused_aligned(p) && p.V <= 0x7fffffffLL;
     if (o && o->class_weights) {
-        // the class-weighted pass runs on the two-stage kernels only
+        // the class-weighted pass: the stream kernel (256-thread shapes) when
+        // the rows and the weight vector are 16-byte aligned and no split is
+        // asked for, the two-stage kernels otherwise
+        const bool cw_aligned = reinterpret_cast<uintptr_t>(o->class_weights) % 16 == 0;
+        if ((force == CE_PATH_AUTO || force == CE_PATH_STREAM) && aligned && cw_aligned &&
+            o->num_vocab_chunks == 0 && plan_stream(o, &pl.stream) && pl.stream.threads == 256) {
+            pl.path = CE_PATH_STREAM;
+            return pl;
+        }
         if (force != CE_PATH_AUTO && force != CE_PATH_TWO_STAGE) {
             pl.path = -2;
             return pl;

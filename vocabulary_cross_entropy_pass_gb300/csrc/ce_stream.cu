@@ -18,6 +18,13 @@
 //     V) is rounded to the storage dtype and stored in place with 16-byte
 //     streaming stores (TENPU #29 section 6: in-place gradient staging).
 //
+// Class weights (torch F.cross_entropy(weight=...), the weighted NLL of
+// mindspore/hyper-parallel #269): the gradient is c * softmax - g (a/V) w_j
+// with c = g ((1-a) w_y + (a/V) W), so pass 1 is unchanged; pass 2 reads the
+// weights (16-byte loads, L2-resident) and also sums w_j x_j for the row's
+// loss, (1-a) w_y (lse - x_y) + (a/V) (W lse - sum_j w_j x_j), written after
+// pass 2.  The mean divides by the summed target weight of the kept rows.
+//
 // Warp specialisation: warps 0..NC/32-1 consume tiles; the last warp only
 // issues copies.  `full[s]` completes when tile s has landed (TMA transaction
 // count); `empty[s]` completes when every consumer warp is done with it.  Both
@@ -50,7 +57,24 @@ struct StreamArgs {
     int l2_keep;           // 1: pass-1 copies ask L2 to keep the row for pass 2
     uint32_t* ticket;      // CTAs done (zeroed by the count kernel)
     float* mean_out;       // reduce_loss: the last CTA to finish writes the mean here
+    const float* cw;       // class weights [V], 16-byte aligned (weighted pass) or NULL
+    const double* wdenom;  // summed weight of the kept rows' targets (count kernel)
+    const double* wsum;    // summed weight over the vocabulary (count kernel)
 };
+
+// The class weights of one 16-byte logits vector: VEC fp32 values, read as
+// 16-byte loads (the weight vector stays in L2: V x 4 bytes).
+template <typename T>
+__device__ __forceinline__ void load_weights(const float* cw, int64_t e0, float2 (&w)[Vec<T>::kElems / 2]) {
+    constexpr int VEC = Vec<T>::kElems;
+    const float4* src = reinterpret_cast<const float4*>(cw + e0);
+#pragma unroll
+    for (int k = 0; k < VEC / 4; ++k) {
+        const float4 f = __ldg(src + k);
+        w[2 * k] = make_float2(f.x, f.y);
+        w[2 * k + 1] = make_float2(f.z, f.w);
+    }
+}
 
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
@@ -81,10 +105,12 @@ struct Ring {
 };
 
 // Pass-1 work on one tile: running max, then p = 2^((x - m) log2e) summed,
-// and the plain sum, in packed f32x2 arithmetic.  FULL: every vector valid.
-template <typename T, int NC, int NV, bool FULL>
+// and the plain sum (WS: the class-weighted sum sum_j w_j x_j instead), in
+// packed f32x2 arithmetic.  FULL: every vector valid.  e0: the row element of
+// the tile's first vector (weights only).
+template <typename T, int NC, int NV, bool FULL, bool WS>
 __device__ __forceinline__ void stats_tile(const uint4* tile, int tid, int nvec, float& m,
-                                           float2& d2, float2& s2) {
+                                           float2& d2, float2& s2, const float* cw, int64_t e0) {
     using VT = Vec<T>;
     constexpr int P = VT::kElems / 2;  // float2 pairs per vector
     uint4 raw[NV];
@@ -111,23 +137,31 @@ __device__ __forceinline__ void stats_tile(const uint4* tile, int tid, int nvec,
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
         if (FULL || tid + i * NC < nvec) {
-            float2 x[P];
+            float2 x[P], w[P];
             VT::unpack2(raw[i], x);
+            if constexpr (WS) load_weights<T>(cw, e0 + (int64_t)(tid + i * NC) * VT::kElems, w);
 #pragma unroll
             for (int j = 0; j < P; ++j) {
                 const float2 a = __ffma2_rn(x[j], L2, NM);
                 d2 = __fadd2_rn(d2, make_float2(ex2_approx(a.x), ex2_approx(a.y)));
-                s2 = __fadd2_rn(s2, x[j]);
+                if constexpr (WS)
+                    s2 = __ffma2_rn(w[j], x[j], s2);
+                else
+                    s2 = __fadd2_rn(s2, x[j]);
             }
         }
     }
 }
 
-// Pass-2 work on one tile: g * 2^((x - lse) log2e) - g a/V, rounded to T and
-// stored over the logits.
-template <typename T, int NC, int NV, bool FULL>
+// Pass-2 work on one tile: c * 2^((x - lse) log2e) - b_j, rounded to T and
+// stored over the logits.  Unweighted: c = g, b_j = g a/V (NB = -b).
+// WT: c = g ((1-a) w_y + (a/V) W), b_j = g (a/V) w_j (NB = -g a/V), and the
+// class-weighted sum sum_j w_j x_j of the loss is accumulated into sw2 here,
+// so each weight is read once per row.
+template <typename T, int NC, int NV, bool FULL, bool WT>
 __device__ __forceinline__ void grad_tile(const uint4* tile, uint4* dst, int tid, int nvec,
-                                          float2 NL, float2 G2, float2 NB) {
+                                          float2 NL, float2 G2, float2 NB, const float* cw,
+                                          int64_t e0, float2& sw2) {
     using VT = Vec<T>;
     constexpr int P = VT::kElems / 2;
     const float2 L2 = make_float2(kLog2e, kLog2e);
@@ -138,19 +172,25 @@ __device__ __forceinline__ void grad_tile(const uint4* tile, uint4* dst, int tid
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
         if (FULL || tid + i * NC < nvec) {
-            float2 x[P], o[P];
+            float2 x[P], o[P], w[P];
             VT::unpack2(raw[i], x);
+            if constexpr (WT) load_weights<T>(cw, e0 + (int64_t)(tid + i * NC) * VT::kElems, w);
 #pragma unroll
             for (int j = 0; j < P; ++j) {
                 const float2 a = __ffma2_rn(x[j], L2, NL);
-                o[j] = __ffma2_rn(make_float2(ex2_approx(a.x), ex2_approx(a.y)), G2, NB);
+                float2 b = NB;
+                if constexpr (WT) {
+                    b = __fmul2_rn(w[j], NB);
+                    sw2 = __ffma2_rn(w[j], x[j], sw2);
+                }
+                o[j] = __ffma2_rn(make_float2(ex2_approx(a.x), ex2_approx(a.y)), G2, b);
             }
             stg128_stream(dst + tid + i * NC, VT::pack2(o));
         }
     }
 }
 
-template <typename T, int NC, int NV, bool GRAD>
+template <typename T, int NC, int NV, bool GRAD, bool WT>
 __global__ void __launch_bounds__(NC + 32, 1)
 ce_stream_kernel(const __grid_constant__ StreamArgs p) {
     using VT = Vec<T>;
@@ -166,7 +206,8 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
     uint64_t* empty = full + 12;
     float4* red = reinterpret_cast<float4*>(empty + 12);  // [2][NW]
     float* xy_s = reinterpret_cast<float*>(red + 2 * NW);  // [2]
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(xy_s + 2);
+    float* sw_s = xy_s + 2;                                 // [2][NW] weighted sums
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sw_s + 2 * NW);
     volatile int* last_flag = abort_flag + 1;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -239,8 +280,12 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
     // the count kernel before this one may still run: wait for n and the
     // error word (the producer's first copies are already in flight)
     griddep_wait();
+    // the mean divides by the number of kept rows, or (weighted) by their
+    // summed target weight
     float g_reduce = 1.f;
-    if (p.reduce) g_reduce = (p.dloss ? __ldg(p.dloss) : 1.f) / (float)(*p.n_dev);
+    if (p.reduce)
+        g_reduce = (p.dloss ? __ldg(p.dloss) : 1.f) / (WT ? (float)(*p.wdenom) : (float)(*p.n_dev));
+    const float wsum = WT ? (float)(*p.wsum) : 0.f;
     Ring rg(p.stages);
     int par = 0;
     auto wait_full = [&]() {
@@ -281,10 +326,12 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
             wait_full();
             const uint4* tile = reinterpret_cast<const uint4*>(ring + (size_t)rg.s * TB);
             if (t == ty && tid == 0) xy_s[par] = VT::load1(ring + (size_t)rg.s * TB + (ybyte - (int64_t)ty * TB));
+            const int64_t e0 = (int64_t)t * TV * VEC;
+            // the weighted sum comes with pass 2 when there is one
             if (t < p.ntiles - 1)
-                stats_tile<T, NC, NV, true>(tile, tid, TV, m, d2, s2);
+                stats_tile<T, NC, NV, true, WT && !GRAD>(tile, tid, TV, m, d2, s2, p.cw, e0);
             else
-                stats_tile<T, NC, NV, false>(tile, tid, last_nvec, m, d2, s2);
+                stats_tile<T, NC, NV, false, WT && !GRAD>(tile, tid, last_nvec, m, d2, s2, p.cw, e0);
             release();
         }
 
@@ -300,8 +347,11 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
         }
         const float lse = G.m + logf(G.d);
         const float xy = xy_s[par];
-        if (tid == 0) {
-            p.loss[r] = lse - (1.f - p.a) * xy - p.a_over_v * G.S;
+        const float wy = WT ? __ldg(p.cw + y) : 1.f;
+        if (!(WT && GRAD) && tid == 0) {
+            // weighted: (1-a) w_y (lse - x_y) + (a/V) (W lse - sum_j w_j x_j)
+            p.loss[r] = WT ? (1.f - p.a) * wy * (lse - xy) + p.a_over_v * (wsum * lse - G.S)
+                           : lse - (1.f - p.a) * xy - p.a_over_v * G.S;
             if (p.lse_out) p.lse_out[r] = lse;
         }
 
@@ -309,24 +359,52 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
         if (GRAD) {
             const float nll = -lse * kLog2e;
             const float bb = g * p.a_over_v;
+            // softmax scale: g, or (weighted) g ((1-a) w_y + (a/V) W)
+            const float c = WT ? g * ((1.f - p.a) * wy + p.a_over_v * wsum) : g;
             const float2 NL = make_float2(nll, nll);
-            const float2 G2 = make_float2(g, g);
+            const float2 G2 = make_float2(c, c);
             const float2 NB = make_float2(-bb, -bb);
+            float2 sw2 = make_float2(0.f, 0.f);
             for (int t = 0; t < p.ntiles; ++t) {
                 wait_full();
                 const uint4* tile = reinterpret_cast<const uint4*>(ring + (size_t)rg.s * TB);
                 uint4* dst = reinterpret_cast<uint4*>(rowp + (size_t)t * TB);
-                if (t < p.ntiles - 1)
-                    grad_tile<T, NC, NV, true>(tile, dst, tid, TV, NL, G2, NB);
-                else
-                    grad_tile<T, NC, NV, false>(tile, dst, tid, last_nvec, NL, G2, NB);
+                const int64_t e0 = (int64_t)t * TV * VEC;
+                // without smoothing the weighted gradient is c * softmax -
+                // c [j == y] and the loss has no sum_j w_j x_j term: no
+                // per-class weight is read
+                if (WT && p.a != 0.f) {
+                    if (t < p.ntiles - 1)
+                        grad_tile<T, NC, NV, true, true>(tile, dst, tid, TV, NL, G2, NB, p.cw, e0, sw2);
+                    else
+                        grad_tile<T, NC, NV, false, true>(tile, dst, tid, last_nvec, NL, G2, NB, p.cw, e0, sw2);
+                } else {
+                    if (t < p.ntiles - 1)
+                        grad_tile<T, NC, NV, true, false>(tile, dst, tid, TV, NL, G2, NB, p.cw, e0, sw2);
+                    else
+                        grad_tile<T, NC, NV, false, false>(tile, dst, tid, last_nvec, NL, G2, NB, p.cw, e0, sw2);
+                }
                 release();
                 // the target element: the thread that stored its vector rewrites
                 // it with the one-hot term subtracted (same thread, so the second
                 // store lands after the first)
                 if (t == ty && tid == yv % NC) {
                     const float e = ex2_approx(fmaf(xy, kLog2e, nll));
-                    VT::store1(rowp + ybyte, fmaf(e, g, -bb) - g * (1.f - p.a));
+                    VT::store1(rowp + ybyte, fmaf(e, c, -bb * wy) - g * (1.f - p.a) * wy);
+                }
+            }
+            if (WT) {
+                // the weighted loss needs sum_j w_j x_j: CTA sum in a fixed order
+                float sw = sw2.x + sw2.y;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) sw += __shfl_xor_sync(kFull, sw, off);
+                if (lane == 0) sw_s[par * NW + warp] = sw;
+                named_bar_sync(1, NC);
+                if (tid == 0) {
+                    float S = 0.f;
+                    for (int w = 0; w < NW; ++w) S += sw_s[par * NW + w];
+                    p.loss[r] = (1.f - p.a) * wy * (lse - xy) + p.a_over_v * (wsum * lse - S);
+                    if (p.lse_out) p.lse_out[r] = lse;
                 }
             }
         }
@@ -357,15 +435,16 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
             if (tid == 0) {
                 double tot = 0.0;
                 for (int w = 0; w < NW; ++w) tot += dred[w];
-                p.mean_out[0] = (float)(tot / (double)(*p.n_dev));  // 0/0 = NaN: all ignored
+                const double den = WT ? *p.wdenom : (double)(*p.n_dev);
+                p.mean_out[0] = (float)(tot / den);  // 0/0 = NaN: all ignored
             }
         }
     }
 }
 
-template <typename T, int NC, int NV, bool GRAD>
+template <typename T, int NC, int NV, bool GRAD, bool WT>
 cudaError_t launch_stream_one(const Problem& pb, const StreamPlan& plan, cudaStream_t s) {
-    auto kern = ce_stream_kernel<T, NC, NV, GRAD>;
+    auto kern = ce_stream_kernel<T, NC, NV, GRAD, WT>;
     constexpr int NW = NC / 32;
     StreamArgs a;
     a.logits = pb.logits;
@@ -394,8 +473,11 @@ cudaError_t launch_stream_one(const Problem& pb, const StreamPlan& plan, cudaStr
     a.l2_keep = plan.l2_keep;
     a.ticket = pb.ticket;
     a.mean_out = pb.mean_out;
+    a.cw = pb.cw;
+    a.wdenom = pb.wdenom;
+    a.wsum = pb.wsum;
     const size_t smem = (size_t)plan.stages * a.tile_bytes + 24 * sizeof(uint64_t) +
-                        2 * NW * sizeof(float4) + 2 * sizeof(float) + 2 * sizeof(int) + 16;
+                        2 * NW * sizeof(float4) + (2 + 2 * NW) * sizeof(float) + 2 * sizeof(int) + 16;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0, per_sm = 0;
@@ -420,18 +502,23 @@ cudaError_t launch_stream_one(const Problem& pb, const StreamPlan& plan, cudaStr
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-// Tiles of 16 or 32 KB, consumed by 256 or 512 threads.
+// Tiles of 16 or 32 KB, consumed by 256 or 512 threads; the weighted pass
+// runs the 256-thread shapes only.
 template <typename T, bool GRAD>
 cudaError_t launch_stream_typed(const Problem& pb, const StreamPlan& plan, cudaStream_t s) {
+    if (pb.cw) {
+        if (plan.threads != 256) return cudaErrorInvalidConfiguration;
+        return plan.tile_kb == 16 ? launch_stream_one<T, 256, 4, GRAD, true>(pb, plan, s)
+                                  : launch_stream_one<T, 256, 8, GRAD, true>(pb, plan, s);
+    }
     if (plan.tile_kb == 16)
-        return plan.threads == 512 ? launch_stream_one<T, 512, 2, GRAD>(pb, plan, s)
-                                   : launch_stream_one<T, 256, 4, GRAD>(pb, plan, s);
-    return plan.threads == 512 ? launch_stream_one<T, 512, 4, GRAD>(pb, plan, s)
-                               : launch_stream_one<T, 256, 8, GRAD>(pb, plan, s);
+        return plan.threads == 512 ? launch_stream_one<T, 512, 2, GRAD, false>(pb, plan, s)
+                                   : launch_stream_one<T, 256, 4, GRAD, false>(pb, plan, s);
+    return plan.threads == 512 ? launch_stream_one<T, 512, 4, GRAD, false>(pb, plan, s)
+                               : launch_stream_one<T, 256, 8, GRAD, false>(pb, plan, s);
 }
 
 }  // namespace
-
 cudaError_t launch_stream(const Problem& p, const StreamPlan& plan, cudaStream_t s) {
     switch (p.dtype) {
         case CE_F32:
