@@ -82,6 +82,20 @@ def profiled_traffic(w, path: int):
     return (rec["dram_bytes_read"] + rec["dram_bytes_write"]) * w.N / rec["captured_rows"]
 
 
+L2_BYTES = 129 * 1000 * 1000  # GB300 L2
+
+
+def l2_note(logits_bytes: int) -> str:
+    """How the timed loop stands to the L2: inputs several times larger than
+    it need no flush between steps; smaller ones stay (partly) resident."""
+    if logits_bytes >= 4 * L2_BYTES:
+        return (f"inputs {logits_bytes / 1e9:.2f} GB >> 129 MB L2 (no flush needed)")
+    if logits_bytes > L2_BYTES:
+        return (f"inputs {logits_bytes / 1e6:.0f} MB, 1-4x the 129 MB L2 "
+                "(not flushed: partly L2-resident)")
+    return f"inputs {logits_bytes / 1e6:.1f} MB, smaller than the 129 MB L2 (L2-resident)"
+
+
 def aggregate(local_ms: float, local_tokens: int, world: int, all_reduce_max=None):
     """Whole-job throughput: the units all ranks processed over the slowest
     rank's time.  all_reduce_max(x) returns the max of x over ranks."""
@@ -244,8 +258,7 @@ def config_of(w, args) -> dict:
                         f"label_smoothing={w.label_smoothing}, reduce_loss={w.reduce_loss}, "
                         "gradient in place",
             "tokens_per_step": w.N, "vocab": w.V, "logits_dtype": w.dtype,
-            "accumulate": "f32", "l2": "inputs 4.2 GB >> 129 MB L2 (no flush needed)"
-            if w.logits_bytes > 1 << 30 else "inputs smaller than L2",
+            "accumulate": "f32", "l2": l2_note(w.logits_bytes),
             "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
 
 

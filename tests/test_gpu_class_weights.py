@@ -13,18 +13,30 @@ pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda")
 
 
-# (force_path, tile_kb, weight offset in floats): the planner's choice (the
-# stream kernel when rows and weights are 16-byte aligned), its 16 KB-tile
-# shape, the two-stage kernels forced, and weights 4 bytes off alignment
-# (the planner falls back to the two-stage kernels)
-ROUTES = [(0, 0, 0), (0, 16, 0), (3, 0, 0), (0, 0, 1)]
+# (force_path, tile_kb, stages, weight offset in floats): the planner's
+# choice (the stream kernel when rows and weights are 16-byte aligned, 16 KB
+# tiles 6 deep), its 32 KB-tile shape, a ring of 4 tiles (too shallow for a
+# 16-bit tile and its two weight slots twice: two-stage kernels; enough for
+# fp32), a ring of 12 16-KB tiles, the two-stage kernels forced, and weights
+# 4 bytes off alignment (two-stage)
+ROUTES = [(0, 0, 0, 0), (0, 32, 0, 0), (0, 16, 4, 0), (0, 0, 12, 0), (3, 0, 0, 0),
+          (0, 0, 0, 1)]
 
 
-@pytest.mark.parametrize("route", ROUTES, ids=["auto", "tile16", "two_stage", "unaligned_w"])
+def expected_path(force, stages, woff, elem_bytes):
+    if force == 3 or woff:
+        return 3
+    if stages and stages < 2 * (1 + 4 // elem_bytes):
+        return 3
+    return 4
+
+
+@pytest.mark.parametrize("route", ROUTES, ids=["auto", "tile32", "stages4", "stages12",
+                                               "two_stage", "unaligned_w"])
 @pytest.mark.parametrize("name", ["c1_bsv4096_f32", "c2_sbv8192_bf16", "c3h_bsv32000_f16_spiked",
                                   "c5_bsv128000_bf16_ls"])
 def test_class_weighted_pass(name, route):
-    force, tile_kb, woff = route
+    force, tile_kb, stages, woff = route
     w = wl.WORKLOADS[name]
     rng = np.random.default_rng(31)
     cw = rng.uniform(0.1, 3.0, w.V).astype(np.float32)
@@ -39,10 +51,11 @@ def test_class_weighted_pass(name, route):
     xd, td = x.to(DEV), t.to(DEV)
     cwd = torch.zeros(w.V + woff, device=DEV)[woff:]
     cwd.copy_(torch.tensor(cw))
-    opts = pkg.make_options(force_path=force, tune_tile_kb=tile_kb)
-    want = 3 if (force == 3 or woff) else 4
+    opts = pkg.make_options(force_path=force, tune_tile_kb=tile_kb, tune_stages=stages)
+    want = expected_path(force, stages, woff, w.elem_bytes)
     assert pkg.ce_plan_path(xd, opts=pkg.make_options(
-        force_path=force, tune_tile_kb=tile_kb, class_weights=cwd.data_ptr()))[0] == want
+        force_path=force, tune_tile_kb=tile_kb, tune_stages=stages,
+        class_weights=cwd.data_ptr()))[0] == want
     n = torch.zeros(1, dtype=torch.int64, device=DEV)
     loss = pkg.ce_fwd_bwd(xd, td, label_smoothing=w.label_smoothing, reduce_loss=w.reduce_loss,
                           dloss=torch.tensor(dl, dtype=torch.float32, device=DEV),
@@ -55,7 +68,8 @@ def test_class_weighted_pass(name, route):
     # forward only gives the same losses
     lf = pkg.ce_fwd_only(x.to(DEV), td, label_smoothing=w.label_smoothing,
                          reduce_loss=w.reduce_loss, layout=w.layout, class_weights=cwd,
-                         opts=pkg.make_options(force_path=force, tune_tile_kb=tile_kb))
+                         opts=pkg.make_options(force_path=force, tune_tile_kb=tile_kb,
+                                               tune_stages=stages))
     harness.check_loss(lf.cpu().numpy(), ref["loss"], w.dtype, name)
 
 

@@ -48,10 +48,13 @@ bool plan_rows(int64_t row_bytes, const ce_options* o, RowsPlan* rp) {
 // Row-streaming kernel: tiles of 16 or 32 KB consumed by 256 or 512 threads,
 // `stages` of them in flight.  Defaults from sweeps over V = 32000 .. 256000
 // bf16 (32 KB x 5 was best or within 2% of best at every width).
-bool plan_stream(const ce_options* o, StreamPlan* sp) {
+// def_tile_kb / def_stages: the shape when the options leave it open (0:
+// 32 KB tiles 5 deep, 16 KB tiles 12 deep).
+bool plan_stream(const ce_options* o, StreamPlan* sp, int def_tile_kb = 0, int def_stages = 0) {
     sp->threads = (o && o->tune_threads) ? o->tune_threads : 256;
-    sp->tile_kb = (o && o->tune_tile_kb) ? o->tune_tile_kb : 32;
-    sp->stages = (o && o->tune_stages) ? o->tune_stages : (sp->tile_kb == 32 ? 5 : 12);
+    sp->tile_kb = (o && o->tune_tile_kb) ? o->tune_tile_kb : (def_tile_kb ? def_tile_kb : 32);
+    sp->stages = (o && o->tune_stages) ? o->tune_stages
+                                       : (def_stages ? def_stages : (sp->tile_kb == 32 ? 5 : 12));
     sp->ctas_per_sm_cap = o ? o->tune_ctas_per_sm : 0;
     sp->l2_keep = (o && o->tune_l2_keep == 2) ? 0 : 1;
     const size_t tile = (size_t)sp->tile_kb * 1024;
@@ -127,8 +130,13 @@ Plan make_plan(const Problem& p, const ce_options* o) {
         // the rows and the weight vector are 16-byte aligned and no split is
         // asked for, the two-stage kernels otherwise
         const bool cw_aligned = reinterpret_cast<uintptr_t>(o->class_weights) % 16 == 0;
+        // each gradient tile brings its weights (4/s times its bytes) into
+        // the next ring slots: 16 KB tiles 6 deep unless tuned (two CTAs per
+        // SM), and room for two tiles with their weights
+        const int group = 1 + 4 / (int)p.es;
         if ((force == CE_PATH_AUTO || force == CE_PATH_STREAM) && aligned && cw_aligned &&
-            o->num_vocab_chunks == 0 && plan_stream(o, &pl.stream) && pl.stream.threads == 256) {
+            o->num_vocab_chunks == 0 && plan_stream(o, &pl.stream, 16, 6) &&
+            pl.stream.threads == 256 && pl.stream.stages >= 2 * group) {
             pl.path = CE_PATH_STREAM;
             return pl;
         }

@@ -22,6 +22,7 @@ namespace {
 
 constexpr int kSplitThreads = 256;
 constexpr int kSplitWarps = kSplitThreads / 32;
+constexpr int kSplitBatch = 4;  // 16-byte loads in flight per thread
 
 struct SplitArgs {
     char* logits;
@@ -78,22 +79,38 @@ __global__ void __launch_bounds__(kSplitThreads) ce_split_stats_kernel(const __g
 
     float m = -INFINITY, d = 0.f, S = 0.f;
     if (VECOK) {
-        // chunk boundaries are multiples of the vector length
+        // chunk boundaries are multiples of the vector length; kSplitBatch
+        // loads in flight per thread, one rescale per batch with a new max
         const uint4* rv = reinterpret_cast<const uint4*>(row);
-        for (int64_t v = k0 / VEC + threadIdx.x; v < k1 / VEC; v += kSplitThreads) {
-            const uint4 raw = __ldcs(rv + v);
-            const float vm = VT::vmax(raw);
+        const int64_t vend = k1 / VEC;
+        for (int64_t vb = k0 / VEC + threadIdx.x; vb < vend; vb += kSplitThreads * kSplitBatch) {
+            uint4 raw[kSplitBatch];
+            float vm = -INFINITY;
+#pragma unroll
+            for (int u = 0; u < kSplitBatch; ++u) {
+                const int64_t v = vb + (int64_t)u * kSplitThreads;
+                if (v < vend) {
+                    raw[u] = __ldcs(rv + v);
+                    vm = fmaxf(vm, VT::vmax(raw[u]));
+                }
+            }
             if (vm > m) {
                 if (m != -INFINITY) d *= ex2_approx((m - vm) * kLog2e);
                 m = vm;
             }
             const float nml = -m * kLog2e;
-            float x[VEC];
-            VT::unpack(raw, x);
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                d += ex2_approx(fmaf(x[e], kLog2e, nml));
-                S = WT ? fmaf(__ldg(p.cw + v * VEC + e), x[e], S) : S + x[e];
+            for (int u = 0; u < kSplitBatch; ++u) {
+                const int64_t v = vb + (int64_t)u * kSplitThreads;
+                if (v < vend) {
+                    float x[VEC];
+                    VT::unpack(raw[u], x);
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) {
+                        d += ex2_approx(fmaf(x[e], kLog2e, nml));
+                        S = WT ? fmaf(__ldg(p.cw + v * VEC + e), x[e], S) : S + x[e];
+                    }
+                }
             }
         }
     } else {
@@ -200,30 +217,41 @@ __global__ void __launch_bounds__(kSplitThreads) ce_split_grad_kernel(const __gr
         const float2 L2 = make_float2(kLog2e, kLog2e), NL = make_float2(nll, nll);
         const float2 C2 = make_float2(c, c), NB = make_float2(-ga, -ga);
         uint4* rv = reinterpret_cast<uint4*>(row);
-        for (int64_t v = k0 / VEC + threadIdx.x; v < k1 / VEC; v += kSplitThreads) {
-            const uint4 raw = __ldcs(rv + v);
-            float2 x[PP], o[PP];
-            VT::unpack2(raw, x);
+        const int64_t vend = k1 / VEC;
+        for (int64_t vb = k0 / VEC + threadIdx.x; vb < vend; vb += kSplitThreads * kSplitBatch) {
+            uint4 raw[kSplitBatch];
 #pragma unroll
-            for (int q = 0; q < PP; ++q) {
-                const float2 e = __ffma2_rn(x[q], L2, NL);
-                const float2 pe = make_float2(ex2_approx(e.x), ex2_approx(e.y));
-                if (WT) {
-                    const float w0 = __ldg(p.cw + v * VEC + 2 * q), w1 = __ldg(p.cw + v * VEC + 2 * q + 1);
-                    o[q] = __ffma2_rn(pe, C2, make_float2(-ga * w0, -ga * w1));
-                } else {
-                    o[q] = __ffma2_rn(pe, C2, NB);
-                }
+            for (int u = 0; u < kSplitBatch; ++u) {
+                const int64_t v = vb + (int64_t)u * kSplitThreads;
+                if (v < vend) raw[u] = __ldcs(rv + v);
             }
-            if (v == y / VEC) {
-                const int ey = (int)(y % VEC);
+#pragma unroll
+            for (int u = 0; u < kSplitBatch; ++u) {
+                const int64_t v = vb + (int64_t)u * kSplitThreads;
+                if (v >= vend) continue;
+                float2 x[PP], o[PP];
+                VT::unpack2(raw[u], x);
 #pragma unroll
                 for (int q = 0; q < PP; ++q) {
-                    if (2 * q == ey) o[q].x -= hit;
-                    if (2 * q + 1 == ey) o[q].y -= hit;
+                    const float2 e = __ffma2_rn(x[q], L2, NL);
+                    const float2 pe = make_float2(ex2_approx(e.x), ex2_approx(e.y));
+                    if (WT) {
+                        const float w0 = __ldg(p.cw + v * VEC + 2 * q), w1 = __ldg(p.cw + v * VEC + 2 * q + 1);
+                        o[q] = __ffma2_rn(pe, C2, make_float2(-ga * w0, -ga * w1));
+                    } else {
+                        o[q] = __ffma2_rn(pe, C2, NB);
+                    }
                 }
+                if (v == y / VEC) {
+                    const int ey = (int)(y % VEC);
+#pragma unroll
+                    for (int q = 0; q < PP; ++q) {
+                        if (2 * q == ey) o[q].x -= hit;
+                        if (2 * q + 1 == ey) o[q].y -= hit;
+                    }
+                }
+                stg128_stream(rv + v, VT::pack2(o));
             }
-            stg128_stream(rv + v, VT::pack2(o));
         }
     } else {
         for (int64_t v = k0 + threadIdx.x; v < k1; v += kSplitThreads) {

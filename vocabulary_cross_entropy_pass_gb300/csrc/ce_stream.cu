@@ -20,10 +20,14 @@
 //
 // Class weights (torch F.cross_entropy(weight=...), the weighted NLL of
 // mindspore/hyper-parallel #269): the gradient is c * softmax - g (a/V) w_j
-// with c = g ((1-a) w_y + (a/V) W), so pass 1 is unchanged; pass 2 reads the
-// weights (16-byte loads, L2-resident) and also sums w_j x_j for the row's
-// loss, (1-a) w_y (lse - x_y) + (a/V) (W lse - sum_j w_j x_j), written after
-// pass 2.  The mean divides by the summed target weight of the kept rows.
+// with c = g ((1-a) w_y + (a/V) W), so pass 1 is unchanged; in pass 2 the
+// producer follows each logits tile with its fp32 weights (4/sizeof(T) times
+// the tile's bytes, L2-resident, in the next ring slots), and the consumers
+// also sum w_j x_j for the row's loss, (1-a) w_y (lse - x_y) + (a/V) (W lse -
+// sum_j w_j x_j), written after pass 2.  Without smoothing (a = 0) no weight
+// but w_y is needed.  The mean divides by the summed target weight of the
+// kept rows.  (The forward-only weighted pass reads the weights in pass 1,
+// with plain loads.)
 //
 // Warp specialisation: warps 0..NC/32-1 consume tiles; the last warp only
 // issues copies.  `full[s]` completes when tile s has landed (TMA transaction
@@ -157,13 +161,19 @@ __device__ __forceinline__ void stats_tile(const uint4* tile, int tid, int nvec,
 // stored over the logits.  Unweighted: c = g, b_j = g a/V (NB = -b).
 // WT: c = g ((1-a) w_y + (a/V) W), b_j = g (a/V) w_j (NB = -g a/V), and the
 // class-weighted sum sum_j w_j x_j of the loss is accumulated into sw2 here,
-// so each weight is read once per row.
+// so each weight is read once per row.  The tile's weights sit in WS ring
+// slots after it (fp32, 4/sizeof(T) times the tile's bytes): vector v of the
+// tile finds its VEC weights in slot v / (TV/WS) at vector v % (TV/WS).
 template <typename T, int NC, int NV, bool FULL, bool WT>
 __device__ __forceinline__ void grad_tile(const uint4* tile, uint4* dst, int tid, int nvec,
-                                          float2 NL, float2 G2, float2 NB, const float* cw,
-                                          int64_t e0, float2& sw2) {
+                                          float2 NL, float2 G2, float2 NB,
+                                          const unsigned char* const* wslot, float2& sw2) {
     using VT = Vec<T>;
-    constexpr int P = VT::kElems / 2;
+    constexpr int VEC = VT::kElems;
+    constexpr int P = VEC / 2;
+    constexpr int WS = 4 / (int)sizeof(T);  // weight slots per tile
+    constexpr int NVS = NV / WS;            // vectors per thread whose weights share a slot
+    static_assert(NV % WS == 0, "a thread's vectors split evenly over the weight slots");
     const float2 L2 = make_float2(kLog2e, kLog2e);
     uint4 raw[NV];
 #pragma unroll
@@ -174,7 +184,16 @@ __device__ __forceinline__ void grad_tile(const uint4* tile, uint4* dst, int tid
         if (FULL || tid + i * NC < nvec) {
             float2 x[P], o[P], w[P];
             VT::unpack2(raw[i], x);
-            if constexpr (WT) load_weights<T>(cw, e0 + (int64_t)(tid + i * NC) * VT::kElems, w);
+            if constexpr (WT) {
+                const float4* ws = reinterpret_cast<const float4*>(wslot[i / NVS]) +
+                                   (size_t)(tid + (i % NVS) * NC) * (VEC / 4);
+#pragma unroll
+                for (int k = 0; k < VEC / 4; ++k) {
+                    const float4 f = ws[k];
+                    w[2 * k] = make_float2(f.x, f.y);
+                    w[2 * k + 1] = make_float2(f.z, f.w);
+                }
+            }
 #pragma unroll
             for (int j = 0; j < P; ++j) {
                 const float2 a = __ffma2_rn(x[j], L2, NL);
@@ -190,8 +209,11 @@ __device__ __forceinline__ void grad_tile(const uint4* tile, uint4* dst, int tid
     }
 }
 
+// The weighted gradient pass issues ~40% more instructions per element than
+// the plain one: its 16 KB-tile shape is built for two CTAs per SM (more warps
+// to hide latency), every other shape for one.
 template <typename T, int NC, int NV, bool GRAD, bool WT>
-__global__ void __launch_bounds__(NC + 32, 1)
+__global__ void __launch_bounds__(NC + 32, (WT && GRAD && NV * NC * 16 == 16384) ? 2 : 1)
 ce_stream_kernel(const __grid_constant__ StreamArgs p) {
     using VT = Vec<T>;
     constexpr int VEC = VT::kElems;
@@ -235,12 +257,17 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
     };
     const int npass = GRAD ? 2 : 1;
     const int last_nvec = (int)(p.last_bytes / 16);
+    // weighted gradient pass with smoothing: each tile brings its class
+    // weights into the next WS ring slots (without smoothing no weight is read)
+    constexpr int WS = 4 / ES;
+    const bool wring = WT && GRAD && p.a != 0.f;
 
     // ------------------------------------------------------------ producer warp
     if (warp == NW) {
         if (lane == 0) {
             const uint64_t pol_keep = p.l2_keep ? l2_evict_last_policy() : l2_evict_first_policy();
             const uint64_t pol_drop = l2_evict_first_policy();
+            const uint64_t pol_wt = l2_evict_last_policy();  // every CTA reads the weights
             Ring rg(p.stages);
             uint32_t issued = 0;
             for (int64_t r = blockIdx.x; r < p.N && !*abort_flag; r += gridDim.x) {
@@ -260,6 +287,30 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
                                     pass == 0 ? pol_keep : pol_drop);
                         rg.next();
                         ++issued;
+                        if (pass == 1 && wring) {
+                            // the tile's weights: WS * bytes from cw + t * WS * TB, one
+                            // slot of up to TB bytes each (a slot past the end of the
+                            // weights completes with no copy)
+                            const char* wsrc = reinterpret_cast<const char*>(p.cw) + (size_t)t * WS * TB;
+                            const uint32_t wbytes = bytes * WS;
+                            for (int h = 0; h < WS; ++h) {
+                                if (!mbar_wait_bounded(&empty[rg.s], rg.ph ^ 1u)) {
+                                    griddep_wait();
+                                    atomicOr(p.err, CE_DEVERR_TIMEOUT);
+                                    *abort_flag = 1;
+                                    break;
+                                }
+                                const uint32_t hb = wbytes > (uint32_t)(h * TB)
+                                                        ? min(wbytes - (uint32_t)(h * TB), (uint32_t)TB)
+                                                        : 0u;
+                                mbar_arrive_expect_tx(&full[rg.s], hb);
+                                if (hb) tma_load_1d(ring + (size_t)rg.s * TB, wsrc + (size_t)h * TB, hb,
+                                                    &full[rg.s], pol_wt);
+                                rg.next();
+                                ++issued;
+                            }
+                            if (*abort_flag) break;
+                        }
                     }
                 }
             }
@@ -367,24 +418,41 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
             float2 sw2 = make_float2(0.f, 0.f);
             for (int t = 0; t < p.ntiles; ++t) {
                 wait_full();
-                const uint4* tile = reinterpret_cast<const uint4*>(ring + (size_t)rg.s * TB);
+                const int st = rg.s;
+                const uint4* tile = reinterpret_cast<const uint4*>(ring + (size_t)st * TB);
                 uint4* dst = reinterpret_cast<uint4*>(rowp + (size_t)t * TB);
-                const int64_t e0 = (int64_t)t * TV * VEC;
+                rg.next();
                 // without smoothing the weighted gradient is c * softmax -
                 // c [j == y] and the loss has no sum_j w_j x_j term: no
                 // per-class weight is read
-                if (WT && p.a != 0.f) {
+                if (WT && wring) {
+                    int sw[WS];
+                    const unsigned char* wslot[WS];
+#pragma unroll
+                    for (int h = 0; h < WS; ++h) {
+                        wait_full();
+                        sw[h] = rg.s;
+                        wslot[h] = ring + (size_t)rg.s * TB;
+                        rg.next();
+                    }
                     if (t < p.ntiles - 1)
-                        grad_tile<T, NC, NV, true, true>(tile, dst, tid, TV, NL, G2, NB, p.cw, e0, sw2);
+                        grad_tile<T, NC, NV, true, true>(tile, dst, tid, TV, NL, G2, NB, wslot, sw2);
                     else
-                        grad_tile<T, NC, NV, false, true>(tile, dst, tid, last_nvec, NL, G2, NB, p.cw, e0, sw2);
+                        grad_tile<T, NC, NV, false, true>(tile, dst, tid, last_nvec, NL, G2, NB, wslot, sw2);
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&empty[st]);
+#pragma unroll
+                        for (int h = 0; h < WS; ++h) mbar_arrive(&empty[sw[h]]);
+                    }
                 } else {
                     if (t < p.ntiles - 1)
-                        grad_tile<T, NC, NV, true, false>(tile, dst, tid, TV, NL, G2, NB, p.cw, e0, sw2);
+                        grad_tile<T, NC, NV, true, false>(tile, dst, tid, TV, NL, G2, NB, nullptr, sw2);
                     else
-                        grad_tile<T, NC, NV, false, false>(tile, dst, tid, last_nvec, NL, G2, NB, p.cw, e0, sw2);
+                        grad_tile<T, NC, NV, false, false>(tile, dst, tid, last_nvec, NL, G2, NB, nullptr, sw2);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[st]);
                 }
-                release();
                 // the target element: the thread that stored its vector rewrites
                 // it with the one-hot term subtracted (same thread, so the second
                 // store lands after the first)

@@ -36,7 +36,10 @@ struct VpPartArgs {
 };
 
 // One CTA per row: a running (max, sum-exp, sum) per thread over 16-byte
-// vectors (one rescale per vector whose max is new), then the CTA combine.
+// vectors, kVpBatch loads in flight per thread (one rescale per batch whose
+// max is new), then the CTA combine.
+constexpr int kVpBatch = 4;
+
 template <typename T>
 __global__ void __launch_bounds__(kVpThreads) ce_vp_partials_kernel(const __grid_constant__ VpPartArgs p) {
     using VT = Vec<T>;
@@ -59,9 +62,17 @@ __global__ void __launch_bounds__(kVpThreads) ce_vp_partials_kernel(const __grid
         if (p.vec_ok) {
             const uint4* rv = reinterpret_cast<const uint4*>(row);
             const int64_t nv = p.V / VEC;
-            for (int64_t v = threadIdx.x; v < nv; v += kVpThreads) {
-                const uint4 raw = __ldcs(rv + v);
-                const float vm = VT::vmax(raw);
+            for (int64_t vb = threadIdx.x; vb < nv; vb += kVpThreads * kVpBatch) {
+                uint4 raw[kVpBatch];
+                float vm = -INFINITY;
+#pragma unroll
+                for (int u = 0; u < kVpBatch; ++u) {
+                    const int64_t v = vb + (int64_t)u * kVpThreads;
+                    if (v < nv) {
+                        raw[u] = __ldcs(rv + v);
+                        vm = fmaxf(vm, VT::vmax(raw[u]));
+                    }
+                }
                 if (vm > m) {
                     if (m != -INFINITY) {
                         const float c = ex2_approx((m - vm) * kLog2e);
@@ -72,13 +83,18 @@ __global__ void __launch_bounds__(kVpThreads) ce_vp_partials_kernel(const __grid
                 }
                 const float nml = -m * kLog2e;
                 const float2 NM = make_float2(nml, nml);
-                float2 x[PP];
-                VT::unpack2(raw, x);
 #pragma unroll
-                for (int q = 0; q < PP; ++q) {
-                    const float2 e = __ffma2_rn(x[q], L2, NM);
-                    d2 = __fadd2_rn(d2, make_float2(ex2_approx(e.x), ex2_approx(e.y)));
-                    s2 = __fadd2_rn(s2, x[q]);
+                for (int u = 0; u < kVpBatch; ++u) {
+                    if (vb + (int64_t)u * kVpThreads < nv) {
+                        float2 x[PP];
+                        VT::unpack2(raw[u], x);
+#pragma unroll
+                        for (int q = 0; q < PP; ++q) {
+                            const float2 e = __ffma2_rn(x[q], L2, NM);
+                            d2 = __fadd2_rn(d2, make_float2(ex2_approx(e.x), ex2_approx(e.y)));
+                            s2 = __fadd2_rn(s2, x[q]);
+                        }
+                    }
                 }
             }
         } else {
