@@ -23,6 +23,9 @@ TDT = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
 @pytest.mark.parametrize("N,H,V,dtype,chunk,a,red", [
     (333, 192, 4000, "bf16", 128, 0.1, True),     # warp path per chunk, ragged last chunk
     (200, 96, 20000, "bf16", 64, 0.0, False),     # stream path per chunk
+    # stream path, chunks of more rows than CTAs: rows are claimed from the
+    # shared counter, which each chunk's pass leaves zeroed for the next
+    (1200, 64, 20000, "bf16", 400, 0.1, True),
     (100, 64, 3000, "f32", 37, 0.1, False),
     (150, 128, 6000, "f16", 1000, 0.0, True),     # one chunk
 ])

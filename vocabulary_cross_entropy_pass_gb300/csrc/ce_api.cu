@@ -240,6 +240,8 @@ ce_status run_pass(Problem& pb, const ce_options* o, float* loss_out, int64_t* n
     pb.cw = o ? o->class_weights : nullptr;
     pb.wdenom = reinterpret_cast<double*>(w + kWsWeightDenomOffset);
     pb.wsum = reinterpret_cast<double*>(w + kWsWeightSumOffset);
+    pb.row_claim = reinterpret_cast<uint32_t*>(w + kWsRowClaimOffset);
+    pb.row_done = reinterpret_cast<uint32_t*>(w + kWsRowDoneOffset);
     // the stream and warp kernels compute the mean themselves (their last CTA)
     const bool mean_in_kernel =
         pb.reduce && (pl.path == CE_PATH_STREAM || pl.path == CE_PATH_WARP) && pb.N > 0;

@@ -21,7 +21,7 @@ __global__ void __launch_bounds__(kAuxThreads)
 ce_count_kernel(const int64_t* __restrict__ targets, int64_t ts0, int64_t ts1, int64_t dim1,
                 int64_t N, int64_t V, int64_t ignore_idx, int64_t* n_ws, int64_t* n_out,
                 uint32_t* err, uint32_t* ticket, const float* __restrict__ cw, double* wdenom,
-                double* wsum) {
+                double* wsum, uint32_t* row_claim, uint32_t* row_done) {
     // the pass launched after this kernel may start now: it waits for this
     // kernel's results itself (griddepcontrol.wait) before it reads them
     griddep_launch_dependents();
@@ -72,6 +72,10 @@ ce_count_kernel(const int64_t* __restrict__ targets, int64_t ts0, int64_t ts1, i
         if (n_out) *n_out = tn;
         *err = te;     // starts the error word of this pass
         *ticket = 0u;  // no CTA of the pass has finished yet
+        if (row_claim) {  // no row of the pass claimed yet
+            *row_claim = 0u;
+            *row_done = 0u;
+        }
         if (cw) {
             *wdenom = twd;
             *wsum = tws;
@@ -104,7 +108,7 @@ ce_mean_kernel(const float* __restrict__ loss_rows, int64_t N, const int64_t* n_
 cudaError_t launch_count(const Problem& p, int64_t* n_out, cudaStream_t s) {
     ce_count_kernel<<<1, kAuxThreads, 0, s>>>(p.targets, p.ts0, p.ts1, p.dim1, p.N, p.V,
                                               p.ignore_idx, p.n_dev, n_out, p.err, p.ticket, p.cw,
-                                              p.wdenom, p.wsum);
+                                              p.wdenom, p.wsum, p.row_claim, p.row_done);
     return cudaGetLastError();
 }
 

@@ -16,6 +16,8 @@ namespace gbce {
 //   [16, 20)    uint32 count of CTAs done (the stream kernel's in-kernel mean)
 //   [24, 32)    double summed class weight of the kept rows' targets (weighted pass)
 //   [32, 40)    double summed class weight over the vocabulary (weighted pass)
+//   [40, 44)    uint32 rows claimed beyond the first grid's worth (stream kernel)
+//   [44, 48)    uint32 CTAs done claiming (the last one zeroes both words)
 //   [256, ...)  float per-row losses (N) -- used when reduce_loss
 //   [...]       float4 per-(row, chunk) partials of the two-stage path
 constexpr size_t kWsErrOffset = 0;
@@ -23,6 +25,8 @@ constexpr size_t kWsCountOffset = 8;
 constexpr size_t kWsTicketOffset = 16;
 constexpr size_t kWsWeightDenomOffset = 24;
 constexpr size_t kWsWeightSumOffset = 32;
+constexpr size_t kWsRowClaimOffset = 40;
+constexpr size_t kWsRowDoneOffset = 44;
 constexpr size_t kWsHeaderBytes = 256;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -49,6 +53,8 @@ struct Problem {
     const float* cw;           // class weights [V] or NULL
     double* wdenom;            // summed weight of kept targets (weighted pass)
     double* wsum;              // summed weight over the vocabulary (weighted pass)
+    uint32_t* row_claim;       // stream kernel: shared row counter (NULL: static rows)
+    uint32_t* row_done;        // stream kernel: CTAs done claiming
 };
 
 // Plan of the fused (row / cluster) kernel.

@@ -100,6 +100,8 @@ ce_status ce_linear_fwd_bwd(const void* hidden, const void* weight, ce_dtype dty
     all.err = reinterpret_cast<uint32_t*>(w + kWsErrOffset);
     all.n_dev = reinterpret_cast<int64_t*>(w + kWsCountOffset);
     all.ticket = reinterpret_cast<uint32_t*>(w + kWsTicketOffset);
+    all.row_claim = reinterpret_cast<uint32_t*>(w + kWsRowClaimOffset);
+    all.row_done = reinterpret_cast<uint32_t*>(w + kWsRowDoneOffset);
     all.loss_rows = reduce_loss ? reinterpret_cast<float*>(w + L.rows_off) : loss_out;
     if (launch_count(all, n_non_ignore_out, s) != cudaSuccess) return CE_ERR_LAUNCH;
     if (N == 0) {
@@ -135,6 +137,8 @@ ce_status ce_linear_fwd_bwd(const void* hidden, const void* weight, ce_dtype dty
         pb.err = all.err;
         pb.n_dev = all.n_dev;
         pb.ticket = all.ticket;
+        pb.row_claim = all.row_claim;  // zeroed by the count kernel, then by each pass's last CTA
+        pb.row_done = all.row_done;
         pb.dloss = reduce_loss ? dloss : (dloss ? dloss + r0 : nullptr);
         pb.loss_rows = all.loss_rows + r0;
         pb.grad = grad_hidden != nullptr || grad_weight != nullptr;

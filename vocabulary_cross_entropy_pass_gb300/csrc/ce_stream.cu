@@ -64,6 +64,8 @@ struct StreamArgs {
     const float* cw;       // class weights [V], 16-byte aligned (weighted pass) or NULL
     const double* wdenom;  // summed weight of the kept rows' targets (count kernel)
     const double* wsum;    // summed weight over the vocabulary (count kernel)
+    uint32_t* row_claim;   // rows claimed past the first grid's worth, or NULL (static rows)
+    uint32_t* row_done;    // CTAs done claiming
 };
 
 // The class weights of one 16-byte logits vector: VEC fp32 values, read as
@@ -92,6 +94,24 @@ __device__ __forceinline__ uint64_t l2_evict_last_policy() {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
     return pol;
+}
+
+// Rows handed from the producer warp to the consumer warps ahead of their tiles.
+constexpr int kRowQ = 8;
+
+// Barrier 1 over the consumer threads, returning whether any of them passed
+// `v`: every consumer warp gets the same answer.
+__device__ __forceinline__ bool named_bar_or(int id, int threads, bool v) {
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred pin, pout;\n\t"
+        "setp.ne.u32 pin, %1, 0;\n\t"
+        "bar.red.or.pred pout, %2, %3, pin;\n\t"
+        "selp.u32 %0, 1, 0, pout;\n\t}"
+        : "=r"(out)
+        : "r"((uint32_t)v), "r"(id), "r"(threads)
+        : "memory");
+    return out != 0;
 }
 
 // One ring slot: stage index and phase parity, advanced without division.
@@ -226,7 +246,10 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
     unsigned char* ring = smem;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)p.stages * TB);
     uint64_t* empty = full + 12;
-    float4* red = reinterpret_cast<float4*>(empty + 12);  // [2][NW]
+    uint64_t* qfull = empty + 12;    // row queue: entry written
+    uint64_t* qempty = qfull + kRowQ;  // row queue: entry read by every consumer warp
+    int64_t* rowq = reinterpret_cast<int64_t*>(qempty + kRowQ);
+    float4* red = reinterpret_cast<float4*>(rowq + kRowQ);  // [2][NW]
     float* xy_s = reinterpret_cast<float*>(red + 2 * NW);  // [2]
     float* sw_s = xy_s + 2;                                 // [2][NW] weighted sums
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sw_s + 2 * NW);
@@ -237,6 +260,10 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], NW);
+        }
+        for (int q = 0; q < kRowQ; ++q) {
+            mbar_init(&qfull[q], 1);
+            mbar_init(&qempty[q], NW);
         }
         *abort_flag = 0;
         *last_flag = 0;
@@ -269,11 +296,40 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
             const uint64_t pol_drop = l2_evict_first_policy();
             const uint64_t pol_wt = l2_evict_last_policy();  // every CTA reads the weights
             Ring rg(p.stages);
+            Ring qr(kRowQ);
             uint32_t issued = 0;
-            for (int64_t r = blockIdx.x; r < p.N && !*abort_flag; r += gridDim.x) {
-                if (!is_loaded(row_target(r))) continue;
+            bool counted = false;
+            // rows: the CTA's own first row, then rows claimed from the shared
+            // counter (the count kernel zeroes it), or without a counter every
+            // gridDim.x-th row
+            auto claim = [&](int64_t cur) -> int64_t {
+                if (!p.row_claim) return cur + gridDim.x;
+                if (!counted) {
+                    griddep_wait();
+                    counted = true;
+                }
+                return (int64_t)gridDim.x + (int64_t)atomicAdd(p.row_claim, 1u);
+            };
+            int64_t r = blockIdx.x;
+            for (int k = 0; !*abort_flag; ++k) {
+                // hand the row (or the end mark -1) to the consumer warps
+                if (!mbar_wait_bounded(&qempty[qr.s], qr.ph ^ 1u)) {
+                    griddep_wait();
+                    atomicOr(p.err, CE_DEVERR_TIMEOUT);
+                    *abort_flag = 1;
+                    break;
+                }
+                rowq[qr.s] = r < p.N ? r : -1;
+                mbar_arrive(&qfull[qr.s]);
+                qr.next();
+                if (r >= p.N) break;
+                // claim the successor ahead of this row's copies, so the atomic's
+                // latency hides behind them; the first claim waits for the count
+                // kernel, so it follows the first row's copies instead
+                int64_t next = k > 0 ? claim(r) : -1;
+                const bool loaded = is_loaded(row_target(r));
                 const char* row = row_ptr(r);
-                for (int pass = 0; pass < npass && !*abort_flag; ++pass) {
+                for (int pass = 0; loaded && pass < npass && !*abort_flag; ++pass) {
                     for (int t = 0; t < p.ntiles; ++t) {
                         if (!mbar_wait_bounded(&empty[rg.s], rg.ph ^ 1u)) {
                             griddep_wait();  // the count kernel starts the error word
@@ -313,6 +369,8 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
                         }
                     }
                 }
+                if (k == 0) next = claim(r);
+                r = next;
             }
             if (*abort_flag) {
                 // let every copy already issued land before the CTA goes away
@@ -350,7 +408,25 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
         if (lane == 0) mbar_arrive(&empty[rg.s]);
         rg.next();
     };
-    for (int64_t r = blockIdx.x; r < p.N; r += gridDim.x) {
+    Ring qr(kRowQ);
+    for (;;) {
+        // the next row from the producer warp; the consumer warps take the
+        // exit decision together (a barrier reduction), so every one of them
+        // runs the same rows and the same barriers
+        int64_t r = -1;
+        bool got = false;
+        if (!*abort_flag) {
+            got = mbar_wait_bounded(&qfull[qr.s], qr.ph);
+            if (!got) {
+                atomicOr(p.err, CE_DEVERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+        }
+        if (got) r = rowq[qr.s];
+        __syncwarp();
+        if (got && lane == 0) mbar_arrive(&qempty[qr.s]);
+        qr.next();
+        if (named_bar_or(1, NC, r < 0 || *abort_flag)) break;
         const int64_t y = row_target(r);
         char* rowp = row_ptr(r);
         if (!is_loaded(y)) {
@@ -479,6 +555,16 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
         par ^= 1;
     }
 
+    // the last CTA done claiming rows zeroes the row counter for the next pass
+    // (its rows were all claimed before the end mark this CTA has read)
+    if (p.row_claim && tid == 0) {
+        __threadfence();
+        if (atomicAdd(p.row_done, 1u) == gridDim.x - 1) {
+            atomicExch(p.row_claim, 0u);
+            atomicExch(p.row_done, 0u);
+        }
+    }
+
     // reduce_loss: the last CTA to finish sums the per-row losses in a fixed
     // order (fixed strides per thread, butterflies, warps in order) -- the
     // mean of TENPU #29 section 1, computed on the device
@@ -544,7 +630,10 @@ cudaError_t launch_stream_one(const Problem& pb, const StreamPlan& plan, cudaStr
     a.cw = pb.cw;
     a.wdenom = pb.wdenom;
     a.wsum = pb.wsum;
-    const size_t smem = (size_t)plan.stages * a.tile_bytes + 24 * sizeof(uint64_t) +
+    // rows handed out by a shared counter while row indices fit it
+    a.row_claim = pb.N < (int64_t)0x7fffffff ? pb.row_claim : nullptr;
+    a.row_done = pb.row_done;
+    const size_t smem = (size_t)plan.stages * a.tile_bytes + (24 + 3 * kRowQ) * sizeof(uint64_t) +
                         2 * NW * sizeof(float4) + (2 + 2 * NW) * sizeof(float) + 2 * sizeof(int) + 16;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
