@@ -310,7 +310,7 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
                 }
                 return (int64_t)gridDim.x + (int64_t)atomicAdd(p.row_claim, 1u);
             };
-            int64_t r = blockIdx.x;
+            int64_t r = blockIdx.x, n1 = -1, n2 = -1;  // this row, the two claimed after it
             for (int k = 0; !*abort_flag; ++k) {
                 // hand the row (or the end mark -1) to the consumer warps
                 if (!mbar_wait_bounded(&qempty[qr.s], qr.ph ^ 1u)) {
@@ -323,10 +323,10 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
                 mbar_arrive(&qfull[qr.s]);
                 qr.next();
                 if (r >= p.N) break;
-                // claim the successor ahead of this row's copies, so the atomic's
-                // latency hides behind them; the first claim waits for the count
-                // kernel, so it follows the first row's copies instead
-                int64_t next = k > 0 ? claim(r) : -1;
+                // claims run two rows ahead, each issued before a row's copies so
+                // that the atomic's latency hides behind them; the first claims
+                // wait for the count kernel, so they follow the first row's copies
+                if (k > 0) n2 = claim(n1);
                 const bool loaded = is_loaded(row_target(r));
                 const char* row = row_ptr(r);
                 for (int pass = 0; loaded && pass < npass && !*abort_flag; ++pass) {
@@ -369,8 +369,12 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
                         }
                     }
                 }
-                if (k == 0) next = claim(r);
-                r = next;
+                if (k == 0) {
+                    n1 = claim(r);
+                    n2 = claim(n1);
+                }
+                r = n1;  // claims from one CTA only grow: past N, all later ones are too
+                n1 = n2;
             }
             if (*abort_flag) {
                 // let every copy already issued land before the CTA goes away
