@@ -310,26 +310,43 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
                 }
                 return (int64_t)gridDim.x + (int64_t)atomicAdd(p.row_claim, 1u);
             };
-            int64_t r = blockIdx.x, n1 = -1, n2 = -1;  // this row, the two claimed after it
-            for (int k = 0; !*abort_flag; ++k) {
-                // hand the row (or the end mark -1) to the consumer warps
+            // hand a row (or the end mark -1 for any index past the last row)
+            // to the consumer warps; false when the queue stays full too long
+            auto publish = [&](int64_t row) -> bool {
                 if (!mbar_wait_bounded(&qempty[qr.s], qr.ph ^ 1u)) {
-                    griddep_wait();
+                    griddep_wait();  // the count kernel starts the error word
                     atomicOr(p.err, CE_DEVERR_TIMEOUT);
                     *abort_flag = 1;
-                    break;
+                    return false;
                 }
-                rowq[qr.s] = r < p.N ? r : -1;
+                rowq[qr.s] = row < p.N ? row : -1;
                 mbar_arrive(&qfull[qr.s]);
                 qr.next();
-                if (r >= p.N) break;
-                // claims run two rows ahead, each issued before a row's copies so
-                // that the atomic's latency hides behind them; the first claims
-                // wait for the count kernel, so they follow the first row's copies
-                if (k > 0) n2 = claim(n1);
+                return true;
+            };
+            // The queue runs one row ahead of the copies: the row after this one
+            // is published before this row's copies (for the first row, before
+            // its gradient pass: the first claims wait for the count kernel),
+            // so the consumers can read it while they work on this row.  Claims
+            // run two rows ahead, each one row before it is needed.
+            int64_t r = blockIdx.x, n1 = -1, n2 = -1;  // this row, the two claimed after it
+            publish(r);
+            for (int k = 0; !*abort_flag; ++k) {
+                bool succ = false;  // the next row published
+                if (k > 0) {
+                    n2 = claim(n1);
+                    succ = publish(n1);
+                    if (!succ) break;
+                }
                 const bool loaded = is_loaded(row_target(r));
                 const char* row = row_ptr(r);
                 for (int pass = 0; loaded && pass < npass && !*abort_flag; ++pass) {
+                    if (pass == 1 && !succ) {
+                        n1 = claim(r);
+                        n2 = claim(n1);
+                        succ = publish(n1);
+                        if (!succ) break;
+                    }
                     for (int t = 0; t < p.ntiles; ++t) {
                         if (!mbar_wait_bounded(&empty[rg.s], rg.ph ^ 1u)) {
                             griddep_wait();  // the count kernel starts the error word
@@ -369,12 +386,14 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
                         }
                     }
                 }
-                if (k == 0) {
+                if (!succ && !*abort_flag) {  // a first row without a gradient pass
                     n1 = claim(r);
                     n2 = claim(n1);
+                    if (!publish(n1)) break;
                 }
                 r = n1;  // claims from one CTA only grow: past N, all later ones are too
                 n1 = n2;
+                if (r >= p.N) break;  // its end mark is already in the queue
             }
             if (*abort_flag) {
                 // let every copy already issued land before the CTA goes away
@@ -412,25 +431,32 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
         if (lane == 0) mbar_arrive(&empty[rg.s]);
         rg.next();
     };
+    // Rows come from the producer warp's queue, one entry ahead: each row's
+    // successor is read before the row's CTA combine, and that barrier (a
+    // reduction) also decides for every consumer warp at once whether the
+    // successor is taken -- so all of them run the same rows and barriers,
+    // and rows still overlap at their boundaries.
     Ring qr(kRowQ);
-    for (;;) {
-        // the next row from the producer warp; the consumer warps take the
-        // exit decision together (a barrier reduction), so every one of them
-        // runs the same rows and the same barriers
-        int64_t r = -1;
-        bool got = false;
+    // the next entry: a row, -1 past the last row, -2 when the wait gave up
+    auto next_row = [&]() -> int64_t {
+        int64_t v = -2;
         if (!*abort_flag) {
-            got = mbar_wait_bounded(&qfull[qr.s], qr.ph);
-            if (!got) {
+            const bool got = __all_sync(kFull, mbar_wait_bounded(&qfull[qr.s], qr.ph));
+            if (got) {
+                v = rowq[qr.s];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&qempty[qr.s]);
+            } else {
                 atomicOr(p.err, CE_DEVERR_TIMEOUT);
                 *abort_flag = 1;
             }
         }
-        if (got) r = rowq[qr.s];
-        __syncwarp();
-        if (got && lane == 0) mbar_arrive(&qempty[qr.s]);
         qr.next();
-        if (named_bar_or(1, NC, r < 0 || *abort_flag)) break;
+        return v;
+    };
+    int64_t r = next_row();
+    bool stop = named_bar_or(1, NC, r < 0 || *abort_flag);
+    while (!stop) {
         const int64_t y = row_target(r);
         char* rowp = row_ptr(r);
         if (!is_loaded(y)) {
@@ -443,6 +469,9 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
                 p.loss[r] = (y == p.ignore_idx) ? 0.f : __int_as_float(0x7fc00000);
                 if (p.lse_out) p.lse_out[r] = __int_as_float(0x7fc00000);
             }
+            const int64_t nx = next_row();
+            stop = named_bar_or(1, NC, nx < 0 || *abort_flag);
+            r = nx;
             continue;
         }
         const float g = p.reduce ? g_reduce : (p.dloss ? __ldg(p.dloss + r) : 1.f);
@@ -466,10 +495,12 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
             release();
         }
 
-        // CTA combine, fixed order
+        // the successor (published before this row's copies)
+        const int64_t nx = next_row();
+        // CTA combine, fixed order; its barrier takes the exit decision
         Part q = warp_allreduce_part(Part{m, d2.x + d2.y, s2.x + s2.y});
         if (lane == 0) red[par * NW + warp] = make_float4(q.m, q.d, q.S, 0.f);
-        named_bar_sync(1, NC);
+        stop = named_bar_or(1, NC, nx < 0 || *abort_flag);
         Part G = part_identity();
 #pragma unroll
         for (int w = 0; w < NW; ++w) {
@@ -557,6 +588,7 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
             }
         }
         par ^= 1;
+        r = nx;
     }
 
     // the last CTA done claiming rows zeroes the row counter for the next pass
