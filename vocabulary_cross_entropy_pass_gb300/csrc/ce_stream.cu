@@ -299,16 +299,16 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
             Ring qr(kRowQ);
             uint32_t issued = 0;
             bool counted = false;
-            // rows: the CTA's own first row, then rows claimed from the shared
-            // counter (the count kernel zeroes it), or without a counter every
-            // gridDim.x-th row
+            // rows: the CTA's own two first rows (blockIdx.x and blockIdx.x +
+            // gridDim.x), then rows claimed from the shared counter (the count
+            // kernel zeroes it), or without a counter every gridDim.x-th row
             auto claim = [&](int64_t cur) -> int64_t {
                 if (!p.row_claim) return cur + gridDim.x;
                 if (!counted) {
                     griddep_wait();
                     counted = true;
                 }
-                return (int64_t)gridDim.x + (int64_t)atomicAdd(p.row_claim, 1u);
+                return 2 * (int64_t)gridDim.x + (int64_t)atomicAdd(p.row_claim, 1u);
             };
             // hand a row (or the end mark -1 for any index past the last row)
             // to the consumer warps; false when the queue stays full too long
@@ -325,27 +325,26 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
                 return true;
             };
             // The queue runs one row ahead of the copies: the row after this one
-            // is published before this row's copies (for the first row, before
-            // its gradient pass: the first claims wait for the count kernel),
-            // so the consumers can read it while they work on this row.  Claims
-            // run two rows ahead, each one row before it is needed.
-            int64_t r = blockIdx.x, n1 = -1, n2 = -1;  // this row, the two claimed after it
+            // is published before this row's copies, so the consumers can read
+            // it while they work on this row.  The claim of the row after that
+            // is issued before this row's copies too, so its latency hides
+            // behind them; on the first row it follows the first pass's copies
+            // (the first claim waits for the count kernel).
+            int64_t r = blockIdx.x, n1 = r + gridDim.x, n2 = -1;  // this row, the next two
             publish(r);
             for (int k = 0; !*abort_flag; ++k) {
-                bool succ = false;  // the next row published
+                if (!publish(n1)) break;
+                bool claimed = false;
                 if (k > 0) {
                     n2 = claim(n1);
-                    succ = publish(n1);
-                    if (!succ) break;
+                    claimed = true;
                 }
                 const bool loaded = is_loaded(row_target(r));
                 const char* row = row_ptr(r);
                 for (int pass = 0; loaded && pass < npass && !*abort_flag; ++pass) {
-                    if (pass == 1 && !succ) {
-                        n1 = claim(r);
+                    if (pass == 1 && !claimed) {
                         n2 = claim(n1);
-                        succ = publish(n1);
-                        if (!succ) break;
+                        claimed = true;
                     }
                     for (int t = 0; t < p.ntiles; ++t) {
                         if (!mbar_wait_bounded(&empty[rg.s], rg.ph ^ 1u)) {
@@ -386,12 +385,8 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
                         }
                     }
                 }
-                if (!succ && !*abort_flag) {  // a first row without a gradient pass
-                    n1 = claim(r);
-                    n2 = claim(n1);
-                    if (!publish(n1)) break;
-                }
-                r = n1;  // claims from one CTA only grow: past N, all later ones are too
+                if (!claimed) n2 = claim(n1);  // a first row without a gradient pass
+                r = n1;  // one CTA's rows only grow: past N, all later ones are too
                 n1 = n2;
                 if (r >= p.N) break;  // its end mark is already in the queue
             }
