@@ -302,22 +302,13 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
             // rows: the CTA's own two first rows (blockIdx.x and blockIdx.x +
             // gridDim.x), then rows claimed from the shared counter (the count
             // kernel zeroes it), or without a counter every gridDim.x-th row
-            // A claim is issued one row before its value is read: claim_issue()
-            // starts the atomic, claim_row() turns its result into a row index
-            // (the empty asm keeps that read where it is written).
-            uint32_t pend = 0;
-            auto claim_issue = [&]() {
-                if (!p.row_claim) return;
+            auto claim = [&](int64_t cur) -> int64_t {
+                if (!p.row_claim) return cur + gridDim.x;
                 if (!counted) {
                     griddep_wait();
                     counted = true;
                 }
-                pend = atomicAdd(p.row_claim, 1u);
-            };
-            auto claim_row = [&](int64_t prev) -> int64_t {
-                if (!p.row_claim) return prev + gridDim.x;
-                asm volatile("" : "+r"(pend));
-                return 2 * (int64_t)gridDim.x + (int64_t)pend;
+                return 2 * (int64_t)gridDim.x + (int64_t)atomicAdd(p.row_claim, 1u);
             };
             // hand a row (or the end mark -1 for any index past the last row)
             // to the consumer warps; false when the queue stays full too long
@@ -339,23 +330,20 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
             // is issued before this row's copies too, so its latency hides
             // behind them; on the first row it follows the first pass's copies
             // (the first claim waits for the count kernel).
-            int64_t r = blockIdx.x, n1 = r + gridDim.x;  // this row and the next
-            int64_t yr = row_target(r);                  // this row's target
+            int64_t r = blockIdx.x, n1 = r + gridDim.x, n2 = -1;  // this row, the next two
             publish(r);
             for (int k = 0; !*abort_flag; ++k) {
                 if (!publish(n1)) break;
                 bool claimed = false;
                 if (k > 0) {
-                    claim_issue();
+                    n2 = claim(n1);
                     claimed = true;
                 }
-                // the next row's target, read now and used one row later
-                const int64_t ynext = n1 < p.N ? row_target(n1) : 0;
-                const bool loaded = is_loaded(yr);
+                const bool loaded = is_loaded(row_target(r));
                 const char* row = row_ptr(r);
                 for (int pass = 0; loaded && pass < npass && !*abort_flag; ++pass) {
                     if (pass == 1 && !claimed) {
-                        claim_issue();
+                        n2 = claim(n1);
                         claimed = true;
                     }
                     for (int t = 0; t < p.ntiles; ++t) {
@@ -397,11 +385,9 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
                         }
                     }
                 }
-                if (!claimed) claim_issue();  // a first row without a gradient pass
-                const int64_t n2 = claim_row(n1);
+                if (!claimed) n2 = claim(n1);  // a first row without a gradient pass
                 r = n1;  // one CTA's rows only grow: past N, all later ones are too
                 n1 = n2;
-                yr = ynext;
                 if (r >= p.N) break;  // its end mark is already in the queue
             }
             if (*abort_flag) {
@@ -464,9 +450,9 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
         return v;
     };
     int64_t r = next_row();
-    int64_t y = r >= 0 ? row_target(r) : 0;
     bool stop = named_bar_or(1, NC, r < 0 || *abort_flag);
     while (!stop) {
+        const int64_t y = row_target(r);
         char* rowp = row_ptr(r);
         if (!is_loaded(y)) {
             if (GRAD) {
@@ -479,10 +465,8 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
                 if (p.lse_out) p.lse_out[r] = __int_as_float(0x7fc00000);
             }
             const int64_t nx = next_row();
-            const int64_t ny = nx >= 0 ? row_target(nx) : 0;
             stop = named_bar_or(1, NC, nx < 0 || *abort_flag);
             r = nx;
-            y = ny;
             continue;
         }
         const float g = p.reduce ? g_reduce : (p.dloss ? __ldg(p.dloss + r) : 1.f);
@@ -506,9 +490,8 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
             release();
         }
 
-        // the successor (published before this row's copies) and its target
+        // the successor (published before this row's copies)
         const int64_t nx = next_row();
-        const int64_t ny = nx >= 0 ? row_target(nx) : 0;
         // CTA combine, fixed order; its barrier takes the exit decision
         Part q = warp_allreduce_part(Part{m, d2.x + d2.y, s2.x + s2.y});
         if (lane == 0) red[par * NW + warp] = make_float4(q.m, q.d, q.S, 0.f);
@@ -601,7 +584,6 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
         }
         par ^= 1;
         r = nx;
-        y = ny;
     }
 
     // the last CTA done claiming rows zeroes the row counter for the next pass
