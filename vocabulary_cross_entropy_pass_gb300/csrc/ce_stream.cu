@@ -1,7 +1,11 @@
 // ce_stream.cu -- the row-streaming fused cross-entropy kernel.
 //
-// One CTA owns whole token rows (a persistent grid walks rows r = cta,
-// cta + grid, ...), so no CTA ever waits for another.  Each row goes twice
+// One CTA owns whole token rows, so no CTA ever waits for another: a
+// persistent grid, each CTA starting on rows cta and cta + grid and then
+// claiming the next unclaimed row from a counter in the workspace, so the CTAs
+// finish together although ignored rows (no read) fall unevenly among them.
+// The producer warp claims rows and hands them, with their targets, to the
+// consumer warps through a small queue in shared memory.  Each row goes twice
 // through a ring of shared-memory tiles fed by 1-D TMA bulk copies:
 //
 //   pass 1 (statistics): a running (max m, sum-exp d, sum S) per thread, the
@@ -248,8 +252,9 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
     uint64_t* empty = full + 12;
     uint64_t* qfull = empty + 12;    // row queue: entry written
     uint64_t* qempty = qfull + kRowQ;  // row queue: entry read by every consumer warp
-    int64_t* rowq = reinterpret_cast<int64_t*>(qempty + kRowQ);
-    float4* red = reinterpret_cast<float4*>(rowq + kRowQ);  // [2][NW]
+    int64_t* rowq = reinterpret_cast<int64_t*>(qempty + kRowQ);  // row index
+    int64_t* yq = rowq + kRowQ;                                   // its target
+    float4* red = reinterpret_cast<float4*>(yq + kRowQ);  // [2][NW]
     float* xy_s = reinterpret_cast<float*>(red + 2 * NW);  // [2]
     float* sw_s = xy_s + 2;                                 // [2][NW] weighted sums
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sw_s + 2 * NW);
@@ -312,7 +317,7 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
             };
             // hand a row (or the end mark -1 for any index past the last row)
             // to the consumer warps; false when the queue stays full too long
-            auto publish = [&](int64_t row) -> bool {
+            auto publish = [&](int64_t row, int64_t y) -> bool {
                 if (!mbar_wait_bounded(&qempty[qr.s], qr.ph ^ 1u)) {
                     griddep_wait();  // the count kernel starts the error word
                     atomicOr(p.err, CE_DEVERR_TIMEOUT);
@@ -320,6 +325,7 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
                     return false;
                 }
                 rowq[qr.s] = row < p.N ? row : -1;
+                yq[qr.s] = y;
                 mbar_arrive(&qfull[qr.s]);
                 qr.next();
                 return true;
@@ -330,16 +336,20 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
             // is issued before this row's copies too, so its latency hides
             // behind them; on the first row it follows the first pass's copies
             // (the first claim waits for the count kernel).
+            // Each entry carries the row's target, read here once for the
+            // consumer warps as well.
             int64_t r = blockIdx.x, n1 = r + gridDim.x, n2 = -1;  // this row, the next two
-            publish(r);
+            int64_t yr = row_target(r);
+            publish(r, yr);
             for (int k = 0; !*abort_flag; ++k) {
-                if (!publish(n1)) break;
+                const int64_t y1 = n1 < p.N ? row_target(n1) : 0;
+                if (!publish(n1, y1)) break;
                 bool claimed = false;
                 if (k > 0) {
                     n2 = claim(n1);
                     claimed = true;
                 }
-                const bool loaded = is_loaded(row_target(r));
+                const bool loaded = is_loaded(yr);
                 const char* row = row_ptr(r);
                 for (int pass = 0; loaded && pass < npass && !*abort_flag; ++pass) {
                     if (pass == 1 && !claimed) {
@@ -387,6 +397,7 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
                 }
                 if (!claimed) n2 = claim(n1);  // a first row without a gradient pass
                 r = n1;  // one CTA's rows only grow: past N, all later ones are too
+                yr = y1;
                 n1 = n2;
                 if (r >= p.N) break;  // its end mark is already in the queue
             }
@@ -432,13 +443,16 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
     // successor is taken -- so all of them run the same rows and barriers,
     // and rows still overlap at their boundaries.
     Ring qr(kRowQ);
-    // the next entry: a row, -1 past the last row, -2 when the wait gave up
-    auto next_row = [&]() -> int64_t {
+    // the next entry: a row, -1 past the last row, -2 when the wait gave up;
+    // yout gets the row's target
+    auto next_row = [&](int64_t& yout) -> int64_t {
         int64_t v = -2;
+        yout = 0;
         if (!*abort_flag) {
             const bool got = __all_sync(kFull, mbar_wait_bounded(&qfull[qr.s], qr.ph));
             if (got) {
                 v = rowq[qr.s];
+                yout = yq[qr.s];
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&qempty[qr.s]);
             } else {
@@ -449,10 +463,10 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
         qr.next();
         return v;
     };
-    int64_t r = next_row();
+    int64_t y;
+    int64_t r = next_row(y);
     bool stop = named_bar_or(1, NC, r < 0 || *abort_flag);
     while (!stop) {
-        const int64_t y = row_target(r);
         char* rowp = row_ptr(r);
         if (!is_loaded(y)) {
             if (GRAD) {
@@ -464,9 +478,11 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
                 p.loss[r] = (y == p.ignore_idx) ? 0.f : __int_as_float(0x7fc00000);
                 if (p.lse_out) p.lse_out[r] = __int_as_float(0x7fc00000);
             }
-            const int64_t nx = next_row();
+            int64_t ny;
+            const int64_t nx = next_row(ny);
             stop = named_bar_or(1, NC, nx < 0 || *abort_flag);
             r = nx;
+            y = ny;
             continue;
         }
         const float g = p.reduce ? g_reduce : (p.dloss ? __ldg(p.dloss + r) : 1.f);
@@ -491,7 +507,8 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
         }
 
         // the successor (published before this row's copies)
-        const int64_t nx = next_row();
+        int64_t ny;
+        const int64_t nx = next_row(ny);
         // CTA combine, fixed order; its barrier takes the exit decision
         Part q = warp_allreduce_part(Part{m, d2.x + d2.y, s2.x + s2.y});
         if (lane == 0) red[par * NW + warp] = make_float4(q.m, q.d, q.S, 0.f);
@@ -584,6 +601,7 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
         }
         par ^= 1;
         r = nx;
+        y = ny;
     }
 
     // the last CTA done claiming rows zeroes the row counter for the next pass
@@ -664,7 +682,7 @@ cudaError_t launch_stream_one(const Problem& pb, const StreamPlan& plan, cudaStr
     // rows handed out by a shared counter while row indices fit it
     a.row_claim = pb.N < (int64_t)0x7fffffff ? pb.row_claim : nullptr;
     a.row_done = pb.row_done;
-    const size_t smem = (size_t)plan.stages * a.tile_bytes + (24 + 3 * kRowQ) * sizeof(uint64_t) +
+    const size_t smem = (size_t)plan.stages * a.tile_bytes + (24 + 4 * kRowQ) * sizeof(uint64_t) +
                         2 * NW * sizeof(float4) + (2 + 2 * NW) * sizeof(float) + 2 * sizeof(int) + 16;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
