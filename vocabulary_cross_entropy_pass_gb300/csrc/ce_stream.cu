@@ -339,21 +339,26 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
             // Each entry carries the row's target, read here once for the
             // consumer warps as well.
             int64_t r = blockIdx.x, n1 = r + gridDim.x, n2 = -1;  // this row, the next two
-            int64_t yr = row_target(r);
+            int64_t yr = row_target(r), y1 = n1 < p.N ? row_target(n1) : 0, y2 = 0;
+            // a claimed row's target is read as soon as the row is known, one
+            // row before it is published
+            auto claim_y = [&]() {
+                n2 = claim(n1);
+                y2 = n2 < p.N ? row_target(n2) : 0;
+            };
             publish(r, yr);
             for (int k = 0; !*abort_flag; ++k) {
-                const int64_t y1 = n1 < p.N ? row_target(n1) : 0;
                 if (!publish(n1, y1)) break;
                 bool claimed = false;
                 if (k > 0) {
-                    n2 = claim(n1);
+                    claim_y();
                     claimed = true;
                 }
                 const bool loaded = is_loaded(yr);
                 const char* row = row_ptr(r);
                 for (int pass = 0; loaded && pass < npass && !*abort_flag; ++pass) {
                     if (pass == 1 && !claimed) {
-                        n2 = claim(n1);
+                        claim_y();
                         claimed = true;
                     }
                     for (int t = 0; t < p.ntiles; ++t) {
@@ -395,10 +400,11 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
                         }
                     }
                 }
-                if (!claimed) n2 = claim(n1);  // a first row without a gradient pass
+                if (!claimed) claim_y();  // a first row without a gradient pass
                 r = n1;  // one CTA's rows only grow: past N, all later ones are too
                 yr = y1;
                 n1 = n2;
+                y1 = y2;
                 if (r >= p.N) break;  // its end mark is already in the queue
             }
             if (*abort_flag) {
