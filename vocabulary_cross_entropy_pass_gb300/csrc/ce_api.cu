@@ -37,14 +37,14 @@ struct Plan {
 bool plan_rows(int64_t row_bytes, const ce_options* o, RowsPlan* rp) {
     rp->tile_kb = (o && o->tune_tile_kb) ? o->tune_tile_kb : (row_bytes <= 16 * 1024 ? 16 : 32);
     if (row_bytes > (int64_t)rp->tile_kb * 1024) return false;
-    // one tile per warp: 96 KB (16 KB tiles, two CTAs per SM) or 192 KB (32 KB)
-    rp->stages = (o && o->tune_stages) ? o->tune_stages : 6;
+    // 16 KB tiles: two per warp (192 KB, one CTA per SM), so a warp's next
+    // row lands while it works on this one; 32 KB tiles: one per warp (192 KB)
+    rp->stages = (o && o->tune_stages) ? o->tune_stages : (rp->tile_kb == 16 ? 12 : 6);
     if (rp->stages % 6 != 0) return false;
     rp->ctas_per_sm_cap = o ? o->tune_ctas_per_sm : 0;
     return rp->stages * (size_t)rp->tile_kb * 1024 + 1024 <= kSmemLimit;
 }
 
-// Row-streaming kernel: tiles of threads*64 bytes, `stages` of them in flight.
 // Row-streaming kernel: tiles of 16 or 32 KB consumed by 256 or 512 threads,
 // `stages` of them in flight.  Defaults from sweeps over V = 32000 .. 256000
 // bf16 (32 KB x 5 was best or within 2% of best at every width).
