@@ -9,12 +9,10 @@
 //     tile of the warp that will take it (rows of ignored targets are not read:
 //     the producer warp writes their zero gradient itself);
 //   - consumer warp w takes the kept rows w, w + NW, w + 2 NW, ... of its CTA
-//     and makes two sweeps over the tile in shared memory: per lane a running
-//     max with the sum of 2^((x - m) log2e) and the plain sum (the online
-//     softmax update, one rescale per batch of vectors with a new max; a
-//     butterfly combines the lanes: lse = m + log d, CSDN "Ascend CANN ops-nn
-//     cross-entropy fusion", pitfall 1), then the gradient g (softmax - a/V) -
-//     g (1-a) [j == y]
+//     and makes three sweeps over the tile in shared memory: the row max, the
+//     sum of 2^((x - m) log2e) and the plain sum (warp shuffles combine the
+//     lanes: lse = m + log d, CSDN "Ascend CANN ops-nn cross-entropy fusion",
+//     pitfall 1), then the gradient g (softmax - a/V) - g (1-a) [j == y]
 //     (same article, "Backward", pitfall 3, smoothing over V) stored in place
 //     over the row (TENPU #29 section 6) with 16-byte streaming stores.
 //
@@ -60,7 +58,6 @@ __device__ __forceinline__ uint64_t l2_evict_first() {
 }
 
 constexpr int kRowsWarps = 6;  // consumer warps per CTA
-constexpr int kRowsBatch = 4;  // 16-byte vectors per lane per step of the first sweep
 
 template <typename T, int NW, int TB, bool GRAD>
 __global__ void __launch_bounds__(NW * 32 + 32, 1)
@@ -212,49 +209,30 @@ ce_rows_kernel(const __grid_constant__ RowsArgs p) {
         const uint4* tile = reinterpret_cast<const uint4*>(ring + (size_t)s * TB);
         const float g = p.reduce ? g_reduce : (p.dloss ? __ldg(p.dloss + r) : 1.f);
 
-        // sweep 1: per lane a running max, sum of 2^((x - m) log2e) and sum of
-        // x over its vectors, kRowsBatch at a time (one rescale per batch with
-        // a new max), then the lanes' partials combined in a fixed butterfly
-        float m = -INFINITY;
+        // sweep 1: row max (packed pairs), warp-wide
+        typename VT::Max pm = VT::max_init();
+#pragma unroll 4
+        for (int v = lane; v < nvec; v += 32) pm = VT::max_acc(pm, tile[v]);
+        const float m = warp_allmax(VT::max_done(pm));
+        const float nml = -m * kLog2e;
+        const float2 NM = make_float2(nml, nml);
+
+        // sweep 2: sum of 2^((x - m) log2e) and of x, packed f32x2
         float2 d2 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
-        for (int v0 = lane; v0 < nvec; v0 += 32 * kRowsBatch) {
-            uint4 raw[kRowsBatch];
-            typename VT::Max bm = VT::max_init();
+#pragma unroll 4
+        for (int v = lane; v < nvec; v += 32) {
+            float2 x[P];
+            VT::unpack2(tile[v], x);
 #pragma unroll
-            for (int b = 0; b < kRowsBatch; ++b) {
-                if (v0 + 32 * b < nvec) {
-                    raw[b] = tile[v0 + 32 * b];
-                    bm = VT::max_acc(bm, raw[b]);
-                }
-            }
-            const float bmf = VT::max_done(bm);
-            if (bmf > m) {
-                if (m != -INFINITY) {
-                    const float c = ex2_approx((m - bmf) * kLog2e);
-                    d2.x *= c;
-                    d2.y *= c;
-                }
-                m = bmf;
-            }
-            const float nml = -m * kLog2e;
-            const float2 NM = make_float2(nml, nml);
-#pragma unroll
-            for (int b = 0; b < kRowsBatch; ++b) {
-                if (v0 + 32 * b < nvec) {
-                    float2 x[P];
-                    VT::unpack2(raw[b], x);
-#pragma unroll
-                    for (int j = 0; j < P; ++j) {
-                        const float2 e = __ffma2_rn(x[j], L2, NM);
-                        d2 = __fadd2_rn(d2, make_float2(ex2_approx(e.x), ex2_approx(e.y)));
-                        s2 = __fadd2_rn(s2, x[j]);
-                    }
-                }
+            for (int j = 0; j < P; ++j) {
+                const float2 e = __ffma2_rn(x[j], L2, NM);
+                d2 = __fadd2_rn(d2, make_float2(ex2_approx(e.x), ex2_approx(e.y)));
+                s2 = __fadd2_rn(s2, x[j]);
             }
         }
-        const Part q = warp_allreduce_part(Part{m, d2.x + d2.y, s2.x + s2.y});
-        const float S = (p.a != 0.f) ? q.S : 0.f;  // no 0 * inf without smoothing
-        const float lse = q.m + logf(q.d);
+        const float d = warp_allsum(d2.x + d2.y);
+        const float S = (p.a != 0.f) ? warp_allsum(s2.x + s2.y) : 0.f;
+        const float lse = m + logf(d);
         const float xy = VT::load1(reinterpret_cast<const unsigned char*>(tile) + y * ES);
         if (lane == 0) {
             p.loss[r] = lse - (1.f - p.a) * xy - p.a_over_v * S;
