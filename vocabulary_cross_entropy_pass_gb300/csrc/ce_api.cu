@@ -53,7 +53,8 @@ bool plan_rows(int64_t row_bytes, int64_t N, const ce_options* o, RowsPlan* rp) 
 
 // Row-streaming kernel: tiles of 16 or 32 KB consumed by 256 or 512 threads,
 // `stages` of them in flight.  Defaults from sweeps over V = 32000 .. 256000
-// bf16 (32 KB x 5 was best or within 2% of best at every width).
+// bf16 (32 KB tiles and 256 threads best at every width; the ring depth is
+// chosen by the caller from the row width).
 // def_tile_kb / def_stages: the shape when the options leave it open (0:
 // 32 KB tiles 5 deep, 16 KB tiles 12 deep).
 bool plan_stream(const ce_options* o, StreamPlan* sp, int def_tile_kb = 0, int def_stages = 0) {
@@ -172,7 +173,11 @@ Plan make_plan(const Problem& p, const ce_options* o) {
     }
     const bool stream_auto = force == CE_PATH_AUTO && aligned && K == 0;
     if (force == CE_PATH_STREAM || stream_auto) {
-        if (!aligned || !plan_stream(o, &pl.stream)) {
+        // rows of four or more 32 KB tiles run a 6-deep ring (128000 bf16
+        // columns: 1.178 ms against 1.196 ms at 5), shorter ones 5 deep
+        // (32000 columns: 0.713 ms at 5, 0.715 at 6, 0.721 at 7)
+        const int def_stages = row_bytes >= 128 * 1024 ? 6 : 0;
+        if (!aligned || !plan_stream(o, &pl.stream, 0, def_stages)) {
             pl.path = -2;
             return pl;
         }
