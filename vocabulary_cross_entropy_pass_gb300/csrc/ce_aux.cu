@@ -16,6 +16,7 @@ namespace gbce {
 namespace {
 
 constexpr int kAuxThreads = 1024;
+constexpr int kAuxBatch = 8;  // loads in flight per thread
 
 __global__ void __launch_bounds__(kAuxThreads)
 ce_count_kernel(const int64_t* __restrict__ targets, int64_t ts0, int64_t ts1, int64_t dim1,
@@ -31,18 +32,43 @@ ce_count_kernel(const int64_t* __restrict__ targets, int64_t ts0, int64_t ts1, i
     long long n = 0;
     unsigned e = 0;
     double wd = 0.0, ws = 0.0;
-    for (int64_t r = threadIdx.x; r < N; r += kAuxThreads) {
-        const int64_t i = r / dim1, j = r - i * dim1;
-        const int64_t y = targets[i * ts0 + j * ts1];
-        if (y == ignore_idx) continue;
-        ++n;
-        if (y < 0 || y >= V)
-            e |= CE_DEVERR_TARGET_RANGE;
-        else if (cw)
-            wd += (double)cw[y];
+    // thread t takes rows t, t + T, t + 2T, ... in that order, kAuxBatch loads
+    // in flight at a time
+    for (int64_t r0 = threadIdx.x; r0 < N; r0 += (int64_t)kAuxThreads * kAuxBatch) {
+        int64_t yb[kAuxBatch];
+#pragma unroll
+        for (int u = 0; u < kAuxBatch; ++u) {
+            const int64_t r = r0 + (int64_t)u * kAuxThreads;
+            if (r < N) {
+                const int64_t i = r / dim1, j = r - i * dim1;
+                yb[u] = targets[i * ts0 + j * ts1];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kAuxBatch; ++u) {
+            if (r0 + (int64_t)u * kAuxThreads >= N) break;
+            const int64_t y = yb[u];
+            if (y == ignore_idx) continue;
+            ++n;
+            if (y < 0 || y >= V)
+                e |= CE_DEVERR_TARGET_RANGE;
+            else if (cw)
+                wd += (double)__ldg(cw + y);
+        }
     }
-    if (cw)
-        for (int64_t v = threadIdx.x; v < V; v += kAuxThreads) ws += (double)cw[v];
+    if (cw) {
+        for (int64_t v0 = threadIdx.x; v0 < V; v0 += (int64_t)kAuxThreads * kAuxBatch) {
+            float wb[kAuxBatch];
+#pragma unroll
+            for (int u = 0; u < kAuxBatch; ++u) {
+                const int64_t v = v0 + (int64_t)u * kAuxThreads;
+                wb[u] = v < V ? __ldg(cw + v) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < kAuxBatch; ++u)
+                if (v0 + (int64_t)u * kAuxThreads < V) ws += (double)wb[u];
+        }
+    }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
         n += __shfl_xor_sync(kFull, n, off);
@@ -87,8 +113,7 @@ __global__ void __launch_bounds__(kAuxThreads)
 ce_mean_kernel(const float* __restrict__ loss_rows, int64_t N, const int64_t* n_dev,
                const double* wdenom, float* out) {
     __shared__ double s_sum[kAuxThreads / 32];
-    double acc = 0.0;
-    for (int64_t r = threadIdx.x; r < N; r += kAuxThreads) acc += (double)loss_rows[r];
+    double acc = strided_sum_fixed(loss_rows, N, threadIdx.x, kAuxThreads);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(kFull, acc, off);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;

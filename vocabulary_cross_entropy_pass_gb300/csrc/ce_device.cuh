@@ -349,4 +349,24 @@ __device__ __forceinline__ float warp_allsum(float v) {
     return v;
 }
 
+// Sum in double of x[t], x[t + T], x[t + 2T], ... in that order (t: this
+// thread's index among T threads), eight loads in flight at a time: the first
+// level of the fixed-order mean, the same on every run.
+__device__ __forceinline__ double strided_sum_fixed(const float* x, int64_t n, int t, int T) {
+    constexpr int B = 8;
+    double acc = 0.0;
+    for (int64_t r0 = t; r0 < n; r0 += (int64_t)T * B) {
+        float v[B];
+#pragma unroll
+        for (int u = 0; u < B; ++u) {
+            const int64_t r = r0 + (int64_t)u * T;
+            v[u] = r < n ? __ldcg(x + r) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < B; ++u)
+            if (r0 + (int64_t)u * T < n) acc += (double)v[u];
+    }
+    return acc;
+}
+
 }  // namespace gbce

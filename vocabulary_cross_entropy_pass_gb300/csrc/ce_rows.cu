@@ -283,8 +283,7 @@ ce_rows_kernel(const __grid_constant__ RowsArgs p) {
         asm volatile("bar.sync 2, %0;" ::"r"(NW * 32) : "memory");
         if (flags[1]) {
             __threadfence();
-            double acc = 0.0;
-            for (int64_t r = tid; r < p.N; r += NW * 32) acc += (double)__ldcg(p.loss + r);
+            double acc = strided_sum_fixed(p.loss, p.N, tid, NW * 32);
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(kFull, acc, off);
             if (lane == 0) dred[warp] = acc;

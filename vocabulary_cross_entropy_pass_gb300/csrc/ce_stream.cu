@@ -634,8 +634,7 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
         named_bar_sync(1, NC);
         if (*last_flag) {
             __threadfence();
-            double acc = 0.0;
-            for (int64_t r = tid; r < p.N; r += NC) acc += (double)__ldcg(p.loss + r);
+            double acc = strided_sum_fixed(p.loss, p.N, tid, NC);
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(kFull, acc, off);
             double* dred = reinterpret_cast<double*>(red);
