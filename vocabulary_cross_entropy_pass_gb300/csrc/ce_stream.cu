@@ -421,28 +421,19 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
     }
 
     // ------------------------------------------------------------ consumer warps
-    // The count kernel before this one may still run.  Its outputs (n, the
-    // class-weight sums, the error word and the counters it zeroes) are first
-    // needed after the first row's statistics pass, so the consumers wait for
-    // it there -- or before touching the error word, if a wait gives up
-    // earlier -- and the first pass overlaps it.
-    bool counted = false;
-    float g_reduce = 1.f, wsum = 0.f;
-    auto ensure_count = [&]() {
-        if (counted) return;
-        griddep_wait();
-        counted = true;
-        // the mean divides by the number of kept rows, or (weighted) by their
-        // summed target weight
-        if (p.reduce)
-            g_reduce = (p.dloss ? __ldg(p.dloss) : 1.f) / (WT ? (float)(*p.wdenom) : (float)(*p.n_dev));
-        if (WT) wsum = (float)(*p.wsum);
-    };
+    // the count kernel before this one may still run: wait for n and the
+    // error word (the producer's first copies are already in flight)
+    griddep_wait();
+    // the mean divides by the number of kept rows, or (weighted) by their
+    // summed target weight
+    float g_reduce = 1.f;
+    if (p.reduce)
+        g_reduce = (p.dloss ? __ldg(p.dloss) : 1.f) / (WT ? (float)(*p.wdenom) : (float)(*p.n_dev));
+    const float wsum = WT ? (float)(*p.wsum) : 0.f;
     Ring rg(p.stages);
     int par = 0;
     auto wait_full = [&]() {
         if (!*abort_flag && !mbar_wait_bounded(&full[rg.s], rg.ph)) {
-            ensure_count();
             atomicOr(p.err, CE_DEVERR_TIMEOUT);
             *abort_flag = 1;
         }
@@ -471,7 +462,6 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&qempty[qr.s]);
             } else {
-                ensure_count();
                 atomicOr(p.err, CE_DEVERR_TIMEOUT);
                 *abort_flag = 1;
             }
@@ -501,6 +491,7 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
             y = ny;
             continue;
         }
+        const float g = p.reduce ? g_reduce : (p.dloss ? __ldg(p.dloss + r) : 1.f);
         const int64_t ybyte = y * ES;
         const int ty = (int)(ybyte / TB);                 // tile holding the target
         const int yv = (int)((ybyte - (int64_t)ty * TB) / 16);  // its vector in that tile
@@ -537,8 +528,6 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
         const float lse = G.m + logf(G.d);
         const float xy = xy_s[par];
         const float wy = WT ? __ldg(p.cw + y) : 1.f;
-        ensure_count();  // n and the weight sums from here on
-        const float g = p.reduce ? g_reduce : (p.dloss ? __ldg(p.dloss + r) : 1.f);
         if (!(WT && GRAD) && tid == 0) {
             // weighted: (1-a) w_y (lse - x_y) + (a/V) (W lse - sum_j w_j x_j)
             p.loss[r] = WT ? (1.f - p.a) * wy * (lse - xy) + p.a_over_v * (wsum * lse - G.S)
@@ -621,7 +610,6 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
         y = ny;
     }
 
-    ensure_count();  // the counters below are zeroed by the count kernel
     // the last CTA done claiming rows zeroes the row counter for the next pass
     // (its rows were all claimed before the end mark this CTA has read)
     if (p.row_claim && tid == 0) {
