@@ -58,7 +58,6 @@ __device__ __forceinline__ uint64_t l2_evict_first() {
 }
 
 constexpr int kRowsWarps = 6;  // consumer warps per CTA
-constexpr int kRowsAcc = 4;    // independent running maxima / partial sums per lane
 
 template <typename T, int NW, int TB, bool GRAD>
 __global__ void __launch_bounds__(NW * 32 + 32, 1)
@@ -210,54 +209,29 @@ ce_rows_kernel(const __grid_constant__ RowsArgs p) {
         const uint4* tile = reinterpret_cast<const uint4*>(ring + (size_t)s * TB);
         const float g = p.reduce ? g_reduce : (p.dloss ? __ldg(p.dloss + r) : 1.f);
 
-        // sweep 1: row max (packed pairs), warp-wide, kRowsAcc running maxima
-        typename VT::Max pm[kRowsAcc];
-#pragma unroll
-        for (int k = 0; k < kRowsAcc; ++k) pm[k] = VT::max_init();
-        for (int v0 = lane; v0 < nvec; v0 += 32 * kRowsAcc) {
-#pragma unroll
-            for (int k = 0; k < kRowsAcc; ++k)
-                if (v0 + 32 * k < nvec) pm[k] = VT::max_acc(pm[k], tile[v0 + 32 * k]);
-        }
-        float mt = VT::max_done(pm[0]);
-#pragma unroll
-        for (int k = 1; k < kRowsAcc; ++k) mt = fmaxf(mt, VT::max_done(pm[k]));
-        const float m = warp_allmax(mt);
+        // sweep 1: row max (packed pairs), warp-wide
+        typename VT::Max pm = VT::max_init();
+#pragma unroll 4
+        for (int v = lane; v < nvec; v += 32) pm = VT::max_acc(pm, tile[v]);
+        const float m = warp_allmax(VT::max_done(pm));
         const float nml = -m * kLog2e;
         const float2 NM = make_float2(nml, nml);
 
-        // sweep 2: sum of 2^((x - m) log2e) and of x, packed f32x2, in
-        // kRowsAcc independent accumulators (vector k of each group of
-        // kRowsAcc goes to accumulator k; they are added in order at the end)
-        float2 d2[kRowsAcc], s2[kRowsAcc];
+        // sweep 2: sum of 2^((x - m) log2e) and of x, packed f32x2
+        float2 d2 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
+#pragma unroll 4
+        for (int v = lane; v < nvec; v += 32) {
+            float2 x[P];
+            VT::unpack2(tile[v], x);
 #pragma unroll
-        for (int k = 0; k < kRowsAcc; ++k) {
-            d2[k] = make_float2(0.f, 0.f);
-            s2[k] = make_float2(0.f, 0.f);
-        }
-        for (int v0 = lane; v0 < nvec; v0 += 32 * kRowsAcc) {
-#pragma unroll
-            for (int k = 0; k < kRowsAcc; ++k) {
-                const int v = v0 + 32 * k;
-                if (v < nvec) {
-                    float2 x[P];
-                    VT::unpack2(tile[v], x);
-#pragma unroll
-                    for (int j = 0; j < P; ++j) {
-                        const float2 e = __ffma2_rn(x[j], L2, NM);
-                        d2[k] = __fadd2_rn(d2[k], make_float2(ex2_approx(e.x), ex2_approx(e.y)));
-                        s2[k] = __fadd2_rn(s2[k], x[j]);
-                    }
-                }
+            for (int j = 0; j < P; ++j) {
+                const float2 e = __ffma2_rn(x[j], L2, NM);
+                d2 = __fadd2_rn(d2, make_float2(ex2_approx(e.x), ex2_approx(e.y)));
+                s2 = __fadd2_rn(s2, x[j]);
             }
         }
-#pragma unroll
-        for (int k = 1; k < kRowsAcc; ++k) {
-            d2[0] = __fadd2_rn(d2[0], d2[k]);
-            s2[0] = __fadd2_rn(s2[0], s2[k]);
-        }
-        const float d = warp_allsum(d2[0].x + d2[0].y);
-        const float S = (p.a != 0.f) ? warp_allsum(s2[0].x + s2[0].y) : 0.f;
+        const float d = warp_allsum(d2.x + d2.y);
+        const float S = (p.a != 0.f) ? warp_allsum(s2.x + s2.y) : 0.f;
         const float lse = m + logf(d);
         const float xy = VT::load1(reinterpret_cast<const unsigned char*>(tile) + y * ES);
         if (lane == 0) {

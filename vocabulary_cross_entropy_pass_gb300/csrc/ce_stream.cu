@@ -162,10 +162,6 @@ __device__ __forceinline__ void stats_tile(const uint4* tile, int tid, int nvec,
     const float nml = (m == -INFINITY) ? 0.f : -m * kLog2e;
     const float2 L2 = make_float2(kLog2e, kLog2e);
     const float2 NM = make_float2(nml, nml);
-    // two partial sums per tile (even and odd vectors) break the dependency
-    // chain of the adds; they join the running sums in a fixed order
-    float2 da[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-    float2 sa[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
         if (FULL || tid + i * NC < nvec) {
@@ -175,16 +171,14 @@ __device__ __forceinline__ void stats_tile(const uint4* tile, int tid, int nvec,
 #pragma unroll
             for (int j = 0; j < P; ++j) {
                 const float2 a = __ffma2_rn(x[j], L2, NM);
-                da[i & 1] = __fadd2_rn(da[i & 1], make_float2(ex2_approx(a.x), ex2_approx(a.y)));
+                d2 = __fadd2_rn(d2, make_float2(ex2_approx(a.x), ex2_approx(a.y)));
                 if constexpr (WS)
-                    sa[i & 1] = __ffma2_rn(w[j], x[j], sa[i & 1]);
+                    s2 = __ffma2_rn(w[j], x[j], s2);
                 else
-                    sa[i & 1] = __fadd2_rn(sa[i & 1], x[j]);
+                    s2 = __fadd2_rn(s2, x[j]);
             }
         }
     }
-    d2 = __fadd2_rn(d2, __fadd2_rn(da[0], da[1]));
-    s2 = __fadd2_rn(s2, __fadd2_rn(sa[0], sa[1]));
 }
 
 // Pass-2 work on one tile: c * 2^((x - lse) log2e) - b_j, rounded to T and
