@@ -253,3 +253,34 @@ def test_warp_path_tiles(V, dtype, tile_kb, stages):
                               workspace=ws, opts=opts)
         assert pkg.ce_get_error(ws) == (0, 0)
         _compare(w, x, t, loss, xd, n)
+
+
+@pytest.mark.parametrize("grad", [True, False])
+def test_row_counter_left_zeroed(grad):
+    """The stream kernel hands out rows past each CTA's first two from a
+    counter in the workspace; every pass must leave it (and the count of CTAs
+    done with it) at zero, so a pass that follows without a count kernel in
+    between -- the chunks of the lm_head pass -- starts from row 0 again."""
+    w = wl.WORKLOADS["c3_bsv32000_bf16_spiked"]  # 1024 rows: more than the CTAs
+    dev = torch.device("cuda")
+    x = wl.logits(w).to(dev)
+    t = wl.targets(w).to(dev)
+    assert pkg.ce_plan_path(x)[0] == pkg.CE_PATH_STREAM
+    ws = torch.full((pkg.ce_workspace_bytes(w.dim0, w.dim1, w.V, x.dtype),), 0x5A,
+                    dtype=torch.uint8, device=dev)  # garbage before the first pass
+    first = None
+    for _ in range(2):
+        xi = x.clone()
+        if grad:
+            loss = pkg.ce_fwd_bwd(xi, t, reduce_loss=False, workspace=ws)
+        else:
+            loss = pkg.ce_fwd_only(xi, t, reduce_loss=False, workspace=ws)
+        words = ws[40:48].cpu().numpy().view(np.uint32)
+        assert words.tolist() == [0, 0], words
+        st, err = pkg.ce_get_error(ws)
+        assert st == 0 and err == 0
+        if first is None:
+            first = (loss.clone(), xi)
+        else:  # the second pass over the same workspace gives the same results
+            assert torch.equal(loss, first[0])
+            assert torch.equal(xi, first[1])
