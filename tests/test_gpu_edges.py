@@ -284,3 +284,17 @@ def test_row_counter_left_zeroed(grad):
         else:  # the second pass over the same workspace gives the same results
             assert torch.equal(loss, first[0])
             assert torch.equal(xi, first[1])
+
+
+@pytest.mark.parametrize("N", [1, 151, 152, 153, 303, 304, 305, 700])
+@pytest.mark.parametrize("reduce", [True, False])
+def test_stream_row_counts(N, reduce):
+    """Row counts around one and two grids of the stream kernel (152 CTAs on
+    a GB300): CTAs with one row, with their two first rows only, and the first
+    rows claimed from the shared counter -- every row is computed once, and
+    matches the oracle."""
+    w = wl.WORKLOADS["c5_bsv128000_bf16_ls"].with_(
+        name=f"stream_rows_{N}", dim0=1, dim1=N, V=20000, reduce_loss=reduce, seed=3000 + N)
+    x = wl.logits(w)
+    assert pkg.ce_plan_path(x.to(DEV))[0] == pkg.CE_PATH_STREAM
+    harness.run_gpu_vs_oracle(w, per_row_dloss=not reduce)
