@@ -243,7 +243,6 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
     constexpr int VEC = VT::kElems;
     constexpr int ES = sizeof(T);
     constexpr int NW = NC / 32;           // consumer warps
-    static_assert(NW >= 1 && NW <= 32 && (NW & (NW - 1)) == 0, "a power-of-two warp count");
     constexpr int TB = NC * NV * 16;      // tile bytes
     constexpr int TV = NC * NV;           // vectors per tile
 
@@ -520,25 +519,12 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
         Part q = warp_allreduce_part(Part{m, d2.x + d2.y, s2.x + s2.y});
         if (lane == 0) red[par * NW + warp] = make_float4(q.m, q.d, q.S, 0.f);
         stop = named_bar_or(1, NC, nx < 0 || *abort_flag);
-        // every warp combines the NW warp partials the same way: lane w takes
-        // warp w's, a butterfly over lanes 0..NW-1, then lane 0's result to all
-        // lanes -- the same bits in every thread of the CTA
         Part G = part_identity();
-        if (lane < NW) {
-            const float4 v4 = red[par * NW + lane];
-            G = Part{v4.x, v4.y, v4.z};
-        }
 #pragma unroll
-        for (int off = NW / 2; off > 0; off >>= 1) {
-            Part o;
-            o.m = __shfl_xor_sync(kFull, G.m, off);
-            o.d = __shfl_xor_sync(kFull, G.d, off);
-            o.S = __shfl_xor_sync(kFull, G.S, off);
-            G = part_combine(G, o);
+        for (int w = 0; w < NW; ++w) {
+            const float4 v4 = red[par * NW + w];
+            G = part_combine(G, Part{v4.x, v4.y, v4.z});
         }
-        G.m = __shfl_sync(kFull, G.m, 0);
-        G.d = __shfl_sync(kFull, G.d, 0);
-        G.S = __shfl_sync(kFull, G.S, 0);
         const float lse = G.m + logf(G.d);
         const float xy = xy_s[par];
         const float wy = WT ? __ldg(p.cw + y) : 1.f;
