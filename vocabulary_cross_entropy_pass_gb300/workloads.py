@@ -96,6 +96,10 @@ WORKLOADS = {
                                     0.10, label_smoothing=0.1, reduce_loss=True, seed=1025),
     "c5_bsv128000_f32": Workload("c5_bsv128000_f32", 1, 512, 128000, "f32", "bsv", 2.0, 0.10,
                                  label_smoothing=0.0, reduce_loss=True, seed=1035),
+    # profiling size of 32 KB rows (the widest the warp path takes): (8, 4096,
+    # 16384) bf16, ~1.07 GB
+    "c2w_bsv16384_bf16": Workload("c2w_bsv16384_bf16", 8, 4096, 16384, "bf16", "bsv", 2.0, 0.05,
+                                  label_smoothing=0.1, reduce_loss=True, seed=1062),
     # profiling size of the 32000-column family: (16, 2048, 32000) bf16, ~2.1 GB
     "c3p_bsv32000_bf16": Workload("c3p_bsv32000_bf16", 16, 2048, 32000, "bf16", "bsv", 3.0,
                                   0.10, spike_frac=0.01, seed=1033),
