@@ -315,6 +315,18 @@ ce_status ce_fwd_bwd_noalloc(void* logits, ce_dtype dtype, ce_layout layout, int
  * the copy fails.  Diagnostic use: this is the only call that synchronises. */
 ce_status ce_get_error(const void* workspace, void* stream, uint32_t* host_err);
 
+/* Failure detection check (no counterpart on the pages).  Every wait inside
+ * this library's kernels -- on a TMA copy landing, on a ring slot, on a row
+ * handed between warps -- is bounded: after ~1.5 s it gives up, sets
+ * CE_DEVERR_TIMEOUT in the workspace error word and lets the kernel return,
+ * so a lost copy is reported instead of hanging the GPU.  This call runs that
+ * same bounded wait once, in a one-thread kernel, on an mbarrier that nothing
+ * arrives on, and writes the result as the error word of `workspace`
+ * (>= 256 bytes, 16-byte aligned): ce_get_error then returns
+ * CE_ERR_DEVICE_TIMEOUT after ~1.5 s, and the stream stays usable.  Returns
+ * CE_OK once the kernel is enqueued, CE_ERR_INVALID_ARG for a bad workspace. */
+ce_status ce_wait_timeout_probe(void* workspace, size_t workspace_bytes, void* stream);
+
 /* Static English description of a status code. */
 const char* ce_status_string(ce_status status);
 

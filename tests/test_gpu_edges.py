@@ -298,3 +298,20 @@ def test_stream_row_counts(N, reduce):
     x = wl.logits(w)
     assert pkg.ce_plan_path(x.to(DEV))[0] == pkg.CE_PATH_STREAM
     harness.run_gpu_vs_oracle(w, per_row_dloss=not reduce)
+
+
+def test_bounded_wait_reports_timeout():
+    """Failure detection without a fault: the bounded wait the kernels use,
+    left to run out on a barrier nothing completes, reports CE_DEVERR_TIMEOUT
+    through the workspace, and the GPU takes the next pass normally."""
+    import time
+    ws = torch.zeros(4096, dtype=torch.uint8, device=DEV)
+    t0 = time.time()
+    pkg.ce_wait_timeout_probe(ws)
+    st, err = pkg.ce_get_error(ws)
+    waited = time.time() - t0
+    assert err == 0x2 and st == 7, (st, err)  # CE_DEVERR_TIMEOUT, CE_ERR_DEVICE_TIMEOUT
+    assert 1.0 < waited < 30.0
+    assert "gave up" in pkg.ce_status_string(st)
+    w = wl.WORKLOADS["c2_sbv8192_bf16"]
+    harness.run_gpu_vs_oracle(w)  # the context is still usable

@@ -31,6 +31,7 @@ from ._lib import (CE_PATH_AUTO, CE_PATH_CLUSTER, CE_PATH_ROW, CE_PATH_STREAM,
 __all__ = ["ce_fwd_bwd", "ce_fwd_bwd_noalloc", "ce_fwd_only", "ce_bwd", "parallel_cross_entropy",
            "ce_vp_partials", "ce_vp_combine", "ce_vp_bwd", "vocab_parallel_cross_entropy",
            "ce_linear_fwd_bwd", "ce_workspace_bytes", "ce_get_error", "ce_status_string",
+           "ce_wait_timeout_probe",
            "ce_plan_path", "CEError", "make_options", "ce_options",
            "CE_PATH_AUTO", "CE_PATH_ROW", "CE_PATH_CLUSTER", "CE_PATH_TWO_STAGE", "CE_PATH_STREAM", "CE_PATH_WARP"]
 
@@ -223,6 +224,18 @@ def ce_get_error(workspace: torch.Tensor, stream=None) -> tuple[int, int]:
     rc = lib.ce_get_error(ctypes.c_void_p(workspace.data_ptr()), _stream(workspace.device, stream),
                           ctypes.byref(err))
     return int(rc), int(err.value)
+
+
+def ce_wait_timeout_probe(workspace: torch.Tensor, stream=None) -> None:
+    """Run the kernels' bounded wait once on a barrier nothing completes; its
+    timeout lands in ``workspace``'s error word (read it with ce_get_error,
+    ~1.5 s later)."""
+    if not workspace.is_cuda:
+        raise TypeError("workspace must be a CUDA tensor")
+    lib = _lib.load()
+    nbytes = workspace.numel() * workspace.element_size()
+    _raise(lib.ce_wait_timeout_probe(ctypes.c_void_p(workspace.data_ptr()), nbytes,
+                                     _stream(workspace.device, stream)), "ce_wait_timeout_probe")
 
 
 def ce_status_string(status: int) -> str:

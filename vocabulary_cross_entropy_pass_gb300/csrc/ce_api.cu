@@ -565,6 +565,14 @@ ce_status ce_get_error(const void* workspace, void* stream, uint32_t* host_err) 
     return CE_OK;
 }
 
+ce_status ce_wait_timeout_probe(void* workspace, size_t workspace_bytes, void* stream) {
+    if (!workspace || workspace_bytes < kWsHeaderBytes) return CE_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(workspace) % 16) return CE_ERR_INVALID_ARG;
+    uint32_t* err = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + kWsErrOffset);
+    if (launch_wait_probe(err, static_cast<cudaStream_t>(stream)) != cudaSuccess) return CE_ERR_LAUNCH;
+    return CE_OK;
+}
+
 const char* ce_status_string(ce_status status) {
     switch (status) {
         case CE_OK: return "ok";

@@ -5,6 +5,8 @@
 //   "Known limitations") counts n_non_ignore on the host because atomic adds
 //   were unreliable there; here one CTA counts on the device with a
 //   fixed-order integer reduction, before the gradient pass needs dloss/n.
+// ce_wait_probe_kernel: a bounded wait that is left to run out, so a host
+//   can check that a kernel which would otherwise hang reports a timeout.
 // ce_mean_kernel: reduce_loss -- the mean of the per-row losses over the kept
 //   rows (or over their summed class weight), summed in a fixed order (fixed per-thread strides, then a fixed
 //   butterfly and a fixed cross-warp order), so the result is bitwise the same
@@ -128,7 +130,24 @@ ce_mean_kernel(const float* __restrict__ loss_rows, int64_t N, const int64_t* n_
     }
 }
 
+// The bounded wait every kernel uses, on an mbarrier no one arrives on: it
+// gives up after the wait limit and records CE_DEVERR_TIMEOUT, exactly as a
+// kernel whose copy never lands would.  One thread; nothing else runs.
+__global__ void ce_wait_probe_kernel(uint32_t* err) {
+    __shared__ __align__(8) uint64_t bar;
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+    uint32_t e = 0u;
+    if (!mbar_wait_bounded(&bar, 0u)) e |= CE_DEVERR_TIMEOUT;  // phase 0 never completes
+    *err = e;
+}
+
 }  // namespace
+
+cudaError_t launch_wait_probe(uint32_t* err, cudaStream_t s) {
+    ce_wait_probe_kernel<<<1, 1, 0, s>>>(err);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_count(const Problem& p, int64_t* n_out, cudaStream_t s) {
     ce_count_kernel<<<1, kAuxThreads, 0, s>>>(p.targets, p.ts0, p.ts1, p.dim1, p.N, p.V,

@@ -136,6 +136,8 @@ int fused_capacity(int dtype, int threads);  // elements one CTA can hold
 int split_auto_chunks(int64_t V);
 
 cudaError_t launch_count(const Problem& p, int64_t* n_out, cudaStream_t s);
+// one bounded mbarrier wait that runs out; writes the error word
+cudaError_t launch_wait_probe(uint32_t* err, cudaStream_t s);
 // the count kernel and the pass after it overlap (programmatic dependent launch)
 void set_pdl_attr(cudaLaunchAttribute* attr);
 cudaError_t launch_reduce_mean(const Problem& p, float* loss_out, cudaStream_t s);
