@@ -315,3 +315,16 @@ def test_bounded_wait_reports_timeout():
     assert "gave up" in pkg.ce_status_string(st)
     w = wl.WORKLOADS["c2_sbv8192_bf16"]
     harness.run_gpu_vs_oracle(w)  # the context is still usable
+
+
+@pytest.mark.parametrize("V,path", [(1 << 20, pkg.CE_PATH_STREAM), ((1 << 20) + 3, pkg.CE_PATH_TWO_STAGE)])
+@pytest.mark.parametrize("reduce", [True, False])
+def test_very_wide_rows(V, path, reduce):
+    """Rows of a million columns (2 MB of bf16 each: 64 ring tiles per pass on
+    the stream path; an odd width goes to the two-stage kernels), against the
+    oracle."""
+    w = wl.WORKLOADS["c5_bsv128000_bf16_ls"].with_(
+        name=f"wide_{V}", dim0=2, dim1=12, V=V, reduce_loss=reduce, seed=4000 + V % 97)
+    x = wl.logits(w)
+    assert pkg.ce_plan_path(x.to(DEV))[0] == path
+    harness.run_gpu_vs_oracle(w, per_row_dloss=not reduce)
