@@ -233,11 +233,13 @@ __device__ __forceinline__ void grad_tile(const uint4* tile, uint4* dst, int tid
     }
 }
 
-// The weighted gradient pass issues ~40% more instructions per element than
-// the plain one: its 16 KB-tile shape is built for two CTAs per SM (more warps
-// to hide latency), every other shape for one.
+// The 256-thread, 16 KB-tile shape is built for two CTAs per SM (96
+// registers): twice the warps to hide issue latency, for rows short enough
+// that two CTAs' rows between their passes still fit L2 (and for the
+// weighted pass, whose gradient pass issues ~40% more instructions per
+// element).  Every other shape is built for one CTA per SM.
 template <typename T, int NC, int NV, bool GRAD, bool WT>
-__global__ void __launch_bounds__(NC + 32, (WT && GRAD && NV * NC * 16 == 16384) ? 2 : 1)
+__global__ void __launch_bounds__(NC + 32, (NC == 256 && NV * NC * 16 == 16384) ? 2 : 1)
 ce_stream_kernel(const __grid_constant__ StreamArgs p) {
     using VT = Vec<T>;
     constexpr int VEC = VT::kElems;
