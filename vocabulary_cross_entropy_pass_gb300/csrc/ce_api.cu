@@ -173,11 +173,16 @@ Plan make_plan(const Problem& p, const ce_options* o) {
     }
     const bool stream_auto = force == CE_PATH_AUTO && aligned && K == 0;
     if (force == CE_PATH_STREAM || stream_auto) {
-        // rows of four or more 32 KB tiles run a 6-deep ring (128000 bf16
-        // columns: 1.178 ms against 1.196 ms at 5), shorter ones 5 deep
-        // (32000 columns: 0.713 ms at 5, 0.715 at 6, 0.721 at 7)
-        const int def_stages = row_bytes >= 128 * 1024 ? 6 : 0;
-        if (!aligned || !plan_stream(o, &pl.stream, 0, def_stages)) {
+        // Rows up to 128 KB: 16 KB tiles 6 deep, two CTAs per SM (twice the
+        // warps; two CTAs' rows between their passes still fit L2).  Wider
+        // rows: 32 KB tiles 6 deep, one CTA per SM, so fewer rows wait in L2
+        // for their second pass.  Same-GPU sweep, ~2.1 GB of bf16 logits per
+        // width, ms per launch (16 KB x 6 / 32 KB x 6): 32 KB rows 0.795 /
+        // 1.203, 62 KB 0.604 / 0.743, 98 KB 0.605 / 0.728, 128 KB 0.608 /
+        // 0.617, 160 KB 0.618 / 0.598, 250 KB 0.679 / 0.601, 500 KB 0.836 /
+        // 0.681.
+        const int def_tile = row_bytes <= 128 * 1024 ? 16 : 32;
+        if (!aligned || !plan_stream(o, &pl.stream, def_tile, 6)) {
             pl.path = -2;
             return pl;
         }
