@@ -181,10 +181,7 @@ Plan make_plan(const Problem& p, const ce_options* o) {
         // 1.203, 62 KB 0.604 / 0.743, 98 KB 0.605 / 0.728, 128 KB 0.608 /
         // 0.617, 160 KB 0.618 / 0.598, 250 KB 0.679 / 0.601, 500 KB 0.836 /
         // 0.681.
-        // A pass without a gradient reads each row once (nothing waits in L2):
-        // two CTAs per SM at any width (split step at 128000 columns: 1.822
-        // ms against 1.846 ms).
-        const int def_tile = (!p.grad || row_bytes <= 128 * 1024) ? 16 : 32;
+        const int def_tile = row_bytes <= 128 * 1024 ? 16 : 32;
         if (!aligned || !plan_stream(o, &pl.stream, def_tile, 6)) {
             pl.path = -2;
             return pl;
