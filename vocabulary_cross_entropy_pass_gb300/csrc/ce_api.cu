@@ -181,6 +181,11 @@ Plan make_plan(const Problem& p, const ce_options* o) {
         // 1.203, 62 KB 0.604 / 0.743, 98 KB 0.605 / 0.728, 128 KB 0.608 /
         // 0.617, 160 KB 0.618 / 0.598, 250 KB 0.679 / 0.601, 500 KB 0.836 /
         // 0.681.
+        // The same shape with or without a gradient, so a forward-only pass
+        // gives the fused pass's losses bit for bit (one CTA's partial sums
+        // group the same way); two CTAs per SM would speed a forward-only pass
+        // of wider rows too (split step at 128000 columns: 1.822 ms against
+        // 1.846 ms), not worth losing that.
         const int def_tile = row_bytes <= 128 * 1024 ? 16 : 32;
         if (!aligned || !plan_stream(o, &pl.stream, def_tile, 6)) {
             pl.path = -2;
