@@ -334,16 +334,14 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
             };
             // The queue runs one row ahead of the copies: the row after this one
             // is published before this row's copies, so the consumers can read
-            // it while they work on this row.  The claim of the row after that
-            // is issued before this row's copies too, so its latency hides
-            // behind them; on the first row it follows the first pass's copies
-            // (the first claim waits for the count kernel).
-            // Each entry carries the row's target, read here once for the
-            // consumer warps as well.
+            // it while they work on this row.  The row after that is claimed
+            // before this row's copies too (on the first row, after its first
+            // pass: the first claim waits for the count kernel), and its target
+            // is loaded right away but first read one row later, when it is
+            // published.  Each entry carries the row's target, read here once
+            // for the consumer warps as well.
             int64_t r = blockIdx.x, n1 = r + gridDim.x, n2 = -1;  // this row, the next two
             int64_t yr = row_target(r), y1 = n1 < p.N ? row_target(n1) : 0, y2 = 0;
-            // a claimed row's target is read as soon as the row is known, one
-            // row before it is published
             auto claim_y = [&]() {
                 n2 = claim(n1);
                 y2 = n2 < p.N ? row_target(n2) : 0;
