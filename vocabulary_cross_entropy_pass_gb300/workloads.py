@@ -110,6 +110,9 @@ WORKLOADS = {
     # profiling size: ~1 GB of bf16 logits (several times the L2)
     "c5p_bsv128000_bf16": Workload("c5p_bsv128000_bf16", 1, 4096, 128000, "bf16", "bsv", 2.0,
                                    0.10, label_smoothing=0.1, reduce_loss=True, seed=1055),
+    # profiling size of the widest family: (1, 4096, 256000) bf16, ~2.1 GB
+    "c6p_bsv256000_bf16": Workload("c6p_bsv256000_bf16", 1, 4096, 256000, "bf16", "bsv", 2.0,
+                                   0.10, label_smoothing=0.1, reduce_loss=True, seed=1066),
     # throughput size: ~4.2 GB of bf16 logits
     "c5t_bsv128000_bf16": Workload("c5t_bsv128000_bf16", 4, 4096, 128000, "bf16", "bsv", 2.0,
                                    0.10, label_smoothing=0.1, reduce_loss=True, seed=1045),
