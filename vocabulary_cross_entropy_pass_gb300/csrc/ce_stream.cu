@@ -295,6 +295,14 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
     // weights into the next WS ring slots (without smoothing no weight is read)
     constexpr int WS = 4 / ES;
     const bool wring = WT && GRAD && p.a != 0.f;
+    // Parked tiles: when pass 1 of a row ends, the ring's `stages` slots hold
+    // the row's last `stages` tiles (rows of at least `stages` tiles), and the
+    // ring is a queue -- so pass 2 takes those tiles first, straight from
+    // shared memory (the producer re-marks their slots full without a copy),
+    // then reloads tiles 0 .. ntiles - R - 1.  Pass-2 tile k is tile
+    // pass2_tile(k).  Not with weight slots in the ring.
+    const int R = (GRAD && !wring && p.ntiles >= p.stages) ? p.stages : 0;
+    auto pass2_tile = [&](int k) -> int { return k < R ? p.ntiles - R + k : k - R; };
 
     // ------------------------------------------------------------ producer warp
     if (warp == NW) {
@@ -361,17 +369,26 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
                         claim_y();
                         claimed = true;
                     }
-                    for (int t = 0; t < p.ntiles; ++t) {
+                    for (int k = 0; k < p.ntiles; ++k) {
                         if (!mbar_wait_bounded(&empty[rg.s], rg.ph ^ 1u)) {
                             griddep_wait();  // the count kernel starts the error word
                             atomicOr(p.err, CE_DEVERR_TIMEOUT);
                             *abort_flag = 1;
                             break;
                         }
+                        if (pass == 1 && k < R) {
+                            // a parked tile: still in this slot since pass 1
+                            mbar_arrive(&full[rg.s]);
+                            rg.next();
+                            ++issued;
+                            continue;
+                        }
+                        const int t = pass == 1 ? pass2_tile(k) : k;
                         const uint32_t bytes = (t == p.ntiles - 1) ? p.last_bytes : (uint32_t)TB;
+                        // pass 1 asks L2 to keep the tiles pass 2 will reload
+                        const uint64_t pol = (pass == 0 && t < p.ntiles - R) ? pol_keep : pol_drop;
                         mbar_arrive_expect_tx(&full[rg.s], bytes);
-                        tma_load_1d(ring + (size_t)rg.s * TB, row + (size_t)t * TB, bytes, &full[rg.s],
-                                    pass == 0 ? pol_keep : pol_drop);
+                        tma_load_1d(ring + (size_t)rg.s * TB, row + (size_t)t * TB, bytes, &full[rg.s], pol);
                         rg.next();
                         ++issued;
                         if (pass == 1 && wring) {
@@ -545,7 +562,8 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
             const float2 G2 = make_float2(c, c);
             const float2 NB = make_float2(-bb, -bb);
             float2 sw2 = make_float2(0.f, 0.f);
-            for (int t = 0; t < p.ntiles; ++t) {
+            for (int k = 0; k < p.ntiles; ++k) {
+                const int t = pass2_tile(k);  // the parked tiles first
                 wait_full();
                 const int st = rg.s;
                 const uint4* tile = reinterpret_cast<const uint4*>(ring + (size_t)st * TB);
