@@ -317,12 +317,14 @@ def test_bounded_wait_reports_timeout():
     harness.run_gpu_vs_oracle(w)  # the context is still usable
 
 
-@pytest.mark.parametrize("V,path", [(1 << 20, pkg.CE_PATH_STREAM), ((1 << 20) + 3, pkg.CE_PATH_TWO_STAGE)])
+@pytest.mark.parametrize("V,path", [(1 << 20, pkg.CE_PATH_STREAM), ((1 << 20) + 3, pkg.CE_PATH_TWO_STAGE),
+                                    (256000, pkg.CE_PATH_STREAM), (200000, pkg.CE_PATH_STREAM)])
 @pytest.mark.parametrize("reduce", [True, False])
 def test_very_wide_rows(V, path, reduce):
     """Rows of a million columns (2 MB of bf16 each: 64 ring tiles per pass on
-    the stream path; an odd width goes to the two-stage kernels), against the
-    oracle."""
+    the stream path; an odd width goes to the two-stage kernels), and rows of
+    16 and 13 tiles (the last one partial) -- all wide enough for pass 2 to
+    take the ring's last tiles from shared memory -- against the oracle."""
     w = wl.WORKLOADS["c5_bsv128000_bf16_ls"].with_(
         name=f"wide_{V}", dim0=2, dim1=12, V=V, reduce_loss=reduce, seed=4000 + V % 97)
     x = wl.logits(w)
