@@ -330,3 +330,13 @@ def test_very_wide_rows(V, path, reduce):
     x = wl.logits(w)
     assert pkg.ce_plan_path(x.to(DEV))[0] == path
     harness.run_gpu_vs_oracle(w, per_row_dloss=not reduce)
+
+
+def test_warp_path_two_tiles_by_default():
+    """From 8192 rows on, the planner gives each consumer warp of the
+    warp-per-row kernel two 16 KB tiles (a 12-deep ring): many rows per warp,
+    tiles reused in turn, against the oracle."""
+    w = wl.Workload("warp_many_rows", 1, 9000, 8192, "bf16", sigma=2.0, ignore_frac=0.05,
+                    label_smoothing=0.1, reduce_loss=True, seed=9000)
+    assert pkg.ce_plan_path(wl.logits(w).to(DEV))[0] == pkg.CE_PATH_WARP
+    harness.run_gpu_vs_oracle(w)
