@@ -92,8 +92,12 @@ typedef enum {
     CE_PATH_ROW = 1,       /* one CTA holds a whole row in shared memory and registers */
     CE_PATH_CLUSTER = 2,   /* a thread-block cluster splits each row; combine over DSMEM */
     CE_PATH_TWO_STAGE = 3, /* per-chunk statistics kernel, then combine + gradient kernel */
-    CE_PATH_STREAM = 4,    /* one CTA streams whole rows twice through a TMA ring; the
-                              second read of a row is served by L2 */
+    CE_PATH_STREAM = 4,    /* one CTA streams whole rows twice through a TMA ring (rows
+                              claimed from a counter in the workspace); the second read
+                              of a row is served by L2, or for rows of at least twice
+                              the ring by the ring's last tiles still in shared memory.
+                              Default shape: rows up to 128 KB 16 KB tiles, 6 deep, two
+                              CTAs per SM; wider rows 32 KB tiles, 6 deep, one CTA */
     CE_PATH_WARP = 5       /* one warp per row, the row held in one shared-memory tile
                               (rows up to 32 KB) */
 } ce_path;
@@ -111,7 +115,8 @@ typedef struct {
                                path the number of consuming threads) */
     int tune_stages;        /* 0 = default; otherwise TMA pipeline depth (2..4 rows on the
                                row/cluster paths, 2..12 tiles on the stream path, 6 or 12
-                               tiles on the warp path) */
+                               tiles on the warp path: 12 = two tiles per consumer warp,
+                               the default for 16 KB tiles from 8192 rows on) */
     int tune_ctas_per_sm;   /* 0 = as many as fit; otherwise a cap */
     int tune_l2_keep;       /* stream path: 0 = default (1), 1 = the first read asks L2 to
                                keep the row for the second (evict-last), 2 = evict-first */
