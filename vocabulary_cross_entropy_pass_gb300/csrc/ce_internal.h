@@ -16,7 +16,7 @@ namespace gbce {
 //   [16, 20)    uint32 count of CTAs done (the stream kernel's in-kernel mean)
 //   [24, 32)    double summed class weight of the kept rows' targets (weighted pass)
 //   [32, 40)    double summed class weight over the vocabulary (weighted pass)
-//   [40, 44)    uint32 rows claimed beyond the first grid's worth (stream kernel)
+//   [40, 44)    uint32 rows claimed beyond each CTA's first two (stream kernel)
 //   [44, 48)    uint32 CTAs done claiming (the last one zeroes both words)
 //   [256, ...)  float per-row losses (N) -- used when reduce_loss
 //   [...]       float4 per-(row, chunk) partials of the two-stage path

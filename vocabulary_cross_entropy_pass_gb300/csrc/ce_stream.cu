@@ -68,7 +68,7 @@ struct StreamArgs {
     const float* cw;       // class weights [V], 16-byte aligned (weighted pass) or NULL
     const double* wdenom;  // summed weight of the kept rows' targets (count kernel)
     const double* wsum;    // summed weight over the vocabulary (count kernel)
-    uint32_t* row_claim;   // rows claimed past the first grid's worth, or NULL (static rows)
+    uint32_t* row_claim;   // rows claimed past each CTA's first two, or NULL (static rows)
     uint32_t* row_done;    // CTAs done claiming
 };
 
