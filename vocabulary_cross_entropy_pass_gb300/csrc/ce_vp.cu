@@ -41,7 +41,11 @@ struct VpPartArgs {
 constexpr int kVpBatch = 4;
 
 template <typename T>
-__global__ void __launch_bounds__(kVpThreads) ce_vp_partials_kernel(const __grid_constant__ VpPartArgs p) {
+// Six CTAs per SM (<= 42 registers): at the unbounded 54 registers only four
+// fit, too few loads in flight (ncu: long-scoreboard stalls 5.65 per issue,
+// 52 % DRAM throughput); 8 shards of the bench workload: 2.054 ms per step
+// against 2.134 ms (eight CTAs per SM spill and measured 2.181 ms).
+__global__ void __launch_bounds__(kVpThreads, 6) ce_vp_partials_kernel(const __grid_constant__ VpPartArgs p) {
     using VT = Vec<T>;
     constexpr int VEC = VT::kElems;
     constexpr int ES = sizeof(T);
