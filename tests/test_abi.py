@@ -135,6 +135,19 @@ def test_planner(lib):
     assert plan(4_000_000, force_path=2)[0] == -2  # too wide for 16 CTAs
     assert plan(32000, force_path=1)[0] == -2      # one CTA cannot hold the row
     assert plan(4096, force_path=2) == (2, 2)
+    # class weights: the stream kernel when rows and weights are 16-byte
+    # aligned (any width), else the two-stage kernels; paths without weights
+    # are refused; a ring too shallow for a 16-bit tile and its two weight
+    # slots twice falls back to two-stage (fp32 tiles need one weight slot)
+    assert plan(128000, class_weights=0x2000)[0] == 4
+    assert plan(4096, class_weights=0x2000)[0] == 4
+    assert plan(128000, class_weights=0x2004)[0] == 3
+    assert plan(4095, class_weights=0x2000)[0] == 3
+    assert plan(4096, class_weights=0x2000, force_path=5)[0] == -2
+    assert plan(4096, class_weights=0x2000, force_path=1)[0] == -2
+    assert plan(128000, class_weights=0x2000, tune_stages=4)[0] == 3
+    assert plan(128000, dtype=0, class_weights=0x2000, tune_stages=4)[0] == 4
+    assert plan(128000, class_weights=0x2000, num_vocab_chunks=4)[0] == 3
 
 
 def test_overlapping_rows_rejected_for_in_place_gradient(lib):
