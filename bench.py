@@ -579,12 +579,23 @@ def main(argv=None) -> int:
     ap.add_argument("--tune-ctas-per-sm", type=int, default=0)
     ap.add_argument("--tune-l2-keep", type=int, default=0)
     ap.add_argument("--tune-tile-kb", type=int, default=0)
+    # another vocabulary width and/or row count for the chosen workload (its
+    # dtype, value spread, ignore fraction and smoothing kept), as (1, rows, V)
+    ap.add_argument("--vocab", type=int, default=0)
+    ap.add_argument("--rows", type=int, default=0)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.vocab < 0 or args.rows < 0:
+        ap.error("--vocab and --rows must be positive")
 
     from vocabulary_cross_entropy_pass_gb300 import workloads as wl
     w = wl.WORKLOADS[args.workload]
+    if args.vocab or args.rows:
+        V = args.vocab or w.V
+        N = args.rows or w.N
+        w = w.with_(name=f"{w.name}_as_{N}x{V}", dim0=1, dim1=N, V=V, layout="bsv",
+                    vocab_chunks=0)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
