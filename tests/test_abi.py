@@ -91,6 +91,8 @@ def test_host_validation_rejects_before_launch(lib):
     assert _call(lib, strides=(-1, 4096, 1)) == 3
     assert _call(lib, tstrides=(-3, 1)) == 3
     assert _call(lib, ws=0x4008) == 1          # not 16-byte aligned
+    assert _call(lib, logits=0x1001) == 1      # bf16 logits off a 2-byte boundary
+    assert _call(lib, logits=0x1002, dtype=0) == 1  # fp32 logits off a 4-byte boundary
     assert _call(lib, wsb=100) == 4
     assert _call(lib, grad=0x9000) == 1        # the gradient must go in place
     o = _lib.make_options()
@@ -177,6 +179,8 @@ def test_bwd_host_validation(lib):
     assert call(gst=(0, 4096, 1)) == 3               # gradient rows may not share memory
     assert call(grad=0x1000, gst=(4096, 2 * 4096, 1)) == 3  # in place means the same strides
     assert call(dtype=9) == 2
+    assert call(logits=0x1001) == 1                   # off the element size
+    assert call(grad=0x9001) == 1
     assert call(d0=0) == 0                            # nothing to do
 
 
@@ -199,6 +203,9 @@ def test_vocab_parallel_host_validation(lib):
     assert lib.ce_vp_partials(ctypes.c_void_p(0x1000), 1, 1, 4, 16, _lib.i64_array((64, 16, 1)),
                               ctypes.c_void_p(0x2000), _lib.i64_array((4, 1)), 0, -100,
                               ctypes.c_void_p(0x3008), None) == 1  # partials not 16-byte aligned
+    assert lib.ce_vp_partials(ctypes.c_void_p(0x1001), 1, 1, 4, 16, _lib.i64_array((64, 16, 1)),
+                              ctypes.c_void_p(0x2000), _lib.i64_array((4, 1)), 0, -100,
+                              ctypes.c_void_p(0x3000), None) == 1  # shard off the element size
     # the shard must lie inside the vocabulary
     assert lib.ce_vp_bwd(ctypes.c_void_p(0x1000), 1, 1, 4, 16, _lib.i64_array((64, 16, 1)),
                          ctypes.c_void_p(0x2000), _lib.i64_array((4, 1)), 40, 50,

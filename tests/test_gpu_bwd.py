@@ -106,3 +106,29 @@ def test_dist_process_group_is_refused():
     t = torch.zeros(1, 2, dtype=torch.int64, device=DEV)
     with pytest.raises(NotImplementedError):
         pkg.parallel_cross_entropy(x, t, dist_process_group=object())
+
+
+@pytest.mark.parametrize("V,dtype,gshift", [(20011, "bf16", 0), (20011, "bf16", 1), (8193, "f16", 0),
+                                            (10007, "f32", 0), (10007, "f32", 3)])
+def test_bwd_unaligned_rows_wide(V, dtype, gshift):
+    """Rows off the 16-byte grid over several 16 KB chunks: with the gradient
+    at the logits' offset from a 16-byte boundary (gshift 0) the chunks move
+    in 16-byte vectors between a scalar head and tail; a gradient view
+    shifted by gshift elements takes the element-by-element kernel.  The
+    gradient buffer's padding stays untouched."""
+    w = wl.Workload("uw", 1, 13, V, dtype, sigma=2.0, ignore_frac=0.2, label_smoothing=0.1, seed=V + gshift)
+    x = wl.logits(w)
+    t = wl.targets(w)
+    ref = harness.oracle_run(w, x, t)
+    xd, td = x.to(DEV), t.to(DEV)
+    lse = torch.empty(w.N, dtype=torch.float32, device=DEV)
+    pkg.ce_fwd_only(xd, td, label_smoothing=0.1, lse_out=lse)
+    gbuf = torch.zeros(1, 13, V + 8, dtype=xd.dtype, device=DEV)
+    gview = gbuf[:, :, gshift:gshift + V]
+    g = pkg.ce_bwd(xd, td, lse, label_smoothing=0.1, grad=gview)
+    excess, _ = harness.grad_errors(g.float().cpu().numpy().astype(np.float64).reshape(w.N, V),
+                                    ref["grad"], dtype)
+    assert excess <= 0.0
+    host = gbuf.cpu()
+    assert torch.all(host[:, :, :gshift] == 0) and torch.all(host[:, :, gshift + V:] == 0)
+    assert torch.equal(xd.cpu(), x)

@@ -340,3 +340,51 @@ def test_warp_path_two_tiles_by_default():
                     label_smoothing=0.1, reduce_loss=True, seed=9000)
     assert pkg.ce_plan_path(wl.logits(w).to(DEV))[0] == pkg.CE_PATH_WARP
     harness.run_gpu_vs_oracle(w)
+
+
+@pytest.mark.parametrize("V,dtype,a,reduce,ignore", [(100277, "bf16", 0.1, True, 0.1),
+                                                     (50257, "f16", 0.0, False, 0.2),
+                                                     (100003, "f32", 0.2, True, 0.0),
+                                                     (16387, "bf16", 0.0, False, 0.05)])
+def test_unaligned_rows_two_stage(V, dtype, a, reduce, ignore):
+    """Odd widths put every row at its own offset from a 16-byte boundary; the
+    two-stage kernels read each chunk as a scalar head, 16-byte vectors and a
+    scalar tail (several chunks per row, the last one ragged)."""
+    w = wl.Workload(f"unaligned_{V}", 2, 17, V, dtype, sigma=2.0, ignore_frac=ignore,
+                    label_smoothing=a, reduce_loss=reduce, seed=V % 1000)
+    assert pkg.ce_plan_path(wl.logits(w).to(DEV))[0] == pkg.CE_PATH_TWO_STAGE
+    harness.run_gpu_vs_oracle(w, per_row_dloss=not reduce)
+
+
+@pytest.mark.parametrize("K", [3, 7, 16])
+def test_unaligned_rows_short_chunks(K):
+    """Chunks shorter than a 16-byte vector (37 bf16 columns in up to 16
+    chunks of 3): some chunks are all head, some hold no whole vector."""
+    w = wl.Workload("short_chunks", 1, 11, 37, "bf16", sigma=2.0, ignore_frac=0.2,
+                    label_smoothing=0.1, reduce_loss=True, seed=37 + K)
+    harness.run_gpu_vs_oracle(w, force_path=pkg.CE_PATH_TWO_STAGE, num_vocab_chunks=K)
+
+
+@pytest.mark.parametrize("dtype,shift", [("bf16", 1), ("bf16", 5), ("f16", 3), ("f32", 1)])
+def test_shifted_view_rows(dtype, shift):
+    """An aligned width read through a view that starts `shift` elements
+    into each padded row: the rows leave the 16-byte grid, the two-stage
+    kernels take them, and the padding on both sides stays untouched."""
+    V, pad = 32000, 9
+    w = wl.Workload("shifted", 2, 5, V, dtype, sigma=2.0, label_smoothing=0.1, seed=50 + shift)
+    x = wl.logits(w)
+    buf = torch.zeros(2, 5, V + pad, dtype=TDT[dtype])
+    buf[:, :, shift:shift + V] = x
+    t = wl.targets(w)
+    bd = buf.to(DEV)
+    view = bd[:, :, shift:shift + V]
+    assert pkg.ce_plan_path(view)[0] == pkg.CE_PATH_TWO_STAGE
+    loss = pkg.ce_fwd_bwd(view, t.to(DEV), label_smoothing=0.1)
+    ref = harness.oracle_run(w, x, t)
+    harness.check_loss(loss.cpu().numpy(), ref["loss"], dtype, "shifted")
+    g = view.float().cpu().numpy().reshape(w.N, V).astype(np.float64)
+    excess, _ = harness.grad_errors(g, ref["grad"], dtype)
+    assert excess <= 0.0
+    host = bd.cpu()
+    assert torch.all(host[:, :, :shift] == 0)
+    assert torch.all(host[:, :, shift + V:] == 0)

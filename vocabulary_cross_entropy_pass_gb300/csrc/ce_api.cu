@@ -235,6 +235,7 @@ ce_status check_common(const void* logits, int dtype, int layout, int64_t dim0, 
     if (!empty && (!logits || !targets || !loss_out)) return CE_ERR_INVALID_ARG;
     if (empty && reduce && !loss_out) return CE_ERR_INVALID_ARG;
     if (!(a >= 0.f && a <= 1.f)) return CE_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(logits) % elem_size(dtype)) return CE_ERR_INVALID_ARG;
     if (!opts_clean(o)) return CE_ERR_INVALID_ARG;
     if (strides[2] != 1 || strides[0] < 0 || strides[1] < 0) return CE_ERR_BAD_STRIDE;
     if (tstrides[0] < 0 || tstrides[1] < 0) return CE_ERR_BAD_STRIDE;
@@ -335,6 +336,9 @@ ce_status bwd_common(const void* logits, int dtype, int64_t dim0, int64_t dim1, 
     const int64_t N = dim0 * dim1;
     if (N > 0 && (!logits || !targets || !lse || !grad)) return CE_ERR_INVALID_ARG;
     if (N > 0 && reduce_loss && !n_non_ignore) return CE_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(logits) % elem_size(dtype) ||
+        reinterpret_cast<uintptr_t>(grad) % elem_size(dtype))
+        return CE_ERR_INVALID_ARG;
     if (strides[2] != 1 || strides[0] < 0 || strides[1] < 0) return CE_ERR_BAD_STRIDE;
     if (grad_strides[2] != 1 || grad_strides[0] < 0 || grad_strides[1] < 0) return CE_ERR_BAD_STRIDE;
     if (target_strides[0] < 0 || target_strides[1] < 0) return CE_ERR_BAD_STRIDE;
@@ -366,10 +370,11 @@ ce_status bwd_common(const void* logits, int dtype, int64_t dim0, int64_t dim1, 
     bp.n_dev = n_non_ignore;
     bp.vocab_offset = vocab_offset;
     bp.V_total = V_total;
-    bp.vec_ok = reinterpret_cast<uintptr_t>(logits) % 16 == 0 &&
-                reinterpret_cast<uintptr_t>(grad) % 16 == 0 && (V * es) % 16 == 0 &&
-                (strides[0] * es) % 16 == 0 && (strides[1] * es) % 16 == 0 &&
-                (grad_strides[0] * es) % 16 == 0 && (grad_strides[1] * es) % 16 == 0;
+    // 16-byte vectors when every gradient row sits at its logits row's offset
+    // from a 16-byte boundary (always so in place)
+    bp.vec_ok = (reinterpret_cast<uintptr_t>(logits) - reinterpret_cast<uintptr_t>(grad)) % 16 == 0 &&
+                ((strides[0] - grad_strides[0]) * es) % 16 == 0 &&
+                ((strides[1] - grad_strides[1]) * es) % 16 == 0;
     if (launch_bwd(bp, stream) != cudaSuccess) return CE_ERR_LAUNCH;
     return CE_OK;
 }
@@ -477,10 +482,10 @@ ce_status ce_vp_partials(const void* shard_logits, ce_dtype dtype, int64_t dim0,
     const int64_t N = dim0 * dim1;
     if (N > 0 && (!shard_logits || !targets || !partials)) return CE_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(partials) % 16) return CE_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(shard_logits) % elem_size(dtype)) return CE_ERR_INVALID_ARG;
     if (strides[2] != 1 || strides[0] < 0 || strides[1] < 0) return CE_ERR_BAD_STRIDE;
     if (target_strides[0] < 0 || target_strides[1] < 0) return CE_ERR_BAD_STRIDE;
     if (N == 0) return CE_OK;
-    const int es = elem_size(dtype);
     VpPartProblem vp;
     vp.logits = static_cast<const char*>(shard_logits);
     vp.dtype = dtype;
@@ -495,8 +500,6 @@ ce_status ce_vp_partials(const void* shard_logits, ce_dtype dtype, int64_t dim0,
     vp.ts1 = target_strides[1];
     vp.ignore_idx = ignore_idx;
     vp.part = reinterpret_cast<float4*>(partials);
-    vp.vec_ok = reinterpret_cast<uintptr_t>(shard_logits) % 16 == 0 && (V_shard * es) % 16 == 0 &&
-                (strides[0] * es) % 16 == 0 && (strides[1] * es) % 16 == 0;
     if (launch_vp_partials(vp, static_cast<cudaStream_t>(stream)) != cudaSuccess) return CE_ERR_LAUNCH;
     return CE_OK;
 }

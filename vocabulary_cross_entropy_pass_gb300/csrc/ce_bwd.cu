@@ -7,12 +7,14 @@
 // pitfall 3, smoothing spread over all V classes), g the row's upstream
 // scale: dloss/n for the mean, dloss[r] per row.  Ignored and out-of-range
 // rows get zeros.  One read of the logits and one write of the gradient per
-// element, no reduction: a plain streaming kernel, 16-byte vectors when the
-// rows allow, element by element otherwise.  The gradient may overwrite the
+// element, no reduction: a plain streaming kernel, 16-byte vectors between
+// a scalar head and tail when the gradient rows sit at the logits rows'
+// offset from a 16-byte boundary, element by element otherwise.  The gradient may overwrite the
 // logits (TENPU "Parallel Cross Entropy (Triton)" #29 section 6, in-place
 // staging) or go to a separate tensor.
 #include "ce_device.cuh"
 #include "ce_internal.h"
+#include "ce_span.cuh"
 
 namespace gbce {
 namespace {
@@ -36,6 +38,9 @@ struct BwdArgs {
     int64_t voff, Vtot;    // vocabulary offset of column 0, and the size targets index
 };
 
+// Rows of the logits and the gradient at the same offset from a 16-byte
+// boundary (always so in place): each chunk's head and tail one element per
+// thread, its body in 16-byte vectors.
 template <typename T>
 __global__ void __launch_bounds__(kBwdThreads) ce_bwd_vec_kernel(const __grid_constant__ BwdArgs p) {
     using VT = Vec<T>;
@@ -49,13 +54,17 @@ __global__ void __launch_bounds__(kBwdThreads) ce_bwd_vec_kernel(const __grid_co
         const int64_t c = b - r * p.nchunks;
         const int64_t i = r / p.dim1, j = r - i * p.dim1;
         const int64_t y = __ldg(p.targets + i * p.ts0 + j * p.ts1);
-        const uint4* src = reinterpret_cast<const uint4*>(p.logits + (i * p.s0 + j * p.s1) * ES);
-        uint4* dst = reinterpret_cast<uint4*>(p.grad + (i * p.gs0 + j * p.gs1) * ES);
-        const int64_t v0 = c * p.chunk / VEC;
-        const int64_t v1 = min(p.V, (c + 1) * p.chunk) / VEC;
+        const char* srow = p.logits + (i * p.s0 + j * p.s1) * ES;
+        char* drow = p.grad + (i * p.gs0 + j * p.gs1) * ES;
+        const int64_t e0 = c * p.chunk, e1 = min(p.V, (c + 1) * p.chunk);
+        const Span16 sp = span16<ES>(srow, e0, e1);
+        const int64_t ee = span16_edge(sp, e0, e1, threadIdx.x);
+        const uint4* src = reinterpret_cast<const uint4*>(srow + sp.h1 * ES);
+        uint4* dst = reinterpret_cast<uint4*>(drow + sp.h1 * ES);
         if (y == p.ignore_idx || y < 0 || y >= p.Vtot) {
+            if (ee >= 0) VT::store1(drow + ee * ES, 0.f);
             const uint4 z = make_uint4(0, 0, 0, 0);
-            for (int64_t v = v0 + threadIdx.x; v < v1; v += kBwdThreads) stg128_stream(dst + v, z);
+            for (int64_t v = threadIdx.x; v < sp.nv; v += kBwdThreads) stg128_stream(dst + v, z);
             continue;
         }
         float g;
@@ -65,22 +74,27 @@ __global__ void __launch_bounds__(kBwdThreads) ce_bwd_vec_kernel(const __grid_co
             g = p.dloss ? __ldg(p.dloss + r) : 1.f;
         const float nll = -__ldg(p.lse + r) * kLog2e;
         const float bb = g * p.a_over_v;
-        const float2 NL = make_float2(nll, nll), G2 = make_float2(g, g), NB = make_float2(-bb, -bb);
-        const int64_t yl = y - p.voff;  // the target's column in these logits
-        const int64_t vy = (yl >= 0 && yl < p.V) ? yl / VEC : -1;
-        const int ey = (int)(yl >= 0 ? yl % VEC : 0);
         const float hit = g * (1.f - p.a);
-        for (int64_t vb = v0 + threadIdx.x; vb < v1; vb += kBwdThreads * kBwdVecs) {
+        const int64_t yl = y - p.voff;  // the target's column in these logits
+        if (ee >= 0) {
+            const float x = VT::load1(srow + ee * ES);
+            float o = fmaf(ex2_approx(fmaf(x, kLog2e, nll)), g, -bb);
+            if (ee == yl) o -= hit;
+            VT::store1(drow + ee * ES, o);
+        }
+        const float2 NL = make_float2(nll, nll), G2 = make_float2(g, g), NB = make_float2(-bb, -bb);
+        const int64_t yb = yl - sp.h1;  // the target's place in the body
+        for (int64_t vb = threadIdx.x; vb < sp.nv; vb += kBwdThreads * kBwdVecs) {
             uint4 raw[kBwdVecs];
 #pragma unroll
             for (int u = 0; u < kBwdVecs; ++u) {
                 const int64_t v = vb + (int64_t)u * kBwdThreads;
-                if (v < v1) raw[u] = __ldcs(src + v);
+                if (v < sp.nv) raw[u] = __ldcs(src + v);
             }
 #pragma unroll
             for (int u = 0; u < kBwdVecs; ++u) {
                 const int64_t v = vb + (int64_t)u * kBwdThreads;
-                if (v < v1) {
+                if (v < sp.nv) {
                     float2 x[PP], o[PP];
                     VT::unpack2(raw[u], x);
 #pragma unroll
@@ -88,7 +102,8 @@ __global__ void __launch_bounds__(kBwdThreads) ce_bwd_vec_kernel(const __grid_co
                         const float2 e = __ffma2_rn(x[q], L2, NL);
                         o[q] = __ffma2_rn(make_float2(ex2_approx(e.x), ex2_approx(e.y)), G2, NB);
                     }
-                    if (v == vy) {
+                    const int64_t ey = yb - v * VEC;
+                    if (ey >= 0 && ey < VEC) {
 #pragma unroll
                         for (int q = 0; q < PP; ++q) {
                             if (2 * q == ey) o[q].x -= hit;
@@ -102,6 +117,8 @@ __global__ void __launch_bounds__(kBwdThreads) ce_bwd_vec_kernel(const __grid_co
     }
 }
 
+// Rows of the two tensors at different offsets from a 16-byte boundary:
+// element by element.
 template <typename T>
 __global__ void __launch_bounds__(kBwdThreads) ce_bwd_scalar_kernel(const __grid_constant__ BwdArgs p) {
     using VT = Vec<T>;

@@ -102,7 +102,7 @@ struct BwdProblem {
     int reduce;
     const float* dloss;
     const int64_t* n_dev;
-    bool vec_ok;               // every row of both tensors 16-byte aligned
+    bool vec_ok;               // gradient rows at the logits rows' offset from 16 bytes
     int64_t vocab_offset;      // global index of column 0 (a vocabulary shard), else 0
     int64_t V_total;           // vocabulary size the targets index, else V
 };
@@ -116,7 +116,6 @@ struct VpPartProblem {
     const int64_t* targets;
     int64_t ts0, ts1, ignore_idx;
     float4* part;
-    bool vec_ok;
 };
 struct VpCombineProblem {
     const float4* part;

@@ -9,13 +9,15 @@
 // split it describes -- then rereads its chunk and writes the gradient in
 // place.  The kernel boundary orders every read of a row before any write.
 //
-// This path takes any alignment and any row strides (scalar element loads);
-// the row and cluster paths need 16-byte aligned rows.  It reads the logits
+// This path takes any row alignment and any row strides: each chunk moves in
+// 16-byte vectors between a scalar head and tail (ce_span.cuh); the other
+// fused paths need 16-byte aligned rows.  It reads the logits
 // twice, so it is the fallback, the forced second implementation of the
 // vocabulary-split workloads, and the path of the class-weighted pass
 // (weights as in torch F.cross_entropy(weight=...)).
 #include "ce_device.cuh"
 #include "ce_internal.h"
+#include "ce_span.cuh"
 
 namespace gbce {
 namespace {
@@ -48,19 +50,12 @@ __device__ __forceinline__ void row_of(const SplitArgs& p, int64_t r, int64_t& y
     off = i * p.s0 + j * p.s1;
 }
 
-// Per-thread running statistics of one element (scalar path) or of one
-// 16-byte vector (vector path): a new maximum rescales the sum first.
-__device__ __forceinline__ void stats_push(float x, float& m, float& d) {
-    if (x > m) {
-        if (m != -INFINITY) d *= ex2_approx((m - x) * kLog2e);
-        m = x;
-    }
-    d += ex2_approx(fmaf(x, kLog2e, -m * kLog2e));
-}
-
 // Stage 1.  WT: the class-weighted pass, whose third statistic is
-// sum_j w_j x_j.  VECOK: rows 16-byte aligned, read in 16-byte vectors.
-template <typename T, bool WT, bool VECOK>
+// sum_j w_j x_j.  The chunk's elements outside whole 16-byte vectors (a row
+// that starts off a 16-byte boundary, a ragged chunk end) go one per thread;
+// the rest in 16-byte vectors, kSplitBatch loads in flight per thread and one
+// rescale per batch with a new max.
+template <typename T, bool WT>
 __global__ void __launch_bounds__(kSplitThreads) ce_split_stats_kernel(const __grid_constant__ SplitArgs p) {
     using VT = Vec<T>;
     constexpr int VEC = VT::kElems;
@@ -76,48 +71,48 @@ __global__ void __launch_bounds__(kSplitThreads) ce_split_stats_kernel(const __g
     const int64_t k1 = min(p.V, k0 + p.chunk);
     const char* row = p.logits + off * (int64_t)ES;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const Span16 sp = span16<ES>(row, k0, k1);
 
     float m = -INFINITY, d = 0.f, S = 0.f;
-    if (VECOK) {
-        // chunk boundaries are multiples of the vector length; kSplitBatch
-        // loads in flight per thread, one rescale per batch with a new max
-        const uint4* rv = reinterpret_cast<const uint4*>(row);
-        const int64_t vend = k1 / VEC;
-        for (int64_t vb = k0 / VEC + threadIdx.x; vb < vend; vb += kSplitThreads * kSplitBatch) {
-            uint4 raw[kSplitBatch];
-            float vm = -INFINITY;
+    const int64_t ee = span16_edge(sp, k0, k1, threadIdx.x);
+    if (ee >= 0) {
+        const float x = VT::load1(row + ee * ES);  // the thread's first element
+        if (x > m) {
+            m = x;
+            d = 1.f;  // exp(x - m); a -inf element adds nothing
+        }
+        S = WT ? __ldg(p.cw + ee) * x : x;
+    }
+    const uint4* rv = reinterpret_cast<const uint4*>(row + sp.h1 * ES);
+    const float* cwb = WT ? p.cw + sp.h1 : nullptr;
+    for (int64_t vb = threadIdx.x; vb < sp.nv; vb += kSplitThreads * kSplitBatch) {
+        uint4 raw[kSplitBatch];
+        float vm = -INFINITY;
 #pragma unroll
-            for (int u = 0; u < kSplitBatch; ++u) {
-                const int64_t v = vb + (int64_t)u * kSplitThreads;
-                if (v < vend) {
-                    raw[u] = __ldcs(rv + v);
-                    vm = fmaxf(vm, VT::vmax(raw[u]));
-                }
-            }
-            if (vm > m) {
-                if (m != -INFINITY) d *= ex2_approx((m - vm) * kLog2e);
-                m = vm;
-            }
-            const float nml = -m * kLog2e;
-#pragma unroll
-            for (int u = 0; u < kSplitBatch; ++u) {
-                const int64_t v = vb + (int64_t)u * kSplitThreads;
-                if (v < vend) {
-                    float x[VEC];
-                    VT::unpack(raw[u], x);
-#pragma unroll
-                    for (int e = 0; e < VEC; ++e) {
-                        d += ex2_approx(fmaf(x[e], kLog2e, nml));
-                        S = WT ? fmaf(__ldg(p.cw + v * VEC + e), x[e], S) : S + x[e];
-                    }
-                }
+        for (int u = 0; u < kSplitBatch; ++u) {
+            const int64_t v = vb + (int64_t)u * kSplitThreads;
+            if (v < sp.nv) {
+                raw[u] = __ldcs(rv + v);
+                vm = fmaxf(vm, VT::vmax(raw[u]));
             }
         }
-    } else {
-        for (int64_t v = k0 + threadIdx.x; v < k1; v += kSplitThreads) {
-            const float x = VT::load1(row + v * ES);
-            stats_push(x, m, d);
-            S = WT ? fmaf(__ldg(p.cw + v), x, S) : S + x;
+        if (vm > m) {
+            if (m != -INFINITY) d *= ex2_approx((m - vm) * kLog2e);
+            m = vm;
+        }
+        const float nml = -m * kLog2e;
+#pragma unroll
+        for (int u = 0; u < kSplitBatch; ++u) {
+            const int64_t v = vb + (int64_t)u * kSplitThreads;
+            if (v < sp.nv) {
+                float x[VEC];
+                VT::unpack(raw[u], x);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    d += ex2_approx(fmaf(x[e], kLog2e, nml));
+                    S = WT ? fmaf(__ldg(cwb + v * VEC + e), x[e], S) : S + x[e];
+                }
+            }
         }
     }
     Part q = warp_allreduce_part(Part{m, d, S});
@@ -134,8 +129,9 @@ __global__ void __launch_bounds__(kSplitThreads) ce_split_stats_kernel(const __g
 
 // Stage 2: the row's K partials combined by one warp in a fixed order (lane
 // l takes partials l, l+32, ... in turn, then a butterfly), then the loss and
-// the gradient of this CTA's chunk.
-template <typename T, bool GRAD, bool WT, bool VECOK>
+// the gradient of this CTA's chunk (head and tail one element per thread, the
+// body in 16-byte vectors, as in stage 1).
+template <typename T, bool GRAD, bool WT>
 __global__ void __launch_bounds__(kSplitThreads) ce_split_grad_kernel(const __grid_constant__ SplitArgs p) {
     using VT = Vec<T>;
     constexpr int VEC = VT::kElems;
@@ -151,18 +147,15 @@ __global__ void __launch_bounds__(kSplitThreads) ce_split_grad_kernel(const __gr
     const int64_t k0 = (int64_t)k * p.chunk;
     const int64_t k1 = min(p.V, k0 + p.chunk);
     char* row = p.logits + off * (int64_t)ES;
+    const Span16 sp = span16<ES>(row, k0, k1);
+    const int64_t ee = span16_edge(sp, k0, k1, threadIdx.x);
+    uint4* rv = reinterpret_cast<uint4*>(row + sp.h1 * ES);
 
     if (y == p.ignore_idx || y < 0 || y >= p.V) {
         if (GRAD) {
-            if (VECOK) {
-                const uint4 z = make_uint4(0, 0, 0, 0);
-                uint4* rv = reinterpret_cast<uint4*>(row);
-                for (int64_t v = k0 / VEC + threadIdx.x; v < k1 / VEC; v += kSplitThreads)
-                    stg128_stream(rv + v, z);
-            } else {
-                for (int64_t v = k0 + threadIdx.x; v < k1; v += kSplitThreads)
-                    VT::store1(row + v * ES, 0.f);
-            }
+            if (ee >= 0) VT::store1(row + ee * ES, 0.f);
+            const uint4 z = make_uint4(0, 0, 0, 0);
+            for (int64_t v = threadIdx.x; v < sp.nv; v += kSplitThreads) stg128_stream(rv + v, z);
         }
         if (k == 0 && threadIdx.x == 0) {
             p.loss[r] = (y == p.ignore_idx) ? 0.f : __int_as_float(0x7fc00000);
@@ -213,53 +206,50 @@ __global__ void __launch_bounds__(kSplitThreads) ce_split_grad_kernel(const __gr
     const float c = WT ? g * ((1.f - p.a) * wy + p.a_over_v * (float)(*p.wsum)) : g;
     const float ga = g * p.a_over_v;
     const float hit = g * (1.f - p.a) * wy;
-    if (VECOK) {
-        const float2 L2 = make_float2(kLog2e, kLog2e), NL = make_float2(nll, nll);
-        const float2 C2 = make_float2(c, c), NB = make_float2(-ga, -ga);
-        uint4* rv = reinterpret_cast<uint4*>(row);
-        const int64_t vend = k1 / VEC;
-        for (int64_t vb = k0 / VEC + threadIdx.x; vb < vend; vb += kSplitThreads * kSplitBatch) {
-            uint4 raw[kSplitBatch];
+    if (ee >= 0) {
+        const float x = VT::load1(row + ee * ES);
+        const float bj = WT ? ga * __ldg(p.cw + ee) : ga;
+        float o = fmaf(ex2_approx(fmaf(x, kLog2e, nll)), c, -bj);
+        if (ee == y) o -= hit;
+        VT::store1(row + ee * ES, o);
+    }
+    const float2 L2 = make_float2(kLog2e, kLog2e), NL = make_float2(nll, nll);
+    const float2 C2 = make_float2(c, c), NB = make_float2(-ga, -ga);
+    const float* cwb = WT ? p.cw + sp.h1 : nullptr;
+    const int64_t yb = y - sp.h1;  // the target's place in the body
+    for (int64_t vb = threadIdx.x; vb < sp.nv; vb += kSplitThreads * kSplitBatch) {
+        uint4 raw[kSplitBatch];
 #pragma unroll
-            for (int u = 0; u < kSplitBatch; ++u) {
-                const int64_t v = vb + (int64_t)u * kSplitThreads;
-                if (v < vend) raw[u] = __ldcs(rv + v);
+        for (int u = 0; u < kSplitBatch; ++u) {
+            const int64_t v = vb + (int64_t)u * kSplitThreads;
+            if (v < sp.nv) raw[u] = __ldcs(rv + v);
+        }
+#pragma unroll
+        for (int u = 0; u < kSplitBatch; ++u) {
+            const int64_t v = vb + (int64_t)u * kSplitThreads;
+            if (v >= sp.nv) continue;
+            float2 x[PP], o[PP];
+            VT::unpack2(raw[u], x);
+#pragma unroll
+            for (int q = 0; q < PP; ++q) {
+                const float2 e = __ffma2_rn(x[q], L2, NL);
+                const float2 pe = make_float2(ex2_approx(e.x), ex2_approx(e.y));
+                if (WT) {
+                    const float w0 = __ldg(cwb + v * VEC + 2 * q), w1 = __ldg(cwb + v * VEC + 2 * q + 1);
+                    o[q] = __ffma2_rn(pe, C2, make_float2(-ga * w0, -ga * w1));
+                } else {
+                    o[q] = __ffma2_rn(pe, C2, NB);
+                }
             }
-#pragma unroll
-            for (int u = 0; u < kSplitBatch; ++u) {
-                const int64_t v = vb + (int64_t)u * kSplitThreads;
-                if (v >= vend) continue;
-                float2 x[PP], o[PP];
-                VT::unpack2(raw[u], x);
+            const int64_t ey = yb - v * VEC;
+            if (ey >= 0 && ey < VEC) {
 #pragma unroll
                 for (int q = 0; q < PP; ++q) {
-                    const float2 e = __ffma2_rn(x[q], L2, NL);
-                    const float2 pe = make_float2(ex2_approx(e.x), ex2_approx(e.y));
-                    if (WT) {
-                        const float w0 = __ldg(p.cw + v * VEC + 2 * q), w1 = __ldg(p.cw + v * VEC + 2 * q + 1);
-                        o[q] = __ffma2_rn(pe, C2, make_float2(-ga * w0, -ga * w1));
-                    } else {
-                        o[q] = __ffma2_rn(pe, C2, NB);
-                    }
+                    if (2 * q == ey) o[q].x -= hit;
+                    if (2 * q + 1 == ey) o[q].y -= hit;
                 }
-                if (v == y / VEC) {
-                    const int ey = (int)(y % VEC);
-#pragma unroll
-                    for (int q = 0; q < PP; ++q) {
-                        if (2 * q == ey) o[q].x -= hit;
-                        if (2 * q + 1 == ey) o[q].y -= hit;
-                    }
-                }
-                stg128_stream(rv + v, VT::pack2(o));
             }
-        }
-    } else {
-        for (int64_t v = k0 + threadIdx.x; v < k1; v += kSplitThreads) {
-            const float x = VT::load1(row + v * ES);
-            const float bj = WT ? ga * __ldg(p.cw + v) : ga;
-            float o = fmaf(ex2_approx(fmaf(x, kLog2e, nll)), c, -bj);
-            if (v == y) o -= hit;
-            VT::store1(row + v * ES, o);
+            stg128_stream(rv + v, VT::pack2(o));
         }
     }
 }
@@ -294,30 +284,21 @@ cudaError_t launch_split_typed(const Problem& pb, const SplitPlan& plan, float4*
     const int64_t blocks = pb.N * plan.chunks;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const bool wt = pb.cw != nullptr;
-    // 16-byte vectors when every row and chunk boundary is 16-byte aligned
-    const bool vec = reinterpret_cast<uintptr_t>(pb.logits) % 16 == 0 &&
-                     (pb.s0 * (int64_t)sizeof(T)) % 16 == 0 && (pb.s1 * (int64_t)sizeof(T)) % 16 == 0 &&
-                     (pb.V * (int64_t)sizeof(T)) % 16 == 0 &&
-                     (plan.chunk * (int64_t)sizeof(T)) % 16 == 0;
     const unsigned gs = (unsigned)blocks, gr = (unsigned)(pb.grad ? blocks : pb.N);
-#define CE_SPLIT_LAUNCH(W, VK)                                                     \
-    do {                                                                           \
-        ce_split_stats_kernel<T, W, VK><<<gs, kSplitThreads, 0, s>>>(a);           \
-        cudaError_t e_ = cudaGetLastError();                                       \
-        if (e_ != cudaSuccess) return e_;                                          \
-        if (pb.grad)                                                               \
-            ce_split_grad_kernel<T, true, W, VK><<<gr, kSplitThreads, 0, s>>>(a);  \
-        else                                                                       \
-            ce_split_grad_kernel<T, false, W, VK><<<gr, kSplitThreads, 0, s>>>(a); \
+#define CE_SPLIT_LAUNCH(W)                                                     \
+    do {                                                                       \
+        ce_split_stats_kernel<T, W><<<gs, kSplitThreads, 0, s>>>(a);           \
+        cudaError_t e_ = cudaGetLastError();                                   \
+        if (e_ != cudaSuccess) return e_;                                      \
+        if (pb.grad)                                                           \
+            ce_split_grad_kernel<T, true, W><<<gr, kSplitThreads, 0, s>>>(a);  \
+        else                                                                   \
+            ce_split_grad_kernel<T, false, W><<<gr, kSplitThreads, 0, s>>>(a); \
     } while (0)
-    if (wt && vec)
-        CE_SPLIT_LAUNCH(true, true);
-    else if (wt)
-        CE_SPLIT_LAUNCH(true, false);
-    else if (vec)
-        CE_SPLIT_LAUNCH(false, true);
+    if (wt)
+        CE_SPLIT_LAUNCH(true);
     else
-        CE_SPLIT_LAUNCH(false, false);
+        CE_SPLIT_LAUNCH(false);
 #undef CE_SPLIT_LAUNCH
     return cudaGetLastError();
 }

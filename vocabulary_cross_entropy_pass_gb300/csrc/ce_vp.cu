@@ -18,6 +18,7 @@
 //     offset (ce_bwd.cu).
 #include "ce_device.cuh"
 #include "ce_internal.h"
+#include "ce_span.cuh"
 
 namespace gbce {
 namespace {
@@ -32,7 +33,6 @@ struct VpPartArgs {
     const int64_t* targets;
     int64_t ts0, ts1, ignore_idx;
     float4* part;                      // [N]
-    bool vec_ok;
 };
 
 // One CTA per row: a running (max, sum-exp, sum) per thread over 16-byte
@@ -63,53 +63,51 @@ __global__ void __launch_bounds__(kVpThreads, 6) ce_vp_partials_kernel(const __g
         const char* row = p.logits + (i * p.s0 + j * p.s1) * ES;
         float m = -INFINITY;
         float2 d2 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
-        if (p.vec_ok) {
-            const uint4* rv = reinterpret_cast<const uint4*>(row);
-            const int64_t nv = p.V / VEC;
-            for (int64_t vb = threadIdx.x; vb < nv; vb += kVpThreads * kVpBatch) {
-                uint4 raw[kVpBatch];
-                float vm = -INFINITY;
+        // head and tail (rows off a 16-byte boundary) one element per thread
+        const Span16 sp = span16<ES>(row, 0, p.V);
+        const int64_t ee = span16_edge(sp, 0, p.V, threadIdx.x);
+        if (ee >= 0) {  // the thread's first element: exp(x - m) = 1 (nothing for -inf)
+            const float x = VT::load1(row + ee * ES);
+            if (x > m) {
+                m = x;
+                d2.x = 1.f;
+            }
+            s2.x = x;
+        }
+        const uint4* rv = reinterpret_cast<const uint4*>(row + sp.h1 * ES);
+        for (int64_t vb = threadIdx.x; vb < sp.nv; vb += kVpThreads * kVpBatch) {
+            uint4 raw[kVpBatch];
+            float vm = -INFINITY;
 #pragma unroll
-                for (int u = 0; u < kVpBatch; ++u) {
-                    const int64_t v = vb + (int64_t)u * kVpThreads;
-                    if (v < nv) {
-                        raw[u] = __ldcs(rv + v);
-                        vm = fmaxf(vm, VT::vmax(raw[u]));
-                    }
-                }
-                if (vm > m) {
-                    if (m != -INFINITY) {
-                        const float c = ex2_approx((m - vm) * kLog2e);
-                        d2.x *= c;
-                        d2.y *= c;
-                    }
-                    m = vm;
-                }
-                const float nml = -m * kLog2e;
-                const float2 NM = make_float2(nml, nml);
-#pragma unroll
-                for (int u = 0; u < kVpBatch; ++u) {
-                    if (vb + (int64_t)u * kVpThreads < nv) {
-                        float2 x[PP];
-                        VT::unpack2(raw[u], x);
-#pragma unroll
-                        for (int q = 0; q < PP; ++q) {
-                            const float2 e = __ffma2_rn(x[q], L2, NM);
-                            d2 = __fadd2_rn(d2, make_float2(ex2_approx(e.x), ex2_approx(e.y)));
-                            s2 = __fadd2_rn(s2, x[q]);
-                        }
-                    }
+            for (int u = 0; u < kVpBatch; ++u) {
+                const int64_t v = vb + (int64_t)u * kVpThreads;
+                if (v < sp.nv) {
+                    raw[u] = __ldcs(rv + v);
+                    vm = fmaxf(vm, VT::vmax(raw[u]));
                 }
             }
-        } else {
-            for (int64_t e = threadIdx.x; e < p.V; e += kVpThreads) {
-                const float x = VT::load1(row + e * ES);
-                if (x > m) {
-                    if (m != -INFINITY) d2.x *= ex2_approx((m - x) * kLog2e);
-                    m = x;
+            if (vm > m) {
+                if (m != -INFINITY) {
+                    const float c = ex2_approx((m - vm) * kLog2e);
+                    d2.x *= c;
+                    d2.y *= c;
                 }
-                d2.x += ex2_approx(fmaf(x, kLog2e, -m * kLog2e));
-                s2.x += x;
+                m = vm;
+            }
+            const float nml = -m * kLog2e;
+            const float2 NM = make_float2(nml, nml);
+#pragma unroll
+            for (int u = 0; u < kVpBatch; ++u) {
+                if (vb + (int64_t)u * kVpThreads < sp.nv) {
+                    float2 x[PP];
+                    VT::unpack2(raw[u], x);
+#pragma unroll
+                    for (int q = 0; q < PP; ++q) {
+                        const float2 e = __ffma2_rn(x[q], L2, NM);
+                        d2 = __fadd2_rn(d2, make_float2(ex2_approx(e.x), ex2_approx(e.y)));
+                        s2 = __fadd2_rn(s2, x[q]);
+                    }
+                }
             }
         }
         Part q = warp_allreduce_part(Part{m, d2.x + d2.y, s2.x + s2.y});
@@ -190,7 +188,6 @@ cudaError_t launch_vp_partials(const VpPartProblem& vp, cudaStream_t s) {
     a.ts1 = vp.ts1;
     a.ignore_idx = vp.ignore_idx;
     a.part = vp.part;
-    a.vec_ok = vp.vec_ok;
     switch (vp.dtype) {
         case CE_F32:
             return launch_vp_partials_typed<float>(a, s);
