@@ -529,7 +529,8 @@ def run_ours(args, w, rank: int, world: int, dist) -> None:
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded, see vocabulary_cross_entropy_pass_gb300/workloads.py)",
-        "config": config_of(w, args) | {"path": {1: "row", 2: "cluster", 3: "two_stage", 4: "stream", 5: "warp"}[path],
+        "config": config_of(w, args) | {"path": {1: "row", 2: "cluster", 3: "two_stage", 4: "stream",
+                                                 5: "warp", 6: "vecrow"}[path],
                                          "vocab_chunks": chunks},
         "hbm_gbs_formula": nbytes * args.steps * world / (ms / 1e3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],

@@ -98,8 +98,12 @@ typedef enum {
                               the ring by the ring's last tiles still in shared memory.
                               Default shape: rows up to 128 KB 16 KB tiles, 6 deep, two
                               CTAs per SM; wider rows 32 KB tiles, 6 deep, one CTA */
-    CE_PATH_WARP = 5       /* one warp per row, the row held in one shared-memory tile
+    CE_PATH_WARP = 5,      /* one warp per row, the row held in one shared-memory tile
                               (rows up to 32 KB) */
+    CE_PATH_VECROW = 6     /* rows off the 16-byte grid (any alignment): one CTA per row
+                              of a persistent grid (two per SM), two passes of plain
+                              16-byte loads between a scalar head and tail, the second
+                              served by L2; no vocabulary split, no class weights */
 } ce_path;
 
 typedef struct {
@@ -336,8 +340,9 @@ ce_status ce_wait_timeout_probe(void* workspace, size_t workspace_bytes, void* s
 const char* ce_status_string(ce_status status);
 
 /* Path the planner would take for these arguments (host only): CE_PATH_ROW,
- * CE_PATH_CLUSTER, CE_PATH_TWO_STAGE, CE_PATH_STREAM or CE_PATH_WARP, with the vocabulary chunk count in
- * *chunks_out (host pointer, may be NULL).  Returns -1 for arguments
+ * CE_PATH_CLUSTER, CE_PATH_TWO_STAGE, CE_PATH_STREAM, CE_PATH_WARP or
+ * CE_PATH_VECROW, with the vocabulary chunk count in *chunks_out (host
+ * pointer, may be NULL).  Returns -1 for arguments
  * ce_fwd_bwd would reject, -2 for a forced path that cannot run them. */
 int ce_plan_path(const void* logits, ce_dtype dtype, int64_t dim0, int64_t dim1, int64_t V,
                  const int64_t strides[3], const ce_options* opts, int* chunks_out);

@@ -102,7 +102,7 @@ def test_host_validation_rejects_before_launch(lib):
     assert _call(lib, opts=ctypes.byref(o)) == 1
     o = _lib.make_options(tune_l2_keep=3)
     assert _call(lib, opts=ctypes.byref(o)) == 1
-    o = _lib.make_options(force_path=6)
+    o = _lib.make_options(force_path=7)
     assert _call(lib, opts=ctypes.byref(o)) == 1
 
 
@@ -130,8 +130,13 @@ def test_planner(lib):
     assert plan(4095, force_path=5)[0] == -2       # and so does the warp path
     assert plan(65536, num_vocab_chunks=8, force_path=2) == (2, 8)
     assert plan(65536, num_vocab_chunks=8, force_path=3) == (3, 8)
-    assert plan(4095)[0] == 3                      # rows not 16-byte aligned
-    assert plan(4096, base=0x1002)[0] == 3         # base not 16-byte aligned
+    assert plan(4095) == (6, 1)                    # rows not 16-byte aligned: plain loads
+    assert plan(4096, base=0x1002) == (6, 1)       # base not 16-byte aligned
+    assert plan(100277) == (6, 1)
+    assert plan(4096, force_path=6) == (6, 1)      # aligned rows on request
+    assert plan(4095, num_vocab_chunks=4) == (3, 4)  # a split asked for: two-stage
+    assert plan(4095, force_path=3) == (3, 1)
+    assert plan(4095, force_path=6, num_vocab_chunks=2)[0] == -2
     assert plan(4096, force_path=1, base=0x1002)[0] == -2
     assert plan(4_000_000)[0] == 4                 # any width streams
     assert plan(4_000_000, force_path=2)[0] == -2  # too wide for 16 CTAs

@@ -106,7 +106,7 @@ def test_empty_chunks():
     harness.run_gpu_vs_oracle(w, force_path=2, num_vocab_chunks=16)
 
 
-@pytest.mark.parametrize("path", [0, 1, 3, 4, 5])
+@pytest.mark.parametrize("path", [0, 1, 3, 4, 5, 6])
 def test_all_ignored_mean_is_nan(path):
     x = torch.randn(3, 4, 1024, device=DEV).to(torch.bfloat16)
     t = torch.full((3, 4), -100, dtype=torch.int64, device=DEV)
@@ -116,7 +116,7 @@ def test_all_ignored_mean_is_nan(path):
     assert torch.all(x == 0)
 
 
-@pytest.mark.parametrize("path", [0, 1, 2, 3, 4, 5])
+@pytest.mark.parametrize("path", [0, 1, 2, 3, 4, 5, 6])
 def test_out_of_range_target_sets_error(path):
     w = wl.Workload("oor", 1, 6, 8192, "bf16", sigma=2.0, ignore_frac=0.0, seed=71)
     x = wl.logits(w)
@@ -165,7 +165,8 @@ def test_zero_rows():
 @pytest.mark.parametrize("name,path", [("c5_bsv128000_bf16_ls", 0), ("c3_bsv32000_bf16_spiked", 0),
                                        ("c2_sbv8192_bf16", 0), ("c4_bsv65536_bf16_split8", 3),
                                        ("c5_bsv128000_bf16_ls", 2), ("c1_bsv4096_f32", 1),
-                                       ("c1_bsv4096_f32", 5)])
+                                       ("c1_bsv4096_f32", 5), ("c1_bsv4096_f32", 6),
+                                       ("c5_bsv128000_bf16_ls", 6)])
 def test_fwd_only_matches(name, path):
     w = wl.WORKLOADS[name]
     x = wl.logits(w)
@@ -189,7 +190,8 @@ def test_fwd_only_matches(name, path):
 
 
 @pytest.mark.parametrize("name,path", [("c5_bsv128000_bf16_ls", 0), ("c2_sbv8192_bf16", 0),
-                                       ("c2_sbv8192_bf16", 1), ("c4_bsv65536_bf16_split8", 3)])
+                                       ("c2_sbv8192_bf16", 1), ("c4_bsv65536_bf16_split8", 3),
+                                       ("c5_bsv128000_bf16_ls", 6)])
 def test_mean_is_deterministic(name, path):
     w = wl.WORKLOADS[name]
     x = wl.logits(w).to(DEV)
@@ -317,12 +319,12 @@ def test_bounded_wait_reports_timeout():
     harness.run_gpu_vs_oracle(w)  # the context is still usable
 
 
-@pytest.mark.parametrize("V,path", [(1 << 20, pkg.CE_PATH_STREAM), ((1 << 20) + 3, pkg.CE_PATH_TWO_STAGE),
+@pytest.mark.parametrize("V,path", [(1 << 20, pkg.CE_PATH_STREAM), ((1 << 20) + 3, pkg.CE_PATH_VECROW),
                                     (256000, pkg.CE_PATH_STREAM), (200000, pkg.CE_PATH_STREAM)])
 @pytest.mark.parametrize("reduce", [True, False])
 def test_very_wide_rows(V, path, reduce):
     """Rows of a million columns (2 MB of bf16 each: 64 ring tiles per pass on
-    the stream path; an odd width goes to the two-stage kernels), and rows of
+    the stream path; an odd width goes to the plain-load kernel), and rows of
     16 and 13 tiles (the last one partial) -- all wide enough for pass 2 to
     take the ring's last tiles from shared memory -- against the oracle."""
     w = wl.WORKLOADS["c5_bsv128000_bf16_ls"].with_(
@@ -346,14 +348,36 @@ def test_warp_path_two_tiles_by_default():
                                                      (50257, "f16", 0.0, False, 0.2),
                                                      (100003, "f32", 0.2, True, 0.0),
                                                      (16387, "bf16", 0.0, False, 0.05)])
-def test_unaligned_rows_two_stage(V, dtype, a, reduce, ignore):
-    """Odd widths put every row at its own offset from a 16-byte boundary; the
-    two-stage kernels read each chunk as a scalar head, 16-byte vectors and a
-    scalar tail (several chunks per row, the last one ragged)."""
+@pytest.mark.parametrize("path", [pkg.CE_PATH_AUTO, pkg.CE_PATH_TWO_STAGE])
+def test_unaligned_rows(V, dtype, a, reduce, ignore, path):
+    """Odd widths put every row at its own offset from a 16-byte boundary.
+    The planner sends them to the plain-load kernel (one CTA per row, a
+    scalar head, 16-byte vectors, a scalar tail); the two-stage kernels read
+    each chunk the same way (several chunks per row, the last one ragged)."""
     w = wl.Workload(f"unaligned_{V}", 2, 17, V, dtype, sigma=2.0, ignore_frac=ignore,
                     label_smoothing=a, reduce_loss=reduce, seed=V % 1000)
-    assert pkg.ce_plan_path(wl.logits(w).to(DEV))[0] == pkg.CE_PATH_TWO_STAGE
-    harness.run_gpu_vs_oracle(w, per_row_dloss=not reduce)
+    if path == pkg.CE_PATH_AUTO:
+        assert pkg.ce_plan_path(wl.logits(w).to(DEV))[0] == pkg.CE_PATH_VECROW
+    harness.run_gpu_vs_oracle(w, force_path=path, per_row_dloss=not reduce)
+
+
+@pytest.mark.parametrize("threads,cap", [(256, 0), (512, 1), (256, 1)])
+def test_vecrow_shapes(threads, cap):
+    """The plain-load kernel's other CTA shapes (256 threads three per SM,
+    and grids capped to one CTA per SM, so each CTA takes many rows)."""
+    w = wl.Workload("vecrow_shapes", 1, 700, 20011, "bf16", sigma=2.0, ignore_frac=0.1,
+                    label_smoothing=0.1, reduce_loss=True, seed=threads + cap)
+    x = wl.logits(w)
+    t = wl.targets(w)
+    ref = harness.oracle_run(w, x, t)
+    xd = x.to(DEV)
+    opts = pkg.make_options(force_path=pkg.CE_PATH_VECROW, tune_threads=threads,
+                            tune_ctas_per_sm=cap)
+    loss = pkg.ce_fwd_bwd(xd, t.to(DEV), label_smoothing=0.1, reduce_loss=True, opts=opts)
+    harness.check_loss(loss.cpu().numpy().reshape(-1), ref["loss"], "bf16")
+    g = xd.float().cpu().numpy().reshape(w.N, w.V).astype(np.float64)
+    excess, _ = harness.grad_errors(g, ref["grad"], "bf16")
+    assert excess <= 0.0
 
 
 @pytest.mark.parametrize("K", [3, 7, 16])
@@ -366,10 +390,12 @@ def test_unaligned_rows_short_chunks(K):
 
 
 @pytest.mark.parametrize("dtype,shift", [("bf16", 1), ("bf16", 5), ("f16", 3), ("f32", 1)])
-def test_shifted_view_rows(dtype, shift):
+@pytest.mark.parametrize("path", [pkg.CE_PATH_AUTO, pkg.CE_PATH_TWO_STAGE])
+def test_shifted_view_rows(dtype, shift, path):
     """An aligned width read through a view that starts `shift` elements
-    into each padded row: the rows leave the 16-byte grid, the two-stage
-    kernels take them, and the padding on both sides stays untouched."""
+    into each padded row: the rows leave the 16-byte grid, the plain-load
+    kernel (or the two-stage kernels, forced) takes them, and the padding on
+    both sides stays untouched."""
     V, pad = 32000, 9
     w = wl.Workload("shifted", 2, 5, V, dtype, sigma=2.0, label_smoothing=0.1, seed=50 + shift)
     x = wl.logits(w)
@@ -378,8 +404,9 @@ def test_shifted_view_rows(dtype, shift):
     t = wl.targets(w)
     bd = buf.to(DEV)
     view = bd[:, :, shift:shift + V]
-    assert pkg.ce_plan_path(view)[0] == pkg.CE_PATH_TWO_STAGE
-    loss = pkg.ce_fwd_bwd(view, t.to(DEV), label_smoothing=0.1)
+    if path == pkg.CE_PATH_AUTO:
+        assert pkg.ce_plan_path(view)[0] == pkg.CE_PATH_VECROW
+    loss = pkg.ce_fwd_bwd(view, t.to(DEV), label_smoothing=0.1, force_path=path)
     ref = harness.oracle_run(w, x, t)
     harness.check_loss(loss.cpu().numpy(), ref["loss"], dtype, "shifted")
     g = view.float().cpu().numpy().reshape(w.N, V).astype(np.float64)

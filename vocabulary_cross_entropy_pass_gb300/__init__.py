@@ -26,14 +26,16 @@ import torch
 
 from . import _lib
 from ._lib import (CE_PATH_AUTO, CE_PATH_CLUSTER, CE_PATH_ROW, CE_PATH_STREAM,
-                   CE_PATH_TWO_STAGE, CE_PATH_WARP, CEError, ce_options, make_options)
+                   CE_PATH_TWO_STAGE, CE_PATH_VECROW, CE_PATH_WARP, CEError, ce_options,
+                   make_options)
 
 __all__ = ["ce_fwd_bwd", "ce_fwd_bwd_noalloc", "ce_fwd_only", "ce_bwd", "parallel_cross_entropy",
            "ce_vp_partials", "ce_vp_combine", "ce_vp_bwd", "vocab_parallel_cross_entropy",
            "ce_linear_fwd_bwd", "ce_workspace_bytes", "ce_get_error", "ce_status_string",
            "ce_wait_timeout_probe",
            "ce_plan_path", "CEError", "make_options", "ce_options",
-           "CE_PATH_AUTO", "CE_PATH_ROW", "CE_PATH_CLUSTER", "CE_PATH_TWO_STAGE", "CE_PATH_STREAM", "CE_PATH_WARP"]
+           "CE_PATH_AUTO", "CE_PATH_ROW", "CE_PATH_CLUSTER", "CE_PATH_TWO_STAGE", "CE_PATH_STREAM",
+           "CE_PATH_WARP", "CE_PATH_VECROW"]
 
 _DTYPE = {torch.float32: _lib.CE_F32, torch.bfloat16: _lib.CE_BF16, torch.float16: _lib.CE_F16}
 _LAYOUT = {"bsv": _lib.CE_LAYOUT_BSV, "sbv": _lib.CE_LAYOUT_SBV}

@@ -16,8 +16,8 @@ LIB_PATH = os.path.join(HERE, "libgbce.so")
 
 CE_F32, CE_BF16, CE_F16 = 0, 1, 2
 CE_LAYOUT_BSV, CE_LAYOUT_SBV = 0, 1
-CE_PATH_AUTO, CE_PATH_ROW, CE_PATH_CLUSTER, CE_PATH_TWO_STAGE, CE_PATH_STREAM, CE_PATH_WARP = (
-    0, 1, 2, 3, 4, 5)
+(CE_PATH_AUTO, CE_PATH_ROW, CE_PATH_CLUSTER, CE_PATH_TWO_STAGE, CE_PATH_STREAM, CE_PATH_WARP,
+ CE_PATH_VECROW) = (0, 1, 2, 3, 4, 5, 6)
 CE_DEVERR_TARGET_RANGE, CE_DEVERR_TIMEOUT = 0x1, 0x2
 
 STATUS = {

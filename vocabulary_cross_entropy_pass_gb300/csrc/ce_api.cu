@@ -27,11 +27,12 @@ constexpr int kMaxCluster = 16;
 constexpr size_t kSmemLimit = 227 * 1024;
 
 struct Plan {
-    int path;  // CE_PATH_ROW / CLUSTER / TWO_STAGE / STREAM / WARP, or < 0 on error
+    int path;  // CE_PATH_ROW / CLUSTER / TWO_STAGE / STREAM / WARP / VECROW, or < 0 on error
     FusedPlan fused;
     SplitPlan split;
     StreamPlan stream;
     RowsPlan rows;
+    VecRowPlan vecrow;
 };
 
 // Warp-per-row kernel: the row must fit one tile of 16 or 32 KB; each of its
@@ -75,7 +76,7 @@ bool opts_clean(const ce_options* o) {
     for (int i = 0; i < 2; ++i)
         if (o->reserved[i] != 0) return false;
     if (o->tune_tile_kb != 0 && o->tune_tile_kb != 16 && o->tune_tile_kb != 32) return false;
-    if (o->force_path < 0 || o->force_path > CE_PATH_WARP) return false;
+    if (o->force_path < 0 || o->force_path > CE_PATH_VECROW) return false;
     if (o->num_vocab_chunks < 0) return false;
     if (o->tune_threads != 0 && o->tune_threads != 256 && o->tune_threads != 512) return false;
     if (o->tune_stages < 0 || o->tune_stages > 12 || o->tune_stages == 1) return false;
@@ -171,6 +172,15 @@ Plan make_plan(const Problem& p, const ce_options* o) {
         pl.path = CE_PATH_WARP;
         return pl;
     }
+    // Rows off the 16-byte grid (TMA cannot copy them): plain 16-byte loads,
+    // one CTA per row, the second pass from L2.  A requested vocabulary split
+    // still goes to the two-stage kernels.
+    if (force == CE_PATH_VECROW || (force == CE_PATH_AUTO && !aligned && K == 0)) {
+        pl.path = (K == 0 && p.V <= 0x7fffffffLL) ? CE_PATH_VECROW : -2;
+        pl.vecrow.threads = (o && o->tune_threads) ? o->tune_threads : 512;
+        pl.vecrow.ctas_per_sm_cap = o ? o->tune_ctas_per_sm : 0;
+        return pl;
+    }
     const bool stream_auto = force == CE_PATH_AUTO && aligned && K == 0;
     if (force == CE_PATH_STREAM || stream_auto) {
         // Rows up to 128 KB: 16 KB tiles 6 deep, two CTAs per SM (twice the
@@ -248,6 +258,7 @@ cudaError_t launch_planned(const Problem& pb, const Plan& pl, float4* parts, cud
     if (pl.path == CE_PATH_TWO_STAGE) return launch_split(pb, pl.split, parts, s);
     if (pl.path == CE_PATH_STREAM) return launch_stream(pb, pl.stream, s);
     if (pl.path == CE_PATH_WARP) return launch_rows(pb, pl.rows, s);
+    if (pl.path == CE_PATH_VECROW) return launch_vecrow(pb, pl.vecrow, s);
     return launch_fused(pb, pl.fused, s);
 }
 
@@ -615,7 +626,8 @@ int ce_plan_path(const void* logits, ce_dtype dtype, int64_t dim0, int64_t dim1,
     if (pl.path < 0) return pl.path;
     if (chunks_out)
         *chunks_out = pl.path == CE_PATH_TWO_STAGE                            ? pl.split.chunks
-                      : (pl.path == CE_PATH_STREAM || pl.path == CE_PATH_WARP) ? 1
+                      : (pl.path == CE_PATH_STREAM || pl.path == CE_PATH_WARP ||
+                         pl.path == CE_PATH_VECROW)                             ? 1
                                                                                 : pl.fused.cluster;
     return pl.path;
 }

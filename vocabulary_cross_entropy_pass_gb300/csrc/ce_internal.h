@@ -82,6 +82,12 @@ struct RowsPlan {
     int ctas_per_sm_cap;       // 0 = no cap
 };
 
+// Plan of the kernel for rows off the 16-byte grid.
+struct VecRowPlan {
+    int threads;               // 512 (two CTAs per SM) or 256 (three)
+    int ctas_per_sm_cap;       // 0 = no cap
+};
+
 // Plan of the two-stage kernels.
 struct SplitPlan {
     int chunks;                // K
@@ -143,6 +149,7 @@ cudaError_t launch_reduce_mean(const Problem& p, float* loss_out, cudaStream_t s
 cudaError_t launch_fused(const Problem& p, const FusedPlan& plan, cudaStream_t s);
 cudaError_t launch_stream(const Problem& p, const StreamPlan& plan, cudaStream_t s);
 cudaError_t launch_rows(const Problem& p, const RowsPlan& plan, cudaStream_t s);
+cudaError_t launch_vecrow(const Problem& p, const VecRowPlan& plan, cudaStream_t s);
 cudaError_t launch_bwd(const BwdProblem& bp, cudaStream_t s);
 cudaError_t launch_vp_partials(const VpPartProblem& vp, cudaStream_t s);
 cudaError_t launch_vp_combine(const VpCombineProblem& vc, cudaStream_t s);
