@@ -34,7 +34,17 @@ if ROOT not in sys.path:
 
 METRIC = "CE fwd+bwd tokens/s at V=128000 bf16; achieved HBM GB/s vs GB300 peak"
 DEFAULT_WORKLOAD = "c5t_bsv128000_bf16"
-KERNELS_PER_STEP = {1: 3, 2: 3, 3: 4, 4: 2, 5: 2}   # count + main (+ second stage) (+ mean)
+
+
+def kernels_per_step(path: int, reduce: bool) -> int:
+    """The library's launches in one fused step: the count kernel, the main
+    kernel (two on the two-stage path), and the mean kernel for a mean on
+    the paths that do not take it in their last CTA (stream, warp)."""
+    main = 2 if path == 3 else 1
+    mean = 1 if reduce and path not in (4, 5) else 0
+    return 1 + main + mean
+
+
 CLOCK_FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
                 "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
                 "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
@@ -547,7 +557,7 @@ def run_ours(args, w, rank: int, world: int, dist) -> None:
                 "how": "ce_fwd_bwd per step on inputs copied from pinned host memory "
                        "(two device buffers: the copy of step k+1 overlaps the pass of "
                        "step k) and the loss read back"},
-        "gpu_launches": KERNELS_PER_STEP[path] * args.steps,
+        "gpu_launches": kernels_per_step(path, w.reduce_loss) * args.steps,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)

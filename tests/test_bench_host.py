@@ -19,6 +19,18 @@ def test_pass_bytes_throughput_workload():
     assert bench.pass_bytes(16384, 128000, 2) == 8_388_739_072
 
 
+def test_kernels_per_step():
+    # count kernel + main kernel(s) + the mean kernel where the path does not
+    # take the mean in its last CTA
+    assert bench.kernels_per_step(4, True) == 2   # stream
+    assert bench.kernels_per_step(5, True) == 2   # warp
+    assert bench.kernels_per_step(3, True) == 4   # two-stage: two kernels + mean
+    assert bench.kernels_per_step(3, False) == 3
+    assert bench.kernels_per_step(6, True) == 3   # plain-load rows
+    assert bench.kernels_per_step(6, False) == 2
+    assert bench.kernels_per_step(1, False) == 2
+
+
 def _free_port():
     s = socket.socket()
     s.bind(("127.0.0.1", 0))

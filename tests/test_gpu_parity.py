@@ -9,7 +9,7 @@ from vocabulary_cross_entropy_pass_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
 
-AUTO, ROW, CLUSTER, TWO, STREAM, WARP = 0, 1, 2, 3, 4, 5
+AUTO, ROW, CLUSTER, TWO, STREAM, WARP, VECROW = 0, 1, 2, 3, 4, 5, 6
 
 CASES = [
     ("c1_bsv4096_f32", AUTO, None), ("c1_bsv4096_f32", TWO, None),
@@ -27,6 +27,8 @@ CASES = [
     ("c5_bsv128000_bf16_ls", TWO, None), ("c5_bsv128000_bf16_ls", CLUSTER, None),
     ("c5_bsv128000_f32", AUTO, None), ("c5_bsv128000_f32_ls", AUTO, None),
     ("c5_bsv128000_f32_ls", TWO, None), ("c5_bsv128000_f32_ls", CLUSTER, None),
+    ("c1_bsv4096_f32", VECROW, None), ("c2_sbv8192_bf16", VECROW, None),
+    ("c3h_bsv32000_f16_spiked", VECROW, None), ("c5_bsv128000_bf16_ls", VECROW, None),
 ]
 
 
@@ -53,7 +55,8 @@ def test_planner_paths():
     x = torch.empty(2, 3, 128000, dtype=torch.bfloat16, device=dev)
     assert pkg.ce_plan_path(x)[0] == STREAM
     x = torch.empty(2, 3, 4095, dtype=torch.bfloat16, device=dev)  # rows not 16-byte aligned
-    assert pkg.ce_plan_path(x)[0] == TWO
+    assert pkg.ce_plan_path(x)[0] == VECROW
+    assert pkg.ce_plan_path(x, pkg.make_options(num_vocab_chunks=2)) == (TWO, 2)
     opts = pkg.make_options(force_path=CLUSTER, num_vocab_chunks=8)
     x = torch.empty(2, 256, 65536, dtype=torch.bfloat16, device=dev)
     assert pkg.ce_plan_path(x, opts) == (CLUSTER, 8)
