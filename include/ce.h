@@ -100,10 +100,12 @@ typedef enum {
                               CTAs per SM; wider rows 32 KB tiles, 6 deep, one CTA */
     CE_PATH_WARP = 5,      /* one warp per row, the row held in one shared-memory tile
                               (rows up to 32 KB) */
-    CE_PATH_VECROW = 6     /* rows off the 16-byte grid (any alignment): one CTA per row
-                              of a persistent grid (two per SM), two passes of plain
-                              16-byte loads between a scalar head and tail, the second
-                              served by L2; no vocabulary split, no class weights */
+    CE_PATH_VECROW = 6     /* rows off the 16-byte grid (any alignment): a persistent
+                              grid, two passes of plain 16-byte loads per row between a
+                              scalar head and tail, the second served by L2; a warp per
+                              row up to 16 KB, else a CTA per row (512 threads two per
+                              SM, rows over 256 KB 1024 threads one per SM); no
+                              vocabulary split, no class weights */
 } ce_path;
 
 typedef struct {
@@ -116,7 +118,9 @@ typedef struct {
                                before the main kernel of the pass */
     void* event_end;        /* cudaEvent_t or NULL: recorded right after it */
     int tune_threads;       /* 0 = default; otherwise CTA size (256 or 512; on the stream
-                               path the number of consuming threads) */
+                               path the number of consuming threads); CE_PATH_VECROW
+                               also takes 1024 (one CTA per SM) and 32 (a row per warp),
+                               which the stream, row and cluster paths refuse */
     int tune_stages;        /* 0 = default; otherwise TMA pipeline depth (2..4 rows on the
                                row/cluster paths, 2..12 tiles on the stream path, 6 or 12
                                tiles on the warp path: 12 = two tiles per consumer warp,

@@ -137,6 +137,10 @@ def test_planner(lib):
     assert plan(4095, num_vocab_chunks=4) == (3, 4)  # a split asked for: two-stage
     assert plan(4095, force_path=3) == (3, 1)
     assert plan(4095, force_path=6, num_vocab_chunks=2)[0] == -2
+    assert plan(4095, tune_threads=1024) == (6, 1)  # the plain-load kernel's other shapes
+    assert plan(4095, tune_threads=32) == (6, 1)
+    assert plan(128000, tune_threads=1024)[0] == -2  # the stream kernel has no such shape
+    assert plan(4096, force_path=1, tune_threads=32)[0] == -2
     assert plan(4096, force_path=1, base=0x1002)[0] == -2
     assert plan(4_000_000)[0] == 4                 # any width streams
     assert plan(4_000_000, force_path=2)[0] == -2  # too wide for 16 CTAs

@@ -361,10 +361,11 @@ def test_unaligned_rows(V, dtype, a, reduce, ignore, path):
     harness.run_gpu_vs_oracle(w, force_path=path, per_row_dloss=not reduce)
 
 
-@pytest.mark.parametrize("threads,cap", [(256, 0), (512, 1), (256, 1)])
+@pytest.mark.parametrize("threads,cap", [(256, 0), (512, 1), (256, 1), (1024, 0), (32, 0), (32, 1)])
 def test_vecrow_shapes(threads, cap):
-    """The plain-load kernel's other CTA shapes (256 threads three per SM,
-    and grids capped to one CTA per SM, so each CTA takes many rows)."""
+    """The plain-load kernel's other shapes on 40 KB rows: a CTA of 256
+    threads (three per SM) or 1024 (one per SM), a warp per row (32), and
+    grids capped to one CTA per SM, so each CTA or warp takes many rows."""
     w = wl.Workload("vecrow_shapes", 1, 700, 20011, "bf16", sigma=2.0, ignore_frac=0.1,
                     label_smoothing=0.1, reduce_loss=True, seed=threads + cap)
     x = wl.logits(w)

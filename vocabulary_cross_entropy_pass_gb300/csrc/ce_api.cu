@@ -66,6 +66,7 @@ bool plan_stream(const ce_options* o, StreamPlan* sp, int def_tile_kb = 0, int d
     sp->ctas_per_sm_cap = o ? o->tune_ctas_per_sm : 0;
     sp->l2_keep = (o && o->tune_l2_keep == 2) ? 0 : 1;
     const size_t tile = (size_t)sp->tile_kb * 1024;
+    if (sp->threads != 256 && sp->threads != 512) return false;
     return sp->stages * tile + 1024 <= kSmemLimit;
 }
 
@@ -78,7 +79,9 @@ bool opts_clean(const ce_options* o) {
     if (o->tune_tile_kb != 0 && o->tune_tile_kb != 16 && o->tune_tile_kb != 32) return false;
     if (o->force_path < 0 || o->force_path > CE_PATH_VECROW) return false;
     if (o->num_vocab_chunks < 0) return false;
-    if (o->tune_threads != 0 && o->tune_threads != 256 && o->tune_threads != 512) return false;
+    if (o->tune_threads != 0 && o->tune_threads != 256 && o->tune_threads != 512 &&
+        o->tune_threads != 32 && o->tune_threads != 1024)
+        return false;
     if (o->tune_stages < 0 || o->tune_stages > 12 || o->tune_stages == 1) return false;
     if (o->tune_ctas_per_sm < 0) return false;
     if (o->tune_l2_keep < 0 || o->tune_l2_keep > 2) return false;
@@ -102,6 +105,7 @@ bool plan_fused(int dtype, int64_t V, const ce_options* o, bool want_cluster, Fu
         if (want_cluster && C < 2) C = 2;
     }
     if (C < 1 || C > kMaxCluster) return false;
+    if (o && o->tune_threads && o->tune_threads != 256 && o->tune_threads != 512) return false;
     const int64_t chunk = round_up_int((V + C - 1) / C, vec);
     int threads = (o && o->tune_threads) ? o->tune_threads : (chunk <= 8192 ? 256 : 512);
     if (chunk > (int64_t)fused_capacity(dtype, threads)) {
@@ -176,8 +180,14 @@ Plan make_plan(const Problem& p, const ce_options* o) {
     // one CTA per row, the second pass from L2.  A requested vocabulary split
     // still goes to the two-stage kernels.
     if (force == CE_PATH_VECROW || (force == CE_PATH_AUTO && !aligned && K == 0)) {
+        // Shapes by row width (tune_threads overrides): up to 16 KB a warp per
+        // row; up to 256 KB 512-thread CTAs, two per SM; wider rows
+        // 1024-thread CTAs, one per SM, so half as many rows wait in L2
+        // between their passes.
         pl.path = (K == 0 && p.V <= 0x7fffffffLL) ? CE_PATH_VECROW : -2;
-        pl.vecrow.threads = (o && o->tune_threads) ? o->tune_threads : 512;
+        const int tt = o ? o->tune_threads : 0;
+        pl.vecrow.warp_rows = tt == 32 || (tt == 0 && row_bytes <= 16 * 1024);
+        pl.vecrow.threads = tt > 32 ? tt : (row_bytes <= 256 * 1024 ? 512 : 1024);
         pl.vecrow.ctas_per_sm_cap = o ? o->tune_ctas_per_sm : 0;
         return pl;
     }

@@ -84,7 +84,8 @@ struct RowsPlan {
 
 // Plan of the kernel for rows off the 16-byte grid.
 struct VecRowPlan {
-    int threads;               // 512 (two CTAs per SM) or 256 (three)
+    int threads;               // a row per CTA: 512 (two CTAs per SM), 256 (three), 1024 (one)
+    bool warp_rows;            // a row per warp instead (512-thread CTAs, two per SM)
     int ctas_per_sm_cap;       // 0 = no cap
 };
 

@@ -27,11 +27,17 @@ namespace {
 
 constexpr int kVrBatch = 4;  // 16-byte loads in flight per thread
 
-// CTA shapes: 512 threads, two CTAs per SM (default), or 256 threads, three
-// per SM; either way 64 or 85 registers a thread and 2 x 152 or 3 x 152 rows
-// waiting in L2 between their passes.
+// Shapes.  A row per CTA: 512 threads two CTAs per SM (default), 256
+// threads three per SM, or 1024 threads one per SM (rows over 256 KB: half
+// the rows wait in L2 between their passes).  A row per warp (rows up to
+// 16 KB): 512 threads, two CTAs per SM, 32 rows in flight per SM and no CTA
+// barrier.
 template <int THREADS>
 struct VrShape;
+template <>
+struct VrShape<1024> {
+    static constexpr int kCtasPerSm = 1;
+};
 template <>
 struct VrShape<512> {
     static constexpr int kCtasPerSm = 2;
@@ -69,10 +75,12 @@ __device__ __forceinline__ uint64_t l2_evict_last_policy() {
     return pol;
 }
 
-template <typename T, bool GRAD, int THREADS>
+// WARPROW: each warp takes its own rows (kVrThreads below is then the 32
+// lanes of a row's group, tid the lane); otherwise the whole CTA takes a row.
+template <typename T, bool GRAD, int THREADS, bool WARPROW>
 __global__ void __launch_bounds__(THREADS, VrShape<THREADS>::kCtasPerSm)
     ce_vecrow_kernel(const __grid_constant__ VecRowArgs p) {
-    constexpr int kVrThreads = THREADS;
+    constexpr int kVrThreads = WARPROW ? 32 : THREADS;  // threads on one row
     constexpr int kVrWarps = THREADS / 32;
     using VT = Vec<T>;
     constexpr int VEC = VT::kElems;
@@ -80,28 +88,31 @@ __global__ void __launch_bounds__(THREADS, VrShape<THREADS>::kCtasPerSm)
     constexpr int PP = VEC / 2;
     // double-buffered so that a warp already in the next row's combine cannot
     // overwrite partials a slower warp is still reading
-    __shared__ float4 s_part[2][kVrWarps];
+    __shared__ float4 s_part[WARPROW ? 1 : 2][kVrWarps];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int tid = WARPROW ? lane : (int)threadIdx.x;
     const uint64_t keep = l2_evict_last_policy();
     const float2 L2 = make_float2(kLog2e, kLog2e);
     griddep_wait();  // the count kernel's n_non_ignore
     int buf = 0;
-    for (int64_t r = blockIdx.x; r < p.N; r += gridDim.x) {
+    const int64_t r0 = WARPROW ? (int64_t)blockIdx.x * kVrWarps + warp : (int64_t)blockIdx.x;
+    const int64_t rstep = WARPROW ? (int64_t)gridDim.x * kVrWarps : (int64_t)gridDim.x;
+    for (int64_t r = r0; r < p.N; r += rstep) {
         const int64_t i = r / p.dim1, j = r - i * p.dim1;
         const int64_t y = __ldg(p.targets + i * p.ts0 + j * p.ts1);
         char* row = p.logits + (i * p.s0 + j * p.s1) * (int64_t)ES;
         const Span16 sp = span16<ES>(row, 0, p.V);
-        const int64_t ee = span16_edge(sp, 0, p.V, threadIdx.x);
+        const int64_t ee = span16_edge(sp, 0, p.V, tid);
         uint4* rv = reinterpret_cast<uint4*>(row + sp.h1 * ES);
         const int nv = (int)sp.nv;  // V < 2^31 elements
 
-        if (y == p.ignore_idx || y < 0 || y >= p.V) {  // the same branch for every thread
+        if (y == p.ignore_idx || y < 0 || y >= p.V) {  // the same branch for the row's threads
             if (GRAD) {
                 if (ee >= 0) VT::store1(row + ee * ES, 0.f);
                 const uint4 z = make_uint4(0, 0, 0, 0);
-                for (int v = threadIdx.x; v < nv; v += kVrThreads) stg128_stream(rv + v, z);
+                for (int v = tid; v < nv; v += kVrThreads) stg128_stream(rv + v, z);
             }
-            if (threadIdx.x == 0) {
+            if (tid == 0) {
                 p.loss[r] = (y == p.ignore_idx) ? 0.f : __int_as_float(0x7fc00000);
                 if (p.lse_out) p.lse_out[r] = __int_as_float(0x7fc00000);
             }
@@ -110,7 +121,7 @@ __global__ void __launch_bounds__(THREADS, VrShape<THREADS>::kCtasPerSm)
 
         // pass 1: statistics; the target logit is read before any thread
         // can overwrite it in pass 2
-        const float xy = threadIdx.x == 0 ? VT::load1(row + y * ES) : 0.f;
+        const float xy = tid == 0 ? VT::load1(row + y * ES) : 0.f;
         float m = -INFINITY;
         float2 d2 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
         if (ee >= 0) {  // the thread's first element: exp(x - m) = 1 (nothing for -inf)
@@ -121,7 +132,7 @@ __global__ void __launch_bounds__(THREADS, VrShape<THREADS>::kCtasPerSm)
             }
             s2.x = x;
         }
-        for (int vb = threadIdx.x; vb < nv; vb += kVrThreads * kVrBatch) {
+        for (int vb = tid; vb < nv; vb += kVrThreads * kVrBatch) {
             uint4 raw[kVrBatch];
             float vm = -INFINITY;
 #pragma unroll
@@ -157,18 +168,21 @@ __global__ void __launch_bounds__(THREADS, VrShape<THREADS>::kCtasPerSm)
             }
         }
         const Part q = warp_allreduce_part(Part{m, d2.x + d2.y, s2.x + s2.y});
-        if (lane == 0) s_part[buf][warp] = make_float4(q.m, q.d, q.S, 0.f);
-        __syncthreads();
-        // every thread combines the warps' partials in the same order
-        Part G = part_identity();
+        Part G = q;
+        if constexpr (!WARPROW) {
+            if (lane == 0) s_part[buf][warp] = make_float4(q.m, q.d, q.S, 0.f);
+            __syncthreads();
+            // every thread combines the warps' partials in the same order
+            G = part_identity();
 #pragma unroll
-        for (int w = 0; w < kVrWarps; ++w) {
-            const float4 f = s_part[buf][w];
-            G = part_combine(G, Part{f.x, f.y, f.z});
+            for (int w = 0; w < kVrWarps; ++w) {
+                const float4 f = s_part[buf][w];
+                G = part_combine(G, Part{f.x, f.y, f.z});
+            }
+            buf ^= 1;
         }
-        buf ^= 1;
         const float lse = G.m + logf(G.d);
-        if (threadIdx.x == 0) {
+        if (tid == 0) {
             p.loss[r] = lse - (1.f - p.a) * xy - p.a_over_v * G.S;
             if (p.lse_out) p.lse_out[r] = lse;
         }
@@ -191,7 +205,7 @@ __global__ void __launch_bounds__(THREADS, VrShape<THREADS>::kCtasPerSm)
         }
         const float2 NL = make_float2(nll, nll), G2 = make_float2(g, g), NB = make_float2(-ga, -ga);
         const int yb = (int)(y - sp.h1);  // the target's place in the body
-        for (int vb = threadIdx.x; vb < nv; vb += kVrThreads * kVrBatch) {
+        for (int vb = tid; vb < nv; vb += kVrThreads * kVrBatch) {
             uint4 raw[kVrBatch];
 #pragma unroll
             for (int u = 0; u < kVrBatch; ++u) {
@@ -223,7 +237,7 @@ __global__ void __launch_bounds__(THREADS, VrShape<THREADS>::kCtasPerSm)
     }
 }
 
-template <typename T, int THREADS>
+template <typename T, int THREADS, bool WARPROW>
 cudaError_t launch_vecrow_shaped(const VecRowArgs& a, const Problem& pb, int ctas_cap, cudaStream_t s) {
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
@@ -231,7 +245,9 @@ cudaError_t launch_vecrow_shaped(const VecRowArgs& a, const Problem& pb, int cta
     int per_sm = VrShape<THREADS>::kCtasPerSm;
     if (ctas_cap > 0 && ctas_cap < per_sm) per_sm = ctas_cap;
     int64_t grid = (int64_t)sms * per_sm;
-    if (grid > pb.N) grid = pb.N;
+    const int64_t rows_per_cta = WARPROW ? THREADS / 32 : 1;
+    const int64_t need = (pb.N + rows_per_cta - 1) / rows_per_cta;
+    if (grid > need) grid = need;
     if (grid < 1) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -242,8 +258,8 @@ cudaError_t launch_vecrow_shaped(const VecRowArgs& a, const Problem& pb, int cta
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (pb.grad) return cudaLaunchKernelEx(&cfg, ce_vecrow_kernel<T, true, THREADS>, a);
-    return cudaLaunchKernelEx(&cfg, ce_vecrow_kernel<T, false, THREADS>, a);
+    if (pb.grad) return cudaLaunchKernelEx(&cfg, ce_vecrow_kernel<T, true, THREADS, WARPROW>, a);
+    return cudaLaunchKernelEx(&cfg, ce_vecrow_kernel<T, false, THREADS, WARPROW>, a);
 }
 
 template <typename T>
@@ -266,8 +282,10 @@ cudaError_t launch_vecrow_typed(const Problem& pb, const VecRowPlan& plan, cudaS
     a.loss = pb.loss_rows;
     a.lse_out = pb.lse_out;
     a.n_dev = pb.n_dev;
-    if (plan.threads == 256) return launch_vecrow_shaped<T, 256>(a, pb, plan.ctas_per_sm_cap, s);
-    return launch_vecrow_shaped<T, 512>(a, pb, plan.ctas_per_sm_cap, s);
+    if (plan.warp_rows) return launch_vecrow_shaped<T, 512, true>(a, pb, plan.ctas_per_sm_cap, s);
+    if (plan.threads == 256) return launch_vecrow_shaped<T, 256, false>(a, pb, plan.ctas_per_sm_cap, s);
+    if (plan.threads == 1024) return launch_vecrow_shaped<T, 1024, false>(a, pb, plan.ctas_per_sm_cap, s);
+    return launch_vecrow_shaped<T, 512, false>(a, pb, plan.ctas_per_sm_cap, s);
 }
 
 }  // namespace
