@@ -103,8 +103,8 @@ typedef enum {
     CE_PATH_VECROW = 6     /* rows off the 16-byte grid (any alignment): a persistent
                               grid, two passes of plain 16-byte loads per row between a
                               scalar head and tail, the second served by L2; a warp per
-                              row up to 16 KB, else a CTA per row (512 threads two per
-                              SM, rows over 256 KB 1024 threads one per SM); no
+                              row up to 32 KB, else a CTA per row (512 threads two per
+                              SM, rows over 320 KB 1024 threads one per SM); no
                               vocabulary split, no class weights */
 } ce_path;
 

@@ -180,14 +180,17 @@ Plan make_plan(const Problem& p, const ce_options* o) {
     // one CTA per row, the second pass from L2.  A requested vocabulary split
     // still goes to the two-stage kernels.
     if (force == CE_PATH_VECROW || (force == CE_PATH_AUTO && !aligned && K == 0)) {
-        // Shapes by row width (tune_threads overrides): up to 16 KB a warp per
-        // row; up to 256 KB 512-thread CTAs, two per SM; wider rows
+        // Shapes by row width (tune_threads overrides): up to 32 KB a warp per
+        // row; up to 320 KB 512-thread CTAs, two per SM; wider rows
         // 1024-thread CTAs, one per SM, so half as many rows wait in L2
-        // between their passes.
+        // between their passes.  Same-GPU sweep, ~2.1 GB of bf16 logits, ms
+        // per launch: 16383 columns warp 0.842 / CTA 1.049; 100277 512-thread
+        // 0.798 / 1024-thread 0.949; 151937 0.855 / 0.878; 200019 0.935 /
+        // 0.907; fp32 100003 0.946 / 0.892.
         pl.path = (K == 0 && p.V <= 0x7fffffffLL) ? CE_PATH_VECROW : -2;
         const int tt = o ? o->tune_threads : 0;
-        pl.vecrow.warp_rows = tt == 32 || (tt == 0 && row_bytes <= 16 * 1024);
-        pl.vecrow.threads = tt > 32 ? tt : (row_bytes <= 256 * 1024 ? 512 : 1024);
+        pl.vecrow.warp_rows = tt == 32 || (tt == 0 && row_bytes <= 32 * 1024);
+        pl.vecrow.threads = tt > 32 ? tt : (row_bytes <= 320 * 1024 ? 512 : 1024);
         pl.vecrow.ctas_per_sm_cap = o ? o->tune_ctas_per_sm : 0;
         return pl;
     }

@@ -28,9 +28,9 @@ namespace {
 constexpr int kVrBatch = 4;  // 16-byte loads in flight per thread
 
 // Shapes.  A row per CTA: 512 threads two CTAs per SM (default), 256
-// threads three per SM, or 1024 threads one per SM (rows over 256 KB: half
+// threads three per SM, or 1024 threads one per SM (rows over 320 KB: half
 // the rows wait in L2 between their passes).  A row per warp (rows up to
-// 16 KB): 512 threads, two CTAs per SM, 32 rows in flight per SM and no CTA
+// 32 KB): 512 threads, two CTAs per SM, 32 rows in flight per SM and no CTA
 // barrier.
 template <int THREADS>
 struct VrShape;
