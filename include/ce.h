@@ -49,6 +49,11 @@
  *     contiguous first, as TENPU #29 "Problems and solutions" does);
  *   - targets: int64, target of row (i, j) at targets[i*target_strides[0] +
  *     j*target_strides[1]];
+ *   - logits (and a separate gradient) must sit on a multiple of their element
+ *     size (CE_ERR_INVALID_ARG otherwise); rows need no further alignment:
+ *     rows on the 16-byte grid take the TMA kernels, others 16-byte loads
+ *     between a scalar head and tail (CE_PATH_VECROW, the two-stage kernels,
+ *     ce_bwd, ce_vp_partials);
  *   - errors found on the host are returned before anything is launched;
  *     a target outside [0, V) that is not ignore_idx is found on the device:
  *     that row gets loss NaN and a zero gradient, and the device error word
@@ -72,7 +77,8 @@ typedef enum { CE_LAYOUT_BSV = 0, CE_LAYOUT_SBV = 1 } ce_layout;
 
 typedef enum {
     CE_OK = 0,
-    CE_ERR_INVALID_ARG = 1,        /* null pointer, bad size, smoothing outside [0,1], ... */
+    CE_ERR_INVALID_ARG = 1,        /* null pointer, bad size, smoothing outside [0,1],
+                                      logits off their element size, ... */
     CE_ERR_UNSUPPORTED_DTYPE = 2,
     CE_ERR_BAD_STRIDE = 3,         /* strides[2] != 1, a negative stride, or (ce_fwd_bwd)
                                       rows that share memory */
