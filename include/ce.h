@@ -310,7 +310,8 @@ ce_status ce_linear_fwd_bwd(const void* hidden, const void* weight, ce_dtype dty
  * 256 (per-row losses), plus 16*dim0*dim1*K bytes rounded up to 256 when the
  * planner takes the two-stage path with K chunks.  Larger problems are
  * rejected with CE_ERR_WORKSPACE_TOO_SMALL before anything is launched
- * (about 520,000 rows on the row, cluster and stream paths).
+ * (about 520,000 rows on the row, cluster, stream, warp and plain-load
+ * paths).
  *
  * Set-up: the first call on a device looks up the scratch's device address
  * with that device current (the caller's current device); make that first

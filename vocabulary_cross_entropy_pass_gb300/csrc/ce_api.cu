@@ -7,10 +7,12 @@
 //                            before any gradient: a kept row is scaled by
 //                            dloss/n under reduce_loss);
 //   2. the main kernel(s) -- the stream kernel (wide rows), the warp-per-row
-//                            kernel (rows of one tile), the row/cluster
-//                            kernel, or the two stage kernels of the split
-//                            path;
-//   3. ce_mean_kernel     -- reduce_loss only: the fixed-order mean.
+//                            kernel (rows of one tile), the plain-load
+//                            kernel (rows off the 16-byte grid), the
+//                            row/cluster kernel, or the two stage kernels of
+//                            the split path;
+//   3. ce_mean_kernel     -- reduce_loss only, on the paths that do not take
+//                            the mean in their last CTA: the fixed-order mean.
 // Nothing is allocated and nothing waits for the device.
 #include <math.h>
 #include <string.h>

@@ -9,9 +9,9 @@
 // rows get zeros.  One read of the logits and one write of the gradient per
 // element, no reduction: a plain streaming kernel, 16-byte vectors between
 // a scalar head and tail when the gradient rows sit at the logits rows'
-// offset from a 16-byte boundary, element by element otherwise.  The gradient may overwrite the
-// logits (TENPU "Parallel Cross Entropy (Triton)" #29 section 6, in-place
-// staging) or go to a separate tensor.
+// offset from a 16-byte boundary, element by element otherwise.  The
+// gradient may overwrite the logits (TENPU "Parallel Cross Entropy (Triton)"
+// #29 section 6, in-place staging) or go to a separate tensor.
 #include "ce_device.cuh"
 #include "ce_internal.h"
 #include "ce_span.cuh"
