@@ -4,20 +4,22 @@
 // widths such as 50257 or 100277 in 16-bit types, padded or shifted views)
 // cannot be copied by TMA, which the stream and warp kernels use.  This kernel
 // streams such rows with plain 16-byte loads instead: a persistent grid, one
-// row per CTA at a time, two passes per row as in the online-softmax fusion
-// of TENPU "Parallel Cross Entropy (Triton)" #29 (section 6):
+// row per CTA (or per warp, for rows up to 32 KB) at a time, two passes per
+// row as in the online-softmax fusion of TENPU "Parallel Cross Entropy
+// (Triton)" #29 (section 6):
 //   pass 1: the row's (max, sum-exp, sum) -- a scalar head up to the first
 //           16-byte boundary, whole 16-byte vectors (kVrBatch loads in flight
 //           per thread, one rescale per batch with a new max), a scalar tail
-//           (ce_span.cuh) -- then a fixed-order CTA combine, lse = m + log d,
-//           loss = lse - (1-a) x_y - (a/V) S;
+//           (ce_span.cuh) -- then a fixed-order combine of the warps' partials
+//           (a warp's butterfly alone when a warp owns the row),
+//           lse = m + log d, loss = lse - (1-a) x_y - (a/V) S;
 //   pass 2: the gradient g (exp(x - lse) - a/V) - g (1-a) [j == y] written in
 //           place, reading the row again.
 // Two CTAs per SM (512 threads) keep 2 x 152 rows between their passes, so
-// for rows up to a few hundred KB the second read comes from L2 and HBM sees one read and
-// one write per element (the two-stage kernels read the logits twice from
-// HBM).  Every access stays inside its row, and head and tail elements are
-// stored one by one, so a row's neighbours are never touched.
+// for rows up to ~300 KB the second read comes from L2 and HBM sees one read
+// and one write per element (the two-stage kernels read the logits twice
+// from HBM).  Every access stays inside its row, and head and tail elements
+// are stored one by one, so a row's neighbours are never touched.
 #include "ce_device.cuh"
 #include "ce_internal.h"
 #include "ce_span.cuh"
@@ -60,8 +62,8 @@ struct VecRowArgs {
     const int64_t* n_dev;
 };
 
-// 16-byte load that keeps the line in L2 for the row's second pass, and the
-// second pass's load, the row's last use.
+// Pass 1's 16-byte load, with an L2 evict-last policy: the row's second pass
+// rereads the line (and takes it with __ldcs, the row's last use).
 __device__ __forceinline__ uint4 ldg128_keep(const uint4* p, uint64_t pol) {
     uint4 v;
     asm volatile("ld.global.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
@@ -180,6 +182,10 @@ __global__ void __launch_bounds__(THREADS, VrShape<THREADS>::kCtasPerSm)
                 G = part_combine(G, Part{f.x, f.y, f.z});
             }
             buf ^= 1;
+        } else {
+            // orders lane 0's read of the target logit before any lane's
+            // pass-2 store (every lane of the warp walks the same rows)
+            __syncwarp();
         }
         const float lse = G.m + logf(G.d);
         if (tid == 0) {
