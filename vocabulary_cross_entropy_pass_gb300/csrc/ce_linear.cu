@@ -30,6 +30,15 @@ namespace {
 constexpr size_t kCublasWorkspaceBytes = (size_t)32 << 20;
 constexpr int kLinMaxDevices = 64;
 
+// Launched in plain stream order between the logits GEMM and the pass.  The
+// pass kernels go out under programmatic dependent launch and their producers
+// issue the first logits copies before they wait on the preceding grid (in
+// ce_fwd_bwd that grid is the count kernel, which writes no logits).  A
+// library GEMM may signal its dependents before its last stores, so the pass
+// follows this empty kernel instead, which starts only once the GEMM has
+// completed.
+__global__ void ce_order_kernel() {}
+
 // One cuBLAS handle per host thread and device (handles are not shared
 // between threads that may run at the same time).
 cublasHandle_t thread_handle(int dev) {
@@ -128,7 +137,10 @@ ce_status ce_linear_fwd_bwd(const void* hidden, const void* weight, ce_dtype dty
                          (int)H, hid + (size_t)r0 * H * es, ty, (int)H, &zero, chunk, ty, (int)V,
                          CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
             return CE_ERR_LAUNCH;
-        // 2. the cross-entropy pass over the chunk, gradient in place
+        // 2. the cross-entropy pass over the chunk, gradient in place, after
+        //    the GEMM has completed (see ce_order_kernel)
+        ce_order_kernel<<<1, 32, 0, s>>>();
+        if (cudaGetLastError() != cudaSuccess) return CE_ERR_LAUNCH;
         const int64_t c_strides[3] = {rows * V, V, 1};
         const int64_t ct_strides[2] = {rows, 1};
         Problem pb;
