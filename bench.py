@@ -71,10 +71,14 @@ def measured_peaks() -> dict:
 
 
 def profiled_traffic(w, path: int):
-    """DRAM bytes per launch of the main kernel from the committed ncu capture
-    (profiles/ce_stream_kernel_traffic.json), scaled from the captured rows to
-    this workload's rows; None when the kernel sources changed since the
-    capture, or the workload or path differ from what was captured."""
+    """DRAM bytes per launch of the main kernel: the reads of the committed
+    ncu capture (profiles/ce_stream_kernel_traffic.json), scaled from the
+    captured rows to this workload's rows, plus the gradient write the kernel
+    must make (every row, ignored ones included: N V s bytes).  A capture's
+    own write count misses the dirty lines still in L2 when it ends (~80 MB
+    of a 1 GB write), so the write side is the required count, not the
+    measured one.  None when the kernel sources changed since the capture, or
+    the workload or path differ from what was captured."""
     import hashlib
     p = os.path.join(ROOT, "profiles", "ce_stream_kernel_traffic.json")
     if path != 4 or not os.path.exists(p):
@@ -89,7 +93,8 @@ def profiled_traffic(w, path: int):
     cap = wl.WORKLOADS[rec["captured_workload"]]
     if (cap.V, cap.dtype, cap.ignore_frac) != (w.V, w.dtype, w.ignore_frac):
         return None
-    return (rec["dram_bytes_read"] + rec["dram_bytes_write"]) * w.N / rec["captured_rows"]
+    return rec["dram_bytes_read"] * w.N / rec["captured_rows"] + logits_bytes(w.N, w.V,
+                                                                               w.elem_bytes)
 
 
 L2_BYTES = 129 * 1000 * 1000  # GB300 L2
@@ -527,6 +532,7 @@ def run_ours(args, w, rank: int, world: int, dist) -> None:
 
     peaks = measured_peaks()
     nbytes = pass_bytes(w.N, w.V, w.elem_bytes)
+    traffic = profiled_traffic(w, path)
     achieved = nbytes / (kernel_ms / 1e3) / 1e9
     cpu = None
     if not args.no_cpu_baseline:
@@ -545,9 +551,15 @@ def run_ours(args, w, rank: int, world: int, dist) -> None:
         "hbm_gbs_formula": nbytes * args.steps * world / (ms / 1e3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": profiled_traffic(w, path),
-                     "traffic_source": "ncu dram__bytes_read+write of the committed capture "
-                                       "(profiles/ce_stream_kernel_traffic.json) scaled by rows",
+                     "traffic": traffic,
+                     "traffic_source": "ncu dram__bytes_read of the committed capture "
+                                       "(profiles/ce_stream_kernel_traffic.json) scaled by "
+                                       "rows + the required gradient write N*V*s",
+                     "achieved_is": "algorithmic bytes (north-star formula: logits read + "
+                                    "gradient write + targets) / kernel time",
+                     "dram_gbs": traffic / (kernel_ms / 1e3) / 1e9 if traffic else None,
+                     "dram_frac": traffic / (kernel_ms / 1e3) / 1e9 / peaks["hbm_gbs"]
+                     if traffic else None,
                      "peak_source": peaks["source"], "kernel_ms": kernel_ms,
                      "algorithmic_bytes": nbytes},
         "cpu_baseline": cpu,

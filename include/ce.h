@@ -320,8 +320,12 @@ ce_status ce_linear_fwd_bwd(const void* hidden, const void* weight, ce_dtype dty
  * array and it keeps the last call's contents, so calls that may overlap on
  * the GPU (different streams, or threads enqueuing at once) race on it:
  * serialise them.  The error word lives in that internal scratch, so
- * ce_get_error cannot read it; out-of-range targets still show as NaN row
- * losses. */
+ * ce_get_error cannot read it: out-of-range targets still show as NaN row
+ * losses, but a bounded wait inside a kernel that gave up (CE_DEVERR_TIMEOUT,
+ * see ce_wait_timeout_probe) is not reported to the caller of this entry
+ * point at all -- the call has returned CE_OK and some loss and gradient rows
+ * may be left unwritten.  Callers that need that signal use ce_fwd_bwd with a
+ * workspace. */
 ce_status ce_fwd_bwd_noalloc(void* logits, ce_dtype dtype, ce_layout layout, int64_t dim0,
                              int64_t dim1, int64_t V, const int64_t strides[3],
                              const int64_t* targets, const int64_t target_strides[2],

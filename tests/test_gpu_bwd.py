@@ -43,8 +43,7 @@ def test_fwd_only_then_bwd(name, inplace):
     else:
         assert torch.equal(xd.cpu(), x)  # logits untouched
     gn = g.float().cpu().numpy().reshape(w.N, w.V).astype(np.float64)
-    excess, _ = harness.grad_errors(gn, ref["grad"], w.dtype)
-    assert excess <= 0.0
+    harness.check_grad(gn, ref, w, t, dloss=dl)
 
 
 @pytest.mark.parametrize("V,dtype", [(4095, "bf16"), (7, "f32"), (1000, "f16")])
@@ -57,9 +56,7 @@ def test_bwd_unaligned_rows(V, dtype):
     lse = torch.empty(w.N, dtype=torch.float32, device=DEV)
     pkg.ce_fwd_only(xd, td, label_smoothing=0.2, lse_out=lse)
     g = pkg.ce_bwd(xd, td, lse, label_smoothing=0.2)
-    excess, _ = harness.grad_errors(g.float().cpu().numpy().astype(np.float64).reshape(w.N, V),
-                                    ref["grad"], dtype)
-    assert excess <= 0.0
+    harness.check_grad(g.float().cpu().numpy(), ref, w, t)
 
 
 @pytest.mark.parametrize("name", ["c2_sbv8192_bf16", "c3_bsv32000_bf16_spiked", "c1_bsv4096_f32"])
@@ -81,8 +78,7 @@ def test_autograd_wrapper(name, inplace):
                         dtype=torch.float32, device=DEV)
     loss.backward(gout)
     gn = xd.grad.float().cpu().numpy().reshape(w.N, w.V).astype(np.float64)
-    excess, _ = harness.grad_errors(gn, ref["grad"], w.dtype)
-    assert excess <= 0.0
+    harness.check_grad(gn, ref, w, t, dloss=dl)
 
 
 def test_fused_and_split_backward_agree():
@@ -97,7 +93,8 @@ def test_fused_and_split_backward_agree():
     b = pkg.ce_bwd(x, t, lse, label_smoothing=0.1, reduce_loss=True, n_non_ignore=n)
     ga = a.float().cpu().numpy().astype(np.float64).reshape(w.N, w.V)
     gb = b.float().cpu().numpy().astype(np.float64).reshape(w.N, w.V)
-    excess, _ = harness.grad_errors(gb, ga, "bf16")
+    scale = harness.grad_scale(w.N, True, int(n.item()))
+    excess, _ = harness.grad_errors(gb, ga, "bf16", scale, 0.1, t.cpu().numpy().ravel())
     assert excess <= 0.0
 
 
@@ -126,9 +123,7 @@ def test_bwd_unaligned_rows_wide(V, dtype, gshift):
     gbuf = torch.zeros(1, 13, V + 8, dtype=xd.dtype, device=DEV)
     gview = gbuf[:, :, gshift:gshift + V]
     g = pkg.ce_bwd(xd, td, lse, label_smoothing=0.1, grad=gview)
-    excess, _ = harness.grad_errors(g.float().cpu().numpy().astype(np.float64).reshape(w.N, V),
-                                    ref["grad"], dtype)
-    assert excess <= 0.0
+    harness.check_grad(g.float().cpu().numpy(), ref, w, t)
     host = gbuf.cpu()
     assert torch.all(host[:, :, :gshift] == 0) and torch.all(host[:, :, gshift + V:] == 0)
     assert torch.equal(xd.cpu(), x)

@@ -63,7 +63,14 @@ def test_class_weighted_pass(name, route):
     assert int(n.item()) == ref["n"]
     harness.check_loss(loss.cpu().numpy(), ref["loss"], w.dtype, name)
     g = xd.float().cpu().numpy().reshape(w.N, w.V).astype(np.float64)
-    excess, _ = harness.grad_errors(g, ref["grad"], w.dtype)
+    # row scale: dloss over the kept rows' summed target weight (mean), or dloss[r]
+    tt = t.numpy().ravel()
+    if w.reduce_loss:
+        scale = np.full(w.N, dl[0] / cw.astype(np.float64)[tt[tt != -100]].sum())
+    else:
+        scale = dl.astype(np.float64)
+    excess, _ = harness.grad_errors(g, ref["grad"], w.dtype, scale, w.label_smoothing, tt,
+                                    weights=cw.astype(np.float64))
     assert excess <= 0.0
     # forward only gives the same losses
     lf = pkg.ce_fwd_only(x.to(DEV), td, label_smoothing=w.label_smoothing,
@@ -83,9 +90,11 @@ def test_unit_weights_equal_unweighted():
     lb = pkg.ce_fwd_bwd(b, t, label_smoothing=0.1, reduce_loss=True,
                         class_weights=torch.ones(w.V, device=DEV))
     harness.check_loss(lb.cpu().numpy(), la.cpu().numpy().astype(np.float64), "bf16")
+    tt = t.cpu().numpy().ravel()
+    scale = harness.grad_scale(w.N, True, int((tt != -100).sum()))
     excess, _ = harness.grad_errors(b.float().cpu().numpy().astype(np.float64).reshape(w.N, w.V),
                                     a.float().cpu().numpy().astype(np.float64).reshape(w.N, w.V),
-                                    "bf16")
+                                    "bf16", scale, 0.1, tt)
     assert excess <= 0.0
 
 

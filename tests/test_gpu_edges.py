@@ -31,8 +31,7 @@ def _compare(w, x_cpu, t_cpu, loss, g_dev, n_dev=None, strides=None, tstrides=No
         assert int(n_dev.item()) == ref["n"]
     if g_dev is not None:
         g = g_dev.float().cpu().numpy().reshape(w.N, w.V).astype(np.float64)
-        excess, _ = harness.grad_errors(g, ref["grad"], w.dtype)
-        assert excess <= 0.0, f"{w.name}: gradient exceeds tolerance by {excess:.3e}"
+        harness.check_grad(g, ref, w, t_cpu, dloss=dl)
     return ref
 
 
@@ -64,8 +63,7 @@ def test_padded_rows(dtype, pad):
     _compare(w, buf, t, loss, None, strides=(5 * (4000 + pad), 4000 + pad))
     g = view.float().cpu().numpy().reshape(w.N, w.V)
     ref = harness.oracle_run(w, x, t)
-    excess, _ = harness.grad_errors(g.astype(np.float64), ref["grad"], dtype)
-    assert excess <= 0.0
+    harness.check_grad(g, ref, w, t)
     # the padding is never touched
     assert torch.all(bd[:, :, 4000:].cpu() == 0)
 
@@ -86,7 +84,9 @@ def test_transposed_view(V):
                     targets=t.numpy().ravel(), target_strides=(1, B), label_smoothing=0.1)
     harness.check_loss(loss.cpu().numpy(), ref["loss"], "bf16")
     g = v.float().cpu().numpy().reshape(B * SQ, V).astype(np.float64)
-    excess, _ = harness.grad_errors(g, ref["grad"], "bf16")
+    # flattened rows of the (B, SQ) view: row b*SQ + s has target t[s, b]
+    excess, _ = harness.grad_errors(g, ref["grad"], "bf16", np.ones(B * SQ), 0.1,
+                                    t.t().contiguous().numpy().ravel())
     assert excess <= 0.0
 
 
@@ -230,7 +230,8 @@ def test_full_size_sampled_rows():
     scale = np.full(len(rows), 1.0 / ref_all["n"])
     ref = oracle.ce(harness.storage_np(sub), oracle.BF16, 1, len(rows), w.V,
                     targets=tsub.numpy(), label_smoothing=w.label_smoothing, dloss=scale)
-    excess, _ = harness.grad_errors(g_rows.astype(np.float64), ref["grad"], "bf16")
+    excess, _ = harness.grad_errors(g_rows.astype(np.float64), ref["grad"], "bf16", scale,
+                                    w.label_smoothing, tsub.numpy())
     assert excess <= 0.0
 
 
@@ -377,8 +378,7 @@ def test_vecrow_shapes(threads, cap):
     loss = pkg.ce_fwd_bwd(xd, t.to(DEV), label_smoothing=0.1, reduce_loss=True, opts=opts)
     harness.check_loss(loss.cpu().numpy().reshape(-1), ref["loss"], "bf16")
     g = xd.float().cpu().numpy().reshape(w.N, w.V).astype(np.float64)
-    excess, _ = harness.grad_errors(g, ref["grad"], "bf16")
-    assert excess <= 0.0
+    harness.check_grad(g, ref, w, t)
 
 
 @pytest.mark.parametrize("K", [3, 7, 16])
@@ -411,8 +411,7 @@ def test_shifted_view_rows(dtype, shift, path):
     ref = harness.oracle_run(w, x, t)
     harness.check_loss(loss.cpu().numpy(), ref["loss"], dtype, "shifted")
     g = view.float().cpu().numpy().reshape(w.N, V).astype(np.float64)
-    excess, _ = harness.grad_errors(g, ref["grad"], dtype)
-    assert excess <= 0.0
+    harness.check_grad(g, ref, w, t)
     host = bd.cpu()
     assert torch.all(host[:, :, :shift] == 0)
     assert torch.all(host[:, :, shift + V:] == 0)
