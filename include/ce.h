@@ -103,7 +103,18 @@ typedef enum {
                               of a row is served by L2, or for rows of at least twice
                               the ring by the ring's last tiles still in shared memory.
                               Default shape: rows up to 128 KB 16 KB tiles, 6 deep, two
-                              CTAs per SM; wider rows 32 KB tiles, 6 deep, one CTA */
+                              CTAs per SM; wider rows 32 KB tiles, 6 deep, one CTA.
+                              Rows off the 16-byte grid (the default for such rows over
+                              32 KB): the ring takes each row's aligned body, and the at
+                              most 2 (16/sizeof(T) - 1) elements before and after it are
+                              read and written one per thread (256 consuming threads).
+                              A vocabulary split (num_vocab_chunks = K, the default path
+                              for a split of aligned rows into at most 32 non-empty
+                              chunks; 16 KB tiles, two CTAs per SM): each chunk streams
+                              as its own run of tiles with the warps' running max shared,
+                              the
+                              chunks' (max, sum-exp, sum, target logit) partials are
+                              combined in chunk order (256 consuming threads) */
     CE_PATH_WARP = 5,      /* one warp per row, the row held in one shared-memory tile
                               (rows up to 32 KB) */
     CE_PATH_VECROW = 6     /* rows off the 16-byte grid (any alignment): a persistent
@@ -118,8 +129,11 @@ typedef struct {
     int force_path;         /* ce_path; CE_PATH_AUTO lets the planner choose */
     int num_vocab_chunks;   /* 0: planner chooses; K > 0: cut V into K contiguous
                                chunks of ceil(V/K) (rounded up to 16 bytes on the
-                               row and cluster paths) whose partials are combined
-                               on the device */
+                               row, cluster and stream paths, so fewer chunks may be
+                               non-empty) whose partials are combined on the device:
+                               the stream path for aligned rows cut into up to 32
+                               non-empty chunks, else the two-stage path (the
+                               cluster path when forced, up to 16 chunks) */
     void* event_begin;      /* cudaEvent_t or NULL: recorded on `stream` right
                                before the main kernel of the pass */
     void* event_end;        /* cudaEvent_t or NULL: recorded right after it */

@@ -126,13 +126,30 @@ def test_planner(lib):
     assert plan(128000, force_path=2) == (2, 16)
     assert plan(32000, force_path=2) == (2, 4)
     assert plan(4096, force_path=4) == (4, 1)
-    assert plan(4095, force_path=4)[0] == -2       # the stream path needs aligned rows too
-    assert plan(4095, force_path=5)[0] == -2       # and so does the warp path
+    assert plan(4095, force_path=4) == (4, 1)      # rows off the grid: TMA body, scalar edges
+    assert plan(4095, force_path=5)[0] == -2       # the warp path needs aligned rows
     assert plan(65536, num_vocab_chunks=8, force_path=2) == (2, 8)
     assert plan(65536, num_vocab_chunks=8, force_path=3) == (3, 8)
     assert plan(4095) == (6, 1)                    # rows not 16-byte aligned: plain loads
     assert plan(4096, base=0x1002) == (6, 1)       # base not 16-byte aligned
-    assert plan(100277) == (6, 1)
+    assert plan(100277) == (4, 1)                  # ... over 32 KB: the stream kernel
+    assert plan(32000, base=0x1002) == (4, 1)
+    assert plan(100277, tune_threads=512) == (6, 1)  # a shape only the plain-load kernel has
+    assert plan(100277, force_path=4, tune_threads=512)[0] == -2
+    # a vocabulary split asked for: the stream kernel combines up to 32 chunk
+    # partials (chunks of ceil(V/K) rounded up to 16 bytes), the two-stage
+    # kernels more; the cluster kernel on request
+    assert plan(65536, num_vocab_chunks=8) == (4, 8)
+    assert plan(65536, num_vocab_chunks=8, force_path=4) == (4, 8)
+    assert plan(128000, num_vocab_chunks=8) == (4, 8)
+    assert plan(104, num_vocab_chunks=3) == (4, 3)
+    assert plan(104, num_vocab_chunks=3, force_path=4) == (4, 3)  # chunks of 40, 40, 24
+    assert plan(16, num_vocab_chunks=8, force_path=4) == (4, 2)   # 8 columns each: two
+    assert plan(128000, num_vocab_chunks=32) == (4, 32)           # 8000-byte chunks
+    assert plan(128000, num_vocab_chunks=32, force_path=4) == (4, 32)
+    assert plan(128000, num_vocab_chunks=40) == (3, 40)
+    assert plan(128000, num_vocab_chunks=40, force_path=4)[0] == -2
+    assert plan(4095, num_vocab_chunks=4, force_path=4)[0] == -2
     assert plan(4096, force_path=6) == (6, 1)      # aligned rows on request
     assert plan(4095, num_vocab_chunks=4) == (3, 4)  # a split asked for: two-stage
     assert plan(4095, force_path=3) == (3, 1)

@@ -90,12 +90,93 @@ def test_transposed_view(V):
     assert excess <= 0.0
 
 
-@pytest.mark.parametrize("K", [2, 3, 5, 8, 16])
+@pytest.mark.parametrize("K", [2, 3, 5, 8, 16, 32])
 def test_cluster_chunk_counts(K):
     w = wl.Workload("k", 1, 40, 24000, "bf16", sigma=2.0, label_smoothing=0.1, reduce_loss=True,
                     seed=50 + K)
-    harness.run_gpu_vs_oracle(w, force_path=2, num_vocab_chunks=K)
+    if K <= 16:
+        harness.run_gpu_vs_oracle(w, force_path=2, num_vocab_chunks=K)
     harness.run_gpu_vs_oracle(w, force_path=3, num_vocab_chunks=K)
+    harness.run_gpu_vs_oracle(w, force_path=4, num_vocab_chunks=K)
+
+
+@pytest.mark.parametrize("name,K,tile_kb", [("c4_bsv65536_bf16_split8", 8, 0),
+                                            ("c5_bsv128000_bf16_ls", 8, 0),
+                                            ("c5_bsv128000_bf16_ls", 8, 16),
+                                            ("c5_bsv128000_f32_ls", 5, 0),
+                                            ("c2_sbv8192_bf16", 3, 0),
+                                            ("c3h_bsv32000_f16_spiked", 32, 32)])
+def test_stream_split_chunk_partials(name, K, tile_kb):
+    """A split asked for on the stream kernel: each chunk of C = ceil(V/K)
+    columns (rounded up to 16 bytes) streams as its own run of tiles and its
+    partial {m, d, S, x_y} lands in the workspace; against the oracle's
+    partials of the same columns (hyper-parallel #269 section 3.1: the
+    per-slice max, sum-exp and target logit that the ranks exchange)."""
+    w = wl.WORKLOADS[name].with_(dim0=1, dim1=48)
+    x = wl.logits(w)
+    t = wl.targets(w)
+    opts = pkg.make_options(force_path=pkg.CE_PATH_STREAM, num_vocab_chunks=K, tune_tile_kb=tile_kb)
+    xd = x.to(DEV)
+    assert pkg.ce_plan_path(xd, opts)[0] == pkg.CE_PATH_STREAM
+    vec = 16 // w.elem_bytes
+    C = -(-(-(-w.V // K)) // vec) * vec
+    nch = -(-w.V // C)
+    assert pkg.ce_plan_path(xd, opts)[1] == nch
+    ws = torch.zeros(pkg.ce_workspace_bytes(1, w.N, w.V, xd.dtype, opts), dtype=torch.uint8,
+                     device=DEV)
+    loss = pkg.ce_fwd_bwd(xd, t.to(DEV), label_smoothing=w.label_smoothing,
+                          reduce_loss=w.reduce_loss, workspace=ws, opts=opts)
+    assert pkg.ce_get_error(ws) == (0, 0)
+    off = 256 + -(-w.N * 4 // 256) * 256
+    part = ws[off:off + w.N * nch * 16].cpu().view(torch.float32).numpy().reshape(w.N, nch, 4)
+    xv = x.float().numpy().reshape(w.N, w.V).astype(np.float64)
+    tt = t.numpy().ravel()
+    for r in range(w.N):
+        if tt[r] == w.ignore_idx:
+            continue
+        for c in range(nch):
+            k0, k1 = c * C, min(w.V, (c + 1) * C)
+            ref = oracle.chunk_partials(xv[r], k0, k1, tt[r])
+            m, d, S, xy = part[r, c].astype(np.float64)
+            assert m == ref[0], (r, c)                            # max of stored values: exact
+            assert abs(d - ref[1]) <= 1e-5 * ref[1], (r, c)
+            assert abs(S - ref[2]) <= 1e-5 * np.abs(xv[r, k0:k1]).sum() + 1e-6, (r, c)
+            assert xy == ref[3], (r, c)                           # the target logit, exact
+    ref = harness.oracle_run(w, x, t, dloss=np.array([1.0]) if w.reduce_loss else None)
+    harness.check_loss(loss.cpu().numpy(), ref["loss"], w.dtype, name)
+    harness.check_grad(xd.float().cpu().numpy(), ref, w, t,
+                       dloss=np.array([1.0]) if w.reduce_loss else None)
+
+
+@pytest.mark.parametrize("V,dtype", [(20011, "bf16"), (16389, "f16"), (10007, "f32"),
+                                     (7, "bf16"), (33, "f16"), (4095, "bf16"), (3, "f32")])
+def test_stream_edges_targets_at_the_edges(V, dtype):
+    """Rows off the 16-byte grid on the stream kernel: the ring takes each
+    row's aligned body, threads take the head and tail elements one each.
+    Row starts cycle through the offsets from a 16-byte boundary (odd
+    widths), and targets sit on the first and last elements of each row, so
+    the target is a head, body or tail element; tiny widths have no body."""
+    N = 48
+    w = wl.Workload(f"edges{V}", 1, N, V, dtype, sigma=2.0, ignore_frac=0.1, label_smoothing=0.1,
+                    seed=V + 5)
+    x = wl.logits(w)
+    t = wl.targets(w)
+    tf = t.view(-1)
+    for r in range(0, 16):
+        if tf[r] != -100:
+            tf[r] = r % min(8, V) if r < 8 else V - 1 - (r % min(8, V))
+    opts = pkg.make_options(force_path=pkg.CE_PATH_STREAM)
+    xd = x.to(DEV)
+    assert pkg.ce_plan_path(xd, opts)[0] == pkg.CE_PATH_STREAM
+    rng = np.random.default_rng(V)
+    dl = rng.uniform(0.5, 2.0, N).astype(np.float32).astype(np.float64)
+    loss = pkg.ce_fwd_bwd(xd, t.to(DEV), label_smoothing=0.1,
+                          dloss=torch.tensor(dl, dtype=torch.float32, device=DEV), opts=opts)
+    ref = harness.oracle_run(w, x, t, dloss=dl)
+    harness.check_loss(loss.cpu().numpy(), ref["loss"], dtype, w.name)
+    g = xd.float().cpu().numpy().reshape(N, V)
+    assert np.all(g[wl.ignored_rows(w)] == 0.0)
+    harness.check_grad(g, ref, w, t, dloss=dl)
 
 
 def test_empty_chunks():
@@ -320,8 +401,9 @@ def test_bounded_wait_reports_timeout():
     harness.run_gpu_vs_oracle(w)  # the context is still usable
 
 
-@pytest.mark.parametrize("V,path", [(1 << 20, pkg.CE_PATH_STREAM), ((1 << 20) + 3, pkg.CE_PATH_VECROW),
-                                    (256000, pkg.CE_PATH_STREAM), (200000, pkg.CE_PATH_STREAM)])
+@pytest.mark.parametrize("V,path", [(1 << 20, pkg.CE_PATH_STREAM), ((1 << 20) + 3, pkg.CE_PATH_STREAM),
+                                    (256000, pkg.CE_PATH_STREAM), (200000, pkg.CE_PATH_STREAM),
+                                    (200003, pkg.CE_PATH_STREAM)])
 @pytest.mark.parametrize("reduce", [True, False])
 def test_very_wide_rows(V, path, reduce):
     """Rows of a million columns (2 MB of bf16 each: 64 ring tiles per pass on
@@ -333,6 +415,8 @@ def test_very_wide_rows(V, path, reduce):
     x = wl.logits(w)
     assert pkg.ce_plan_path(x.to(DEV))[0] == path
     harness.run_gpu_vs_oracle(w, per_row_dloss=not reduce)
+    if V % 8:  # the plain-load kernel on the same odd-width rows
+        harness.run_gpu_vs_oracle(w, force_path=pkg.CE_PATH_VECROW, per_row_dloss=not reduce)
 
 
 def test_warp_path_two_tiles_by_default():
@@ -349,16 +433,20 @@ def test_warp_path_two_tiles_by_default():
                                                      (50257, "f16", 0.0, False, 0.2),
                                                      (100003, "f32", 0.2, True, 0.0),
                                                      (16387, "bf16", 0.0, False, 0.05)])
-@pytest.mark.parametrize("path", [pkg.CE_PATH_AUTO, pkg.CE_PATH_TWO_STAGE])
+@pytest.mark.parametrize("path", [pkg.CE_PATH_AUTO, pkg.CE_PATH_TWO_STAGE, pkg.CE_PATH_VECROW])
 def test_unaligned_rows(V, dtype, a, reduce, ignore, path):
     """Odd widths put every row at its own offset from a 16-byte boundary.
-    The planner sends them to the plain-load kernel (one CTA per row, a
-    scalar head, 16-byte vectors, a scalar tail); the two-stage kernels read
-    each chunk the same way (several chunks per row, the last one ragged)."""
+    The planner sends rows over 32 KB to the stream kernel (the aligned body
+    through the TMA ring, the head and tail elements one per thread), and
+    narrower ones to the plain-load kernel (a scalar head, 16-byte vectors,
+    a scalar tail), which also takes the wide ones when forced; the two-stage
+    kernels read each chunk the same way (several chunks per row, the last
+    one ragged)."""
     w = wl.Workload(f"unaligned_{V}", 2, 17, V, dtype, sigma=2.0, ignore_frac=ignore,
                     label_smoothing=a, reduce_loss=reduce, seed=V % 1000)
     if path == pkg.CE_PATH_AUTO:
-        assert pkg.ce_plan_path(wl.logits(w).to(DEV))[0] == pkg.CE_PATH_VECROW
+        want = pkg.CE_PATH_STREAM if V * w.elem_bytes > 32 * 1024 else pkg.CE_PATH_VECROW
+        assert pkg.ce_plan_path(wl.logits(w).to(DEV))[0] == want
     harness.run_gpu_vs_oracle(w, force_path=path, per_row_dloss=not reduce)
 
 
@@ -391,12 +479,13 @@ def test_unaligned_rows_short_chunks(K):
 
 
 @pytest.mark.parametrize("dtype,shift", [("bf16", 1), ("bf16", 5), ("f16", 3), ("f32", 1)])
-@pytest.mark.parametrize("path", [pkg.CE_PATH_AUTO, pkg.CE_PATH_TWO_STAGE])
+@pytest.mark.parametrize("path", [pkg.CE_PATH_AUTO, pkg.CE_PATH_TWO_STAGE, pkg.CE_PATH_VECROW])
 def test_shifted_view_rows(dtype, shift, path):
     """An aligned width read through a view that starts `shift` elements
-    into each padded row: the rows leave the 16-byte grid, the plain-load
-    kernel (or the two-stage kernels, forced) takes them, and the padding on
-    both sides stays untouched."""
+    into each padded row: the rows leave the 16-byte grid, the stream kernel
+    (aligned body by TMA, head and tail by threads) takes them, or forced the
+    plain-load or two-stage kernels, and the padding on both sides stays
+    untouched."""
     V, pad = 32000, 9
     w = wl.Workload("shifted", 2, 5, V, dtype, sigma=2.0, label_smoothing=0.1, seed=50 + shift)
     x = wl.logits(w)
@@ -406,7 +495,7 @@ def test_shifted_view_rows(dtype, shift, path):
     bd = buf.to(DEV)
     view = bd[:, :, shift:shift + V]
     if path == pkg.CE_PATH_AUTO:
-        assert pkg.ce_plan_path(view)[0] == pkg.CE_PATH_VECROW
+        assert pkg.ce_plan_path(view)[0] == pkg.CE_PATH_STREAM
     loss = pkg.ce_fwd_bwd(view, t.to(DEV), label_smoothing=0.1, force_path=path)
     ref = harness.oracle_run(w, x, t)
     harness.check_loss(loss.cpu().numpy(), ref["loss"], dtype, "shifted")

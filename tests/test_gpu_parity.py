@@ -22,7 +22,10 @@ CASES = [
     ("c3h_bsv32000_f16_spiked", AUTO, None), ("c3h_bsv32000_f16_spiked", TWO, None),
     ("c3h_bsv32000_f16_spiked", CLUSTER, None), ("c1_bsv4096_f32", WARP, None),
     ("c4_bsv65536_bf16_split8", CLUSTER, 8), ("c4_bsv65536_bf16_split8", TWO, 8),
-    ("c4_bsv65536_bf16_split8", STREAM, 0),
+    ("c4_bsv65536_bf16_split8", STREAM, 0), ("c4_bsv65536_bf16_split8", STREAM, 8),
+    ("c4_bsv65536_bf16_split8", AUTO, 8), ("c5_bsv128000_bf16_ls", STREAM, 8),
+    ("c5_bsv128000_f32_ls", STREAM, 8), ("c2_sbv8192_bf16", STREAM, 3),
+    ("c1_bsv4096_f32", STREAM, 5), ("c3h_bsv32000_f16_spiked", STREAM, 16),
     ("c5_bsv128000_bf16", AUTO, None), ("c5_bsv128000_bf16_ls", AUTO, None),
     ("c5_bsv128000_bf16_ls", TWO, None), ("c5_bsv128000_bf16_ls", CLUSTER, None),
     ("c5_bsv128000_f32", AUTO, None), ("c5_bsv128000_f32_ls", AUTO, None),
@@ -57,6 +60,16 @@ def test_planner_paths():
     x = torch.empty(2, 3, 4095, dtype=torch.bfloat16, device=dev)  # rows not 16-byte aligned
     assert pkg.ce_plan_path(x)[0] == VECROW
     assert pkg.ce_plan_path(x, pkg.make_options(num_vocab_chunks=2)) == (TWO, 2)
+    x = torch.empty(2, 3, 50257, dtype=torch.bfloat16, device=dev)  # wide and off the grid
+    assert pkg.ce_plan_path(x) == (STREAM, 1)
     opts = pkg.make_options(force_path=CLUSTER, num_vocab_chunks=8)
     x = torch.empty(2, 256, 65536, dtype=torch.bfloat16, device=dev)
     assert pkg.ce_plan_path(x, opts) == (CLUSTER, 8)
+    # a split asked for: the stream kernel with per-chunk partials (chunks of
+    # ceil(V/K) rounded up to 16 bytes: 104 bf16 columns in 3 -> 40, 40, 24)
+    assert pkg.ce_plan_path(x, pkg.make_options(num_vocab_chunks=8)) == (STREAM, 8)
+    x = torch.empty(2, 3, 104, dtype=torch.bfloat16, device=dev)
+    assert pkg.ce_plan_path(x, pkg.make_options(num_vocab_chunks=3)) == (STREAM, 3)
+    assert pkg.ce_plan_path(x, pkg.make_options(force_path=STREAM, num_vocab_chunks=3)) == (STREAM, 3)
+    x = torch.empty(2, 3, 128000, dtype=torch.bfloat16, device=dev)
+    assert pkg.ce_plan_path(x, pkg.make_options(num_vocab_chunks=40)) == (TWO, 40)

@@ -52,19 +52,22 @@ def test_oversized_problems_are_rejected_on_the_host():
     assert call(8, 4096, tune_threads=300) == 1     # ordinary argument checks still apply
 
 
-# (workload, forced path): the warp path, the stream path with its in-kernel
-# mean and row counter in the scratch header, the two-stage path with its
-# partials in the scratch, fp32 rows, and rows off the 16-byte grid (odd
-# width: the plain-load kernel)
-CASES = [("c2_sbv8192_bf16", 0), ("c5_bsv128000_bf16_ls", 0), ("c3_bsv32000_bf16_spiked", 3),
-         ("c1_bsv4096_f32", 0), ("odd_50257_bf16", 0)]
+# (workload, forced path, vocabulary chunks): the warp path, the stream path
+# with its in-kernel mean and row counter in the scratch header, the stream
+# path split into 8 chunks (its chunk partials in the scratch), the two-stage
+# path with its partials in the scratch, fp32 rows, and rows off the 16-byte
+# grid (odd width: the stream kernel with scalar edges, and the plain-load
+# kernel forced)
+CASES = [("c2_sbv8192_bf16", 0, 0), ("c5_bsv128000_bf16_ls", 0, 0),
+         ("c4_bsv65536_bf16_split8", 0, 8), ("c3_bsv32000_bf16_spiked", 3, 0),
+         ("c1_bsv4096_f32", 0, 0), ("odd_50257_bf16", 0, 0), ("odd_50257_bf16", 6, 0)]
 ODD = wl.Workload("odd_50257_bf16", 1, 64, 50257, "bf16", sigma=2.0, ignore_frac=0.1,
                   label_smoothing=0.1, reduce_loss=True, seed=5257)
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("name,path", CASES)
-def test_noalloc_matches_workspace_entry_point(name, path):
+@pytest.mark.parametrize("name,path,chunks", CASES)
+def test_noalloc_matches_workspace_entry_point(name, path, chunks):
     """Same plan, same kernels: the results must equal ce_fwd_bwd's bit for
     bit.  The second call gets other logits and targets, so scratch the first
     call left behind (row counter, ticket, partials) cannot pass for the
@@ -72,7 +75,7 @@ def test_noalloc_matches_workspace_entry_point(name, path):
     import vocabulary_cross_entropy_pass_gb300 as pkg
     w0 = ODD if name == ODD.name else wl.WORKLOADS[name]
     dev = torch.device("cuda")
-    opts = _lib.make_options(force_path=path)
+    opts = _lib.make_options(force_path=path, num_vocab_chunks=chunks)
     for call in range(2):   # two calls in a row share the fixed scratch
         w = w0.with_(seed=w0.seed + 101 * call)
         x = wl.logits(w).to(dev)
@@ -81,7 +84,7 @@ def test_noalloc_matches_workspace_entry_point(name, path):
             t = t.roll(1)     # ignored rows move too
         xa, xb = x.clone(), x.clone()
         la = pkg.ce_fwd_bwd(xa, t, label_smoothing=w.label_smoothing,
-                            reduce_loss=w.reduce_loss, force_path=path)
+                            reduce_loss=w.reduce_loss, force_path=path, num_vocab_chunks=chunks)
         lb = torch.full_like(la, float("nan"))
         rc = _noalloc_c(xb, t, lb, w.label_smoothing, w.reduce_loss, opts)
         assert rc == 0, _lib.STATUS.get(rc, rc)

@@ -164,9 +164,55 @@ Plan make_plan(const Problem& p, const ce_options* o) {
         return pl;
     }
     const int K = o ? o->num_vocab_chunks : 0;
-    // Rows wider than one CTA's registers go through the stream kernel unless
-    // a vocabulary split is asked for.
     const int64_t row_bytes = p.V * p.es;
+    const int def_tile = row_bytes <= 128 * 1024 ? 16 : 32;
+    // A vocabulary split asked for on aligned rows: the stream kernel streams
+    // each chunk of ceil(V/K) columns (rounded up to 16 bytes) as its own run
+    // of tiles and combines the chunks' partials in chunk order (256
+    // consuming threads).  16 KB tiles, two CTAs per SM, at any width: the
+    // chunk-end sums and part-filled tiles want the extra warps.  Same-GPU
+    // sweep, 2.1 GB of bf16 logits, ms per launch (stream / two-stage /
+    // cluster): 128000 columns K = 8 0.677 (0.813 with 32 KB tiles) / 1.040;
+    // K = 16 0.745 / 1.251 / 1.932; K = 32 1.222 / 1.961; 65536 columns K = 16
+    // 1.201 / 1.911 / 3.315; 32000 columns K = 4 0.820 / 1.252 / 1.448.  More
+    // chunks than 32 go to the two-stage kernels.
+    if (K > 0 && aligned && (force == CE_PATH_AUTO || force == CE_PATH_STREAM)) {
+        const int vec = 16 / p.es;
+        const int64_t C = round_up_int((p.V + K - 1) / K, vec);
+        const int64_t nch = (p.V + C - 1) / C;
+        if (nch <= kMaxStreamChunks && plan_stream(o, &pl.stream, 16, 6) &&
+            pl.stream.threads == 256) {
+            pl.stream.geo = kStreamChunks;
+            pl.stream.chunk_elems = C;
+            pl.stream.nchunks = (int)nch;
+            pl.path = CE_PATH_STREAM;
+            return pl;
+        }
+        if (force == CE_PATH_STREAM) {
+            pl.path = -2;
+            return pl;
+        }
+    }
+    // Rows off the 16-byte grid wider than 32 KB (odd widths such as 50257 or
+    // 100277 in 16-bit types, shifted views): the stream kernel copies each
+    // row's aligned body with TMA and takes the at most 2 (16/s - 1) elements
+    // around it one per thread.  Narrower ones, and shapes the stream kernel
+    // does not have (tune_threads other than 256), take the plain-load kernel
+    // below.
+    const bool edges_auto = force == CE_PATH_AUTO && !aligned && K == 0 && row_bytes > 32 * 1024;
+    const bool edges_forced = force == CE_PATH_STREAM && !aligned && K == 0;
+    if ((edges_auto || edges_forced) && p.V <= 0x7fffffffLL) {
+        if (plan_stream(o, &pl.stream, def_tile, 6) && pl.stream.threads == 256) {
+            pl.stream.geo = kStreamEdges;
+            pl.path = CE_PATH_STREAM;
+            return pl;
+        }
+        if (edges_forced) {
+            pl.path = -2;
+            return pl;
+        }
+        memset(&pl.stream, 0, sizeof pl.stream);
+    }
     // Short rows (one 32 KB tile or less): a warp per row; wider rows: the
     // stream kernel; a requested vocabulary split: the cluster kernel.
     const bool warp_auto = force == CE_PATH_AUTO && aligned && K == 0 && row_bytes <= 32 * 1024;
@@ -178,9 +224,9 @@ Plan make_plan(const Problem& p, const ce_options* o) {
         pl.path = CE_PATH_WARP;
         return pl;
     }
-    // Rows off the 16-byte grid (TMA cannot copy them): plain 16-byte loads,
-    // one CTA per row, the second pass from L2.  A requested vocabulary split
-    // still goes to the two-stage kernels.
+    // Rows off the 16-byte grid up to 32 KB (or forced): plain 16-byte loads,
+    // the second pass from L2.  A requested vocabulary split still goes to
+    // the two-stage kernels.
     if (force == CE_PATH_VECROW || (force == CE_PATH_AUTO && !aligned && K == 0)) {
         // Shapes by row width (tune_threads overrides): up to 32 KB a warp per
         // row; up to 320 KB 512-thread CTAs, two per SM; wider rows
@@ -211,7 +257,6 @@ Plan make_plan(const Problem& p, const ce_options* o) {
         // group the same way); two CTAs per SM would speed a forward-only pass
         // of wider rows too (split step at 128000 columns: 1.822 ms against
         // 1.846 ms), not worth losing that.
-        const int def_tile = row_bytes <= 128 * 1024 ? 16 : 32;
         if (!aligned || !plan_stream(o, &pl.stream, def_tile, 6)) {
             pl.path = -2;
             return pl;
@@ -271,7 +316,9 @@ ce_status check_common(const void* logits, int dtype, int layout, int64_t dim0, 
 
 cudaError_t launch_planned(const Problem& pb, const Plan& pl, float4* parts, cudaStream_t s) {
     if (pl.path == CE_PATH_TWO_STAGE) return launch_split(pb, pl.split, parts, s);
-    if (pl.path == CE_PATH_STREAM) return launch_stream(pb, pl.stream, s);
+    if (pl.path == CE_PATH_STREAM)
+        return pl.stream.geo == kStreamAligned ? launch_stream(pb, pl.stream, s)
+                                               : launch_stream_geo(pb, pl.stream, parts, s);
     if (pl.path == CE_PATH_WARP) return launch_rows(pb, pl.rows, s);
     if (pl.path == CE_PATH_VECROW) return launch_vecrow(pb, pl.vecrow, s);
     return launch_fused(pb, pl.fused, s);
@@ -640,10 +687,10 @@ int ce_plan_path(const void* logits, ce_dtype dtype, int64_t dim0, int64_t dim1,
     Plan pl = make_plan(pb, opts);
     if (pl.path < 0) return pl.path;
     if (chunks_out)
-        *chunks_out = pl.path == CE_PATH_TWO_STAGE                            ? pl.split.chunks
-                      : (pl.path == CE_PATH_STREAM || pl.path == CE_PATH_WARP ||
-                         pl.path == CE_PATH_VECROW)                             ? 1
-                                                                                : pl.fused.cluster;
+        *chunks_out = pl.path == CE_PATH_TWO_STAGE ? pl.split.chunks
+                      : pl.path == CE_PATH_STREAM  ? (pl.stream.geo == kStreamChunks ? pl.stream.nchunks : 1)
+                      : (pl.path == CE_PATH_WARP || pl.path == CE_PATH_VECROW) ? 1
+                                                                               : pl.fused.cluster;
     return pl.path;
 }
 
@@ -694,6 +741,8 @@ size_t noalloc_need(const Problem& pb, const Plan& pl) {
     size_t need = kWsHeaderBytes + align_up((size_t)pb.N * sizeof(float), 256);
     if (pl.path == CE_PATH_TWO_STAGE)
         need += align_up((size_t)pb.N * (size_t)pl.split.chunks * sizeof(float4), 256);
+    if (pl.path == CE_PATH_STREAM && pl.stream.geo == kStreamChunks)
+        need += align_up((size_t)pb.N * (size_t)pl.stream.nchunks * sizeof(float4), 256);
     return need;
 }
 

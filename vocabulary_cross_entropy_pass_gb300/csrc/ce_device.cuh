@@ -343,6 +343,13 @@ __device__ __forceinline__ float warp_allmax(float v) {
     return v;
 }
 
+// Max over the warp in one instruction (sm_100 family): every lane gets it.
+__device__ __forceinline__ float warp_max_redux(float v) {
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+
 __device__ __forceinline__ float warp_allsum(float v) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(kFull, v, off);

@@ -66,6 +66,14 @@ struct FusedPlan {
     int ctas_per_sm_cap;       // 0 = no cap
 };
 
+// Row geometries of the row-streaming kernel: rows on the 16-byte grid;
+// rows anywhere (an aligned body through the ring, a scalar head and tail);
+// rows cut into vocabulary chunks whose partials are combined in order.
+constexpr int kStreamAligned = 0;
+constexpr int kStreamEdges = 1;
+constexpr int kStreamChunks = 2;
+constexpr int kMaxStreamChunks = 32;  // chunks per row the stream kernel combines
+
 // Plan of the row-streaming kernel.
 struct StreamPlan {
     int threads;               // consumer threads: 256 or 512
@@ -73,6 +81,9 @@ struct StreamPlan {
     int stages;                // ring depth in tiles
     int ctas_per_sm_cap;       // 0 = no cap
     int l2_keep;               // 1: first-pass copies use an L2 evict-last policy
+    int geo;                   // kStreamAligned / kStreamEdges / kStreamChunks
+    int64_t chunk_elems;       // kStreamChunks: elements per chunk (16-byte multiple)
+    int nchunks;               // kStreamChunks: non-empty chunks, <= kMaxStreamChunks
 };
 
 // Plan of the warp-per-row kernel (rows that fit one shared-memory tile).
@@ -149,6 +160,10 @@ void set_pdl_attr(cudaLaunchAttribute* attr);
 cudaError_t launch_reduce_mean(const Problem& p, float* loss_out, cudaStream_t s);
 cudaError_t launch_fused(const Problem& p, const FusedPlan& plan, cudaStream_t s);
 cudaError_t launch_stream(const Problem& p, const StreamPlan& plan, cudaStream_t s);
+// rows with a scalar head and tail, or cut into chunks (partials: per-(row,
+// chunk) {m, d, S, x_y}, N * plan.nchunks of them, or NULL)
+cudaError_t launch_stream_geo(const Problem& p, const StreamPlan& plan, float4* partials,
+                              cudaStream_t s);
 cudaError_t launch_rows(const Problem& p, const RowsPlan& plan, cudaStream_t s);
 cudaError_t launch_vecrow(const Problem& p, const VecRowPlan& plan, cudaStream_t s);
 cudaError_t launch_bwd(const BwdProblem& bp, cudaStream_t s);

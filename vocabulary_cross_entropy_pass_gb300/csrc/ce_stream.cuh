@@ -1,4 +1,7 @@
-// ce_stream.cu -- the row-streaming fused cross-entropy kernel.
+// ce_stream.cuh -- the row-streaming fused cross-entropy kernel (template;
+// ce_stream.cu instantiates it for rows on the 16-byte grid and the
+// class-weighted pass, ce_stream_geo.cu for rows with a scalar head and tail
+// and for rows cut into vocabulary chunks).
 //
 // One CTA owns whole token rows, so no CTA ever waits for another: a
 // persistent grid, each CTA starting on rows cta and cta + grid and then
@@ -33,17 +36,46 @@
 // kept rows.  (The forward-only weighted pass reads the weights in pass 1,
 // with plain loads.)
 //
+// Row geometry (GEO):
+//   kGeoAligned  rows on the 16-byte grid: the whole row goes through the
+//                ring, tile k at byte k * TB;
+//   kGeoEdges    rows anywhere (on a multiple of the element size): TMA copies
+//                need 16-byte aligned addresses and sizes, so the ring takes the
+//                row's aligned body -- whole 16-byte vectors from the first
+//                16-byte boundary -- and the at most 2 (16 / sizeof(T) - 1)
+//                elements before and after it (odd widths such as 50257 or
+//                100277, shifted views) are one per thread, read once with a
+//                plain load and kept in a register for the gradient;
+//   kGeoChunks   a vocabulary split asked for: the row is cut into contiguous
+//                chunks of C elements (ceil(V/K) rounded up to 16 bytes), each
+//                streamed as its own run of tiles; at the end of a chunk every
+//                warp reduces its (max, sum-exp, sum) to the chunk's warp
+//                partial, and the CTA combine folds the warps of each chunk,
+//                then the chunks in chunk order -- the (m, d, x_y) combine of
+//                the vocabulary-parallel ranks of mindspore/hyper-parallel #269
+//                section 3.1, inside one CTA.  The chunk partials {m, d, S, x_y}
+//                are also written to the workspace.
+//
 // Warp specialisation: warps 0..NC/32-1 consume tiles; the last warp only
 // issues copies.  `full[s]` completes when tile s has landed (TMA transaction
 // count); `empty[s]` completes when every consumer warp is done with it.  Both
 // waits are bounded; a wait that gives up sets CE_DEVERR_TIMEOUT and the CTA
 // drains without further copies (the producer then waits, bounded, for the
 // copies it already issued before the CTA exits).
+#pragma once
+
 #include "ce_device.cuh"
 #include "ce_internal.h"
+#include "ce_span.cuh"
+
+#include <string.h>
 
 namespace gbce {
 namespace {
+
+constexpr int kGeoAligned = kStreamAligned;
+constexpr int kGeoEdges = kStreamEdges;
+constexpr int kGeoChunks = kStreamChunks;
 
 struct StreamArgs {
     char* logits;
@@ -51,8 +83,7 @@ struct StreamArgs {
     int32_t V;
     int32_t stages;
     uint32_t tile_bytes;   // bytes per ring tile, multiple of 16
-    int32_t ntiles;        // tiles per row
-    uint32_t last_bytes;   // bytes of the last tile of a row
+    int32_t ntiles;        // tiles per row (kGeoEdges: per row, from where it starts)
     const int64_t* targets;
     int64_t ts0, ts1, ignore_idx;
     float a, a_over_v;
@@ -70,7 +101,63 @@ struct StreamArgs {
     const double* wsum;    // summed weight over the vocabulary (count kernel)
     uint32_t* row_claim;   // rows claimed past each CTA's first two, or NULL (static rows)
     uint32_t* row_done;    // CTAs done claiming
+    // kGeoChunks: vocabulary chunks of chunk_elems elements (chunk_bytes, a
+    // multiple of 16), tpc tiles each (the last chunk may take fewer),
+    // nchunks non-empty chunks; part: per-(row, chunk) partials {m, d, S, x_y}
+    // at part[row * nchunks + chunk], or NULL
+    int64_t chunk_elems;
+    uint32_t chunk_bytes;
+    int32_t tpc;
+    int32_t nchunks;
+    float4* part;
 };
+
+// The part of a row that goes through the ring: `body` (16-byte aligned),
+// `body_bytes` (a multiple of 16) in `ntiles` tiles; kGeoEdges: the elements
+// [0, head) and [t0, V) stay outside it.
+struct RowGeo {
+    const char* body;
+    int64_t body_bytes;
+    int32_t ntiles;
+    int64_t head;
+    int64_t t0;
+};
+
+template <int GEO, int ES, int TB>
+__device__ __forceinline__ RowGeo row_geo(const StreamArgs& p, const char* rowp) {
+    RowGeo g;
+    if constexpr (GEO == kGeoEdges) {
+        const Span16 s = span16<ES>(rowp, 0, p.V);
+        g.head = s.h1;
+        g.t0 = s.t0;
+        g.body = rowp + s.h1 * ES;
+        g.body_bytes = s.nv * 16;
+        g.ntiles = (int32_t)((g.body_bytes + TB - 1) / TB);
+    } else {
+        g.head = 0;
+        g.t0 = p.V;
+        g.body = rowp;
+        g.body_bytes = (int64_t)p.V * ES;
+        g.ntiles = p.ntiles;
+    }
+    return g;
+}
+
+// Tile k of a row: its byte offset from the body and its byte count.
+template <int GEO, int TB>
+__device__ __forceinline__ void tile_span(const StreamArgs& p, const RowGeo& g, int k, int64_t& off,
+                                          uint32_t& bytes) {
+    if constexpr (GEO == kGeoChunks) {
+        const int c = k / p.tpc;
+        const int j = k - c * p.tpc;
+        off = (int64_t)c * p.chunk_bytes + (int64_t)j * TB;
+        const int64_t cend = min((int64_t)(c + 1) * p.chunk_bytes, g.body_bytes);
+        bytes = (uint32_t)min((int64_t)TB, cend - off);
+    } else {
+        off = (int64_t)k * TB;
+        bytes = (k == g.ntiles - 1) ? (uint32_t)(g.body_bytes - off) : (uint32_t)TB;
+    }
+}
 
 // The class weights of one 16-byte logits vector: VEC fp32 values, read as
 // 16-byte loads (the weight vector stays in L2: V x 4 bytes).
@@ -135,8 +222,10 @@ struct Ring {
 // Pass-1 work on one tile: running max, then p = 2^((x - m) log2e) summed,
 // and the plain sum (WS: the class-weighted sum sum_j w_j x_j instead), in
 // packed f32x2 arithmetic.  FULL: every vector valid.  e0: the row element of
-// the tile's first vector (weights only).
-template <typename T, int NC, int NV, bool FULL, bool WS>
+// the tile's first vector (weights only).  UNI: the running max is the
+// warp's (one redux per tile), so every lane's sums share it and the warp's
+// partial is two plain sums.
+template <typename T, int NC, int NV, bool FULL, bool WS, bool UNI = false>
 __device__ __forceinline__ void stats_tile(const uint4* tile, int tid, int nvec, float& m,
                                            float2& d2, float2& s2, const float* cw, int64_t e0) {
     using VT = Vec<T>;
@@ -150,7 +239,8 @@ __device__ __forceinline__ void stats_tile(const uint4* tile, int tid, int nvec,
             tm = VT::max_acc(tm, raw[i]);
         }
     }
-    const float tmf = VT::max_done(tm);
+    float tmf = VT::max_done(tm);
+    if constexpr (UNI) tmf = warp_max_redux(tmf);
     if (tmf > m) {  // new running max: rescale what was summed so far
         if (m != -INFINITY) {
             const float c = ex2_approx((m - tmf) * kLog2e);
@@ -238,7 +328,7 @@ __device__ __forceinline__ void grad_tile(const uint4* tile, uint4* dst, int tid
 // that two CTAs' rows between their passes still fit L2 (and for the
 // weighted pass, whose gradient pass issues ~40% more instructions per
 // element).  Every other shape is built for one CTA per SM.
-template <typename T, int NC, int NV, bool GRAD, bool WT>
+template <typename T, int NC, int NV, bool GRAD, bool WT, int GEO>
 __global__ void __launch_bounds__(NC + 32, (NC == 256 && NV * NC * 16 == 16384) ? 2 : 1)
 ce_stream_kernel(const __grid_constant__ StreamArgs p) {
     using VT = Vec<T>;
@@ -247,6 +337,8 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
     constexpr int NW = NC / 32;           // consumer warps
     constexpr int TB = NC * NV * 16;      // tile bytes
     constexpr int TV = NC * NV;           // vectors per tile
+    constexpr int KS = GEO == kGeoChunks ? kMaxStreamChunks : 1;  // chunk slots per row
+    static_assert(!WT || GEO == kGeoAligned, "the weighted pass streams aligned rows only");
 
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* ring = smem;
@@ -256,8 +348,8 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
     uint64_t* qempty = qfull + kRowQ;  // row queue: entry read by every consumer warp
     int64_t* rowq = reinterpret_cast<int64_t*>(qempty + kRowQ);  // row index
     int64_t* yq = rowq + kRowQ;                                   // its target
-    float4* red = reinterpret_cast<float4*>(yq + kRowQ);  // [2][NW]
-    float* xy_s = reinterpret_cast<float*>(red + 2 * NW);  // [2]
+    float4* red = reinterpret_cast<float4*>(yq + kRowQ);  // [2][KS][NW]
+    float* xy_s = reinterpret_cast<float*>(red + 2 * KS * NW);  // [2]
     float* sw_s = xy_s + 2;                                 // [2][NW] weighted sums
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sw_s + 2 * NW);
     volatile int* last_flag = abort_flag + 1;
@@ -290,7 +382,6 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
         return y != p.ignore_idx && y >= 0 && y < (int64_t)p.V;
     };
     const int npass = GRAD ? 2 : 1;
-    const int last_nvec = (int)(p.last_bytes / 16);
     // weighted gradient pass with smoothing: each tile brings its class
     // weights into the next WS ring slots (without smoothing no weight is read)
     constexpr int WS = 4 / ES;
@@ -299,14 +390,16 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
     // the row's last `stages` tiles, and the ring is a queue -- so pass 2 can
     // take those tiles first, straight from shared memory (the producer
     // re-marks their slots full without a copy), then reload tiles 0 ..
-    // ntiles - R - 1.  Pass-2 tile k is tile pass2_tile(k).  This pays for
-    // rows of at least twice the ring (fewer tiles wait in L2 for pass 2:
-    // 256000 bf16 columns, 16 tiles, 6-deep ring, 4096 rows: 0.650 ms
-    // against 0.680 ms); at 8 tiles (128000 columns) the reordered pass
-    // measured 1.3 % slower, so shorter rows reload every tile.  Not with
-    // weight slots in the ring.
-    const int R = (GRAD && !wring && p.ntiles >= 2 * p.stages) ? p.stages : 0;
-    auto pass2_tile = [&](int k) -> int { return k < R ? p.ntiles - R + k : k - R; };
+    // ntiles - R - 1.  Pass-2 tile k is pass2_tile(k).  This pays for rows of
+    // at least twice the ring (fewer tiles wait in L2 for pass 2: 256000 bf16
+    // columns, 16 tiles, 6-deep ring, 4096 rows: 0.650 ms against 0.680 ms);
+    // at 8 tiles (128000 columns) the reordered pass measured 1.3 % slower,
+    // so shorter rows reload every tile.  Not with weight slots in the ring.
+    // R depends on the row's tile count (kGeoEdges: on where the row starts).
+    auto parked = [&](int ntiles) -> int {
+        return (GRAD && !wring && ntiles >= 2 * p.stages) ? p.stages : 0;
+    };
+    auto pass2_tile = [](int k, int R, int ntiles) -> int { return k < R ? ntiles - R + k : k - R; };
 
     // ------------------------------------------------------------ producer warp
     if (warp == NW) {
@@ -367,13 +460,14 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
                     claimed = true;
                 }
                 const bool loaded = is_loaded(yr);
-                const char* row = row_ptr(r);
+                const RowGeo gr = row_geo<GEO, ES, TB>(p, row_ptr(r));
+                const int R = parked(gr.ntiles);
                 for (int pass = 0; loaded && pass < npass && !*abort_flag; ++pass) {
                     if (pass == 1 && !claimed) {
                         claim_y();
                         claimed = true;
                     }
-                    for (int k = 0; k < p.ntiles; ++k) {
+                    for (int k = 0; k < gr.ntiles; ++k) {
                         if (!mbar_wait_bounded(&empty[rg.s], rg.ph ^ 1u)) {
                             griddep_wait();  // the count kernel starts the error word
                             atomicOr(p.err, CE_DEVERR_TIMEOUT);
@@ -387,12 +481,14 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
                             ++issued;
                             continue;
                         }
-                        const int t = pass == 1 ? pass2_tile(k) : k;
-                        const uint32_t bytes = (t == p.ntiles - 1) ? p.last_bytes : (uint32_t)TB;
+                        const int t = pass == 1 ? pass2_tile(k, R, gr.ntiles) : k;
+                        int64_t off;
+                        uint32_t bytes;
+                        tile_span<GEO, TB>(p, gr, t, off, bytes);
                         // pass 1 asks L2 to keep the tiles pass 2 will reload
-                        const uint64_t pol = (pass == 0 && t < p.ntiles - R) ? pol_keep : pol_drop;
+                        const uint64_t pol = (pass == 0 && t < gr.ntiles - R) ? pol_keep : pol_drop;
                         mbar_arrive_expect_tx(&full[rg.s], bytes);
-                        tma_load_1d(ring + (size_t)rg.s * TB, row + (size_t)t * TB, bytes, &full[rg.s], pol);
+                        tma_load_1d(ring + (size_t)rg.s * TB, gr.body + off, bytes, &full[rg.s], pol);
                         rg.next();
                         ++issued;
                         if (pass == 1 && wring) {
@@ -495,11 +591,18 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
     bool stop = named_bar_or(1, NC, r < 0 || *abort_flag);
     while (!stop) {
         char* rowp = row_ptr(r);
+        const RowGeo gr = row_geo<GEO, ES, TB>(p, rowp);
+        // kGeoEdges: this thread's element among the row's head and tail (or
+        // -1), kept in a register from pass 1 to pass 2
+        int64_t ee = -1;
+        if constexpr (GEO == kGeoEdges) ee = span16_edge(Span16{gr.head, gr.body_bytes / 16, gr.t0}, 0, p.V, tid);
         if (!is_loaded(y)) {
             if (GRAD) {
                 const uint4 z = make_uint4(0, 0, 0, 0);
-                const int64_t nv = (int64_t)p.V / VEC;
-                for (int64_t v = tid; v < nv; v += NC) stg128_stream(rowp + v * 16, z);
+                const int64_t nv = gr.body_bytes / 16;
+                char* body = const_cast<char*>(gr.body);
+                for (int64_t v = tid; v < nv; v += NC) stg128_stream(body + v * 16, z);
+                if (ee >= 0) VT::store1(rowp + ee * ES, 0.f);
             }
             if (tid == 0) {
                 p.loss[r] = (y == p.ignore_idx) ? 0.f : __int_as_float(0x7fc00000);
@@ -514,37 +617,107 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
         }
         const float g = p.reduce ? g_reduce : (p.dloss ? __ldg(p.dloss + r) : 1.f);
         const int64_t ybyte = y * ES;
-        const int ty = (int)(ybyte / TB);                 // tile holding the target
-        const int yv = (int)((ybyte - (int64_t)ty * TB) / 16);  // its vector in that tile
+        // the tile holding the target and the target's byte in that tile (-1:
+        // the target is a head or tail element, outside the ring)
+        int ty = -1, yoff = 0;
+        if constexpr (GEO == kGeoChunks) {
+            const int c = (int)(y / p.chunk_elems);
+            const int64_t jb = (y - (int64_t)c * p.chunk_elems) * ES;
+            const int j = (int)(jb / TB);
+            ty = c * p.tpc + j;
+            yoff = (int)(jb - (int64_t)j * TB);
+        } else if (y >= gr.head && y < gr.t0) {
+            const int64_t yb = (y - gr.head) * ES;
+            ty = (int)(yb / TB);
+            yoff = (int)(yb - (int64_t)ty * TB);
+        }
+        const int yv = yoff / 16;  // the target's vector in its tile
 
-        // pass 1: running statistics over the tiles
+        // pass 1: running statistics over the tiles (and this thread's head
+        // or tail element)
         float m = -INFINITY;
         float2 d2 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
-        for (int t = 0; t < p.ntiles; ++t) {
+        float xe = 0.f;
+        if constexpr (GEO == kGeoEdges) {
+            if (ee >= 0) {
+                xe = VT::load1(rowp + ee * ES);
+                m = xe;
+                d2.x = 1.f;
+                s2.x = xe;
+            }
+            if (ty < 0 && ee == y) xy_s[par] = xe;
+        }
+        for (int t = 0; t < gr.ntiles; ++t) {
             wait_full();
+            int64_t off;
+            uint32_t bytes;
+            tile_span<GEO, TB>(p, gr, t, off, bytes);
             const uint4* tile = reinterpret_cast<const uint4*>(ring + (size_t)rg.s * TB);
-            if (t == ty && tid == 0) xy_s[par] = VT::load1(ring + (size_t)rg.s * TB + (ybyte - (int64_t)ty * TB));
-            const int64_t e0 = (int64_t)t * TV * VEC;
-            // the weighted sum comes with pass 2 when there is one
-            if (t < p.ntiles - 1)
-                stats_tile<T, NC, NV, true, WT && !GRAD>(tile, tid, TV, m, d2, s2, p.cw, e0);
+            if (t == ty && tid == 0) xy_s[par] = VT::load1(ring + (size_t)rg.s * TB + yoff);
+            const int64_t e0 = off / ES;
+            // the weighted sum comes with pass 2 when there is one; chunked
+            // rows keep the warp's running max
+            constexpr bool UNI = GEO == kGeoChunks;
+            if (bytes == (uint32_t)TB)
+                stats_tile<T, NC, NV, true, WT && !GRAD, UNI>(tile, tid, TV, m, d2, s2, p.cw, e0);
             else
-                stats_tile<T, NC, NV, false, WT && !GRAD>(tile, tid, last_nvec, m, d2, s2, p.cw, e0);
+                stats_tile<T, NC, NV, false, WT && !GRAD, UNI>(tile, tid, (int)(bytes / 16), m, d2, s2,
+                                                               p.cw, e0);
             release();
+            if constexpr (GEO == kGeoChunks) {
+                // end of a chunk: the warp's partial of this chunk (its lanes
+                // share the running max: two sums), then a fresh running
+                // partial for the next one
+                if (t == gr.ntiles - 1 || (t + 1) % p.tpc == 0) {
+                    const float dw = warp_allsum(d2.x + d2.y);
+                    const float sw = warp_allsum(s2.x + s2.y);
+                    if (lane == 0) red[(par * KS + t / p.tpc) * NW + warp] = make_float4(m, dw, sw, 0.f);
+                    m = -INFINITY;
+                    d2 = make_float2(0.f, 0.f);
+                    s2 = make_float2(0.f, 0.f);
+                }
+            }
         }
 
         // the successor (published before this row's copies)
         int64_t ny;
         const int64_t nx = next_row(ny);
         // CTA combine, fixed order; its barrier takes the exit decision
-        Part q = warp_allreduce_part(Part{m, d2.x + d2.y, s2.x + s2.y});
-        if (lane == 0) red[par * NW + warp] = make_float4(q.m, q.d, q.S, 0.f);
+        if constexpr (GEO != kGeoChunks) {
+            Part q = warp_allreduce_part(Part{m, d2.x + d2.y, s2.x + s2.y});
+            if (lane == 0) red[par * NW + warp] = make_float4(q.m, q.d, q.S, 0.f);
+        }
         stop = named_bar_or(1, NC, nx < 0 || *abort_flag);
         Part G = part_identity();
+        if constexpr (GEO == kGeoChunks) {
+            // lane c folds chunk c's warp partials in warp order, then every
+            // lane folds the chunks in chunk order through shuffles: every
+            // warp gets the same bits
+            Part P = part_identity();
+            if (lane < p.nchunks) {
 #pragma unroll
-        for (int w = 0; w < NW; ++w) {
-            const float4 v4 = red[par * NW + w];
-            G = part_combine(G, Part{v4.x, v4.y, v4.z});
+                for (int w = 0; w < NW; ++w) {
+                    const float4 v4 = red[(par * KS + lane) * NW + w];
+                    P = part_combine(P, Part{v4.x, v4.y, v4.z});
+                }
+                if (p.part && warp == 0) {
+                    const int cy = (int)(y / p.chunk_elems);
+                    p.part[r * p.nchunks + lane] = make_float4(P.m, P.d, P.S, lane == cy ? xy_s[par] : 0.f);
+                }
+            }
+            for (int c = 0; c < p.nchunks; ++c) {
+                Part q;
+                q.m = __shfl_sync(kFull, P.m, c);
+                q.d = __shfl_sync(kFull, P.d, c);
+                q.S = __shfl_sync(kFull, P.S, c);
+                G = part_combine(G, q);
+            }
+        } else {
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const float4 v4 = red[par * NW + w];
+                G = part_combine(G, Part{v4.x, v4.y, v4.z});
+            }
         }
         const float lse = G.m + logf(G.d);
         const float xy = xy_s[par];
@@ -566,12 +739,23 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
             const float2 G2 = make_float2(c, c);
             const float2 NB = make_float2(-bb, -bb);
             float2 sw2 = make_float2(0.f, 0.f);
-            for (int k = 0; k < p.ntiles; ++k) {
-                const int t = pass2_tile(k);  // the parked tiles first
+            if constexpr (GEO == kGeoEdges) {
+                // this thread's head or tail element, from its register
+                if (ee >= 0) {
+                    const float e = ex2_approx(fmaf(xe, kLog2e, nll));
+                    VT::store1(rowp + ee * ES, fmaf(e, c, -bb) - (ee == y ? g * (1.f - p.a) : 0.f));
+                }
+            }
+            const int R = parked(gr.ntiles);
+            for (int k = 0; k < gr.ntiles; ++k) {
+                const int t = pass2_tile(k, R, gr.ntiles);  // the parked tiles first
                 wait_full();
+                int64_t off;
+                uint32_t bytes;
+                tile_span<GEO, TB>(p, gr, t, off, bytes);
                 const int st = rg.s;
                 const uint4* tile = reinterpret_cast<const uint4*>(ring + (size_t)st * TB);
-                uint4* dst = reinterpret_cast<uint4*>(rowp + (size_t)t * TB);
+                uint4* dst = reinterpret_cast<uint4*>(const_cast<char*>(gr.body) + off);
                 rg.next();
                 // without smoothing the weighted gradient is c * softmax -
                 // c [j == y] and the loss has no sum_j w_j x_j term: no
@@ -586,10 +770,10 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
                         wslot[h] = ring + (size_t)rg.s * TB;
                         rg.next();
                     }
-                    if (t < p.ntiles - 1)
+                    if (bytes == (uint32_t)TB)
                         grad_tile<T, NC, NV, true, true>(tile, dst, tid, TV, NL, G2, NB, wslot, sw2);
                     else
-                        grad_tile<T, NC, NV, false, true>(tile, dst, tid, last_nvec, NL, G2, NB, wslot, sw2);
+                        grad_tile<T, NC, NV, false, true>(tile, dst, tid, (int)(bytes / 16), NL, G2, NB, wslot, sw2);
                     __syncwarp();
                     if (lane == 0) {
                         mbar_arrive(&empty[st]);
@@ -597,10 +781,10 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
                         for (int h = 0; h < WS; ++h) mbar_arrive(&empty[sw[h]]);
                     }
                 } else {
-                    if (t < p.ntiles - 1)
+                    if (bytes == (uint32_t)TB)
                         grad_tile<T, NC, NV, true, false>(tile, dst, tid, TV, NL, G2, NB, nullptr, sw2);
                     else
-                        grad_tile<T, NC, NV, false, false>(tile, dst, tid, last_nvec, NL, G2, NB, nullptr, sw2);
+                        grad_tile<T, NC, NV, false, false>(tile, dst, tid, (int)(bytes / 16), NL, G2, NB, nullptr, sw2);
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&empty[st]);
                 }
@@ -672,11 +856,13 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
     }
 }
 
-template <typename T, int NC, int NV, bool GRAD, bool WT>
-cudaError_t launch_stream_one(const Problem& pb, const StreamPlan& plan, cudaStream_t s) {
-    auto kern = ce_stream_kernel<T, NC, NV, GRAD, WT>;
+template <typename T, int NC, int NV, bool GRAD, bool WT, int GEO>
+cudaError_t launch_stream_one(const Problem& pb, const StreamPlan& plan, float4* parts, cudaStream_t s) {
+    auto kern = ce_stream_kernel<T, NC, NV, GRAD, WT, GEO>;
     constexpr int NW = NC / 32;
+    constexpr int KS = GEO == kGeoChunks ? kMaxStreamChunks : 1;
     StreamArgs a;
+    memset(&a, 0, sizeof a);
     a.logits = pb.logits;
     a.s0 = pb.s0;
     a.s1 = pb.s1;
@@ -685,9 +871,28 @@ cudaError_t launch_stream_one(const Problem& pb, const StreamPlan& plan, cudaStr
     a.V = (int32_t)pb.V;
     a.stages = plan.stages;
     a.tile_bytes = (uint32_t)(NC * NV * 16);  // must match the kernel's TB
+    const int64_t TB = a.tile_bytes;
     const int64_t row_bytes = pb.V * (int64_t)sizeof(T);
-    a.ntiles = (int32_t)((row_bytes + a.tile_bytes - 1) / a.tile_bytes);
-    a.last_bytes = (uint32_t)(row_bytes - (int64_t)(a.ntiles - 1) * a.tile_bytes);
+    if (GEO == kGeoChunks) {
+        // chunks of chunk_elems elements (a multiple of the 16-byte vector),
+        // tpc tiles each; the last non-empty chunk may be shorter
+        const int64_t C = plan.chunk_elems;
+        if (C < 1 || (C * (int64_t)sizeof(T)) % 16) return cudaErrorInvalidValue;
+        const int64_t CB = C * (int64_t)sizeof(T);
+        const int64_t nchunks = (pb.V + C - 1) / C;
+        if (nchunks > kMaxStreamChunks) return cudaErrorInvalidValue;
+        const int64_t tpc = (CB + TB - 1) / TB;
+        const int64_t last = row_bytes - (nchunks - 1) * CB;
+        a.chunk_elems = C;
+        a.chunk_bytes = (uint32_t)CB;
+        a.tpc = (int32_t)tpc;
+        a.nchunks = (int32_t)nchunks;
+        a.ntiles = (int32_t)((nchunks - 1) * tpc + (last + TB - 1) / TB);
+        a.part = parts;
+    } else {
+        // kGeoEdges computes its tiles per row, from where the row starts
+        a.ntiles = (int32_t)((row_bytes + TB - 1) / TB);
+    }
     a.targets = pb.targets;
     a.ts0 = pb.ts0;
     a.ts1 = pb.ts1;
@@ -710,7 +915,8 @@ cudaError_t launch_stream_one(const Problem& pb, const StreamPlan& plan, cudaStr
     a.row_claim = pb.N < (int64_t)0x7fffffff ? pb.row_claim : nullptr;
     a.row_done = pb.row_done;
     const size_t smem = (size_t)plan.stages * a.tile_bytes + (24 + 4 * kRowQ) * sizeof(uint64_t) +
-                        2 * NW * sizeof(float4) + (2 + 2 * NW) * sizeof(float) + 2 * sizeof(int) + 16;
+                        2 * KS * NW * sizeof(float4) + (2 + 2 * NW) * sizeof(float) + 2 * sizeof(int) +
+                        16;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0, per_sm = 0;
@@ -735,35 +941,5 @@ cudaError_t launch_stream_one(const Problem& pb, const StreamPlan& plan, cudaStr
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-// Tiles of 16 or 32 KB, consumed by 256 or 512 threads; the weighted pass
-// runs the 256-thread shapes only.
-template <typename T, bool GRAD>
-cudaError_t launch_stream_typed(const Problem& pb, const StreamPlan& plan, cudaStream_t s) {
-    if (pb.cw) {
-        if (plan.threads != 256) return cudaErrorInvalidConfiguration;
-        return plan.tile_kb == 16 ? launch_stream_one<T, 256, 4, GRAD, true>(pb, plan, s)
-                                  : launch_stream_one<T, 256, 8, GRAD, true>(pb, plan, s);
-    }
-    if (plan.tile_kb == 16)
-        return plan.threads == 512 ? launch_stream_one<T, 512, 2, GRAD, false>(pb, plan, s)
-                                   : launch_stream_one<T, 256, 4, GRAD, false>(pb, plan, s);
-    return plan.threads == 512 ? launch_stream_one<T, 512, 4, GRAD, false>(pb, plan, s)
-                               : launch_stream_one<T, 256, 8, GRAD, false>(pb, plan, s);
-}
-
 }  // namespace
-cudaError_t launch_stream(const Problem& p, const StreamPlan& plan, cudaStream_t s) {
-    switch (p.dtype) {
-        case CE_F32:
-            return p.grad ? launch_stream_typed<float, true>(p, plan, s)
-                          : launch_stream_typed<float, false>(p, plan, s);
-        case CE_BF16:
-            return p.grad ? launch_stream_typed<__nv_bfloat16, true>(p, plan, s)
-                          : launch_stream_typed<__nv_bfloat16, false>(p, plan, s);
-        default:
-            return p.grad ? launch_stream_typed<__half, true>(p, plan, s)
-                          : launch_stream_typed<__half, false>(p, plan, s);
-    }
-}
-
 }  // namespace gbce
