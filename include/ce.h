@@ -285,11 +285,14 @@ ce_status ce_vp_bwd(const void* shard_logits, ce_dtype dtype, int64_t dim0, int6
 /* lm_head + cross-entropy, chunked over token rows (the sequence-chunked
  * lm_head + loss of the TorchTitan ChunkedLossWrapper that hyper-parallel
  * #269 describes: the full (N, V) logits never exist).  For each chunk of
- * chunk_rows rows: logits = hidden . weight^T (a cuBLAS GEMM into the
- * workspace), the cross-entropy pass of this library on them (gradient in
- * place, scaled with the kept-row count of the whole batch), then
- * grad_hidden = dlogits . weight and grad_weight += dlogits^T . hidden (cuBLAS
- * GEMMs, fp32 accumulation).
+ * chunk_rows rows: logits = hidden . weight^T into the workspace -- for
+ * bf16 / fp16 with H a multiple of 8 and 16-byte aligned hidden and weight,
+ * this library's tcgen05 GEMM, whose epilogue also folds every (row,
+ * 256-column tile) into softmax statistics that a per-row combine turns into
+ * lse and the loss, then the backward from lse writes the gradient in place;
+ * otherwise a cuBLAS GEMM and this library's fused pass -- scaled with the
+ * kept-row count of the whole batch; then grad_hidden = dlogits . weight and
+ * grad_weight += dlogits^T . hidden (cuBLAS GEMMs, fp32 accumulation).
  *   hidden       (N, H) row-major, dtype; weight (V, H) row-major, dtype.
  *   targets      int64 [N], contiguous.
  *   loss_out     one value (reduce_loss) or N values.
@@ -297,7 +300,8 @@ ce_status ce_vp_bwd(const void* shard_logits, ce_dtype dtype, int64_t dim0, int6
  *   grad_weight  (V, H) row-major float32, ACCUMULATED into (zero it first for
  *                a fresh gradient); or NULL.
  *   workspace    ce_linear_workspace_bytes(N, H, V, dtype, chunk_rows) bytes,
- *                256-byte aligned; it holds one chunk of logits and cuBLAS's
+ *                256-byte aligned; it holds one chunk of logits (rows padded
+ *                to a multiple of 8 elements), their statistics and cuBLAS's
  *                workspace.  cuBLAS creates one handle per host thread and
  *                device on first use (its own small allocation).
  * Returns CE_OK once every kernel and GEMM is enqueued on `stream`. */

@@ -1,5 +1,8 @@
-"""lm_head + cross-entropy chunked over rows (cuBLAS GEMMs around this
-library's pass) against the CPU oracle of the same dataflow.
+"""lm_head + cross-entropy chunked over rows against the CPU oracle of the
+same dataflow: bf16/fp16 take this library's tcgen05 GEMM with the
+cross-entropy statistics in its epilogue, then the backward from lse; fp32
+(and hidden sizes off a multiple of 8) a cuBLAS GEMM and the fused pass; the
+gradient GEMMs are cuBLAS's.
 
 Tolerances: the loss as for the pass, plus one unit in the last place of the
 row's target logit (the GEMM's float32 sum and the oracle's double sum may
@@ -28,6 +31,12 @@ TDT = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
     (1200, 64, 20000, "bf16", 400, 0.1, True),
     (100, 64, 3000, "f32", 37, 0.1, False),
     (150, 128, 6000, "f16", 1000, 0.0, True),     # one chunk
+    # the tensor-core GEMM: 2 x 63 tiles of 128 x 256 per chunk (several per
+    # CTA, both accumulators in turn) and 8 K steps (twice round the ring)
+    (777, 512, 16000, "bf16", 256, 0.1, True),
+    (300, 256, 4001, "bf16", 300, 0.0, False),    # odd vocabulary: padded logits rows
+    (260, 320, 5000, "f16", 130, 0.1, False),     # 5 K steps, the last half out of range
+    (200, 100, 3000, "bf16", 100, 0.1, True),     # hidden size off 8: the cuBLAS path
 ])
 def test_linear_ce_matches_oracle(N, H, V, dtype, chunk, a, red):
     rng = np.random.default_rng(N + V)

@@ -17,7 +17,8 @@ ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libgbce.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
 SOURCES = ["ce_api.cu", "ce_aux.cu", "ce_bwd.cu", "ce_fused.cu", "ce_rows.cu", "ce_split.cu",
-           "ce_vecrow.cu", "ce_linear.cu", "ce_stream.cu", "ce_stream_geo.cu", "ce_vp.cu"]
+           "ce_vecrow.cu", "ce_linear.cu", "ce_lmhead.cu", "ce_stream.cu", "ce_stream_geo.cu",
+           "ce_vp.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", f"-I{os.path.join(ROOT, 'include')}"]

@@ -172,6 +172,29 @@ cudaError_t launch_vp_combine(const VpCombineProblem& vc, cudaStream_t s);
 cudaError_t launch_split(const Problem& p, const SplitPlan& plan, float4* partials,
                          cudaStream_t s);
 
+// lm_head logits of one chunk of rows on the tensor cores (ce_lmhead.cu), with
+// the cross-entropy statistics of every (row, 256-column tile) in the GEMM's
+// epilogue, then combined per row into lse and the row's loss.
+struct LmHeadProblem {
+    const void* hidden;        // (rows, H) row-major, 16-byte aligned
+    const void* weight;        // (V, H) row-major, 16-byte aligned
+    int dtype;                 // CE_BF16 or CE_F16
+    int64_t rows, H, V;
+    int64_t ldl;               // elements between rows of the logits output (multiple of 8)
+    void* logits;              // out: (rows, ldl), the logits rounded to the dtype
+    float4* part;              // scratch: [rows][ceil(V/256)] {m, d, S, x_y}
+    const int64_t* targets;    // [rows], contiguous
+    int64_t ignore_idx;
+    float a;                   // label smoothing
+    float* loss_rows;          // out: per-row loss (0 ignored, NaN out of range)
+    float* lse;                // out: per-row logsumexp (NaN ignored / out of range)
+    uint32_t* err;             // device error word
+};
+bool lmhead_supported(int dtype, int64_t H, int64_t V, const void* hidden, const void* weight);
+size_t lmhead_part_bytes(int64_t rows, int64_t V);
+int64_t lmhead_ldl(int64_t V);
+cudaError_t launch_lmhead(const LmHeadProblem& lp, cudaStream_t s);
+
 // Used by the lm_head + cross-entropy orchestration (ce_linear.cu).
 cudaError_t launch_main_pass(Problem& pb, const ce_options* o, float4* partials, size_t partial_bytes,
                              cudaStream_t s);

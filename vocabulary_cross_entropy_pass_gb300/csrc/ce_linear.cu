@@ -5,18 +5,23 @@
 // chunk of the sequence at a time so that the full (B*L, V) logits never
 // exist, bounding their O(B*L*V) peak memory.  Here, for each chunk of rows:
 //
-//   1. logits_c = hidden_c . weight^T       cuBLAS GEMM (tensor cores), into a
-//                                           chunk buffer of the workspace;
-//   2. the cross-entropy pass of this library on that buffer (loss per row,
-//      gradient written in place over the chunk's logits), scaled with the
-//      kept-row count of the whole batch (counted once, up front);
-//   3. grad_hidden_c = dlogits_c . weight    cuBLAS GEMM;
+//   1. bf16 / fp16 (hidden size a multiple of 8, 16-byte aligned operands):
+//      this library's tcgen05 GEMM (ce_lmhead.cu) writes logits_c = hidden_c .
+//      weight^T into a chunk buffer of the workspace and the cross-entropy
+//      statistics of every (row, 256-column tile) from its epilogue; a
+//      per-row combine turns them into lse and the row's loss; then the
+//      backward from the saved lse (ce_bwd's kernel) writes the gradient in
+//      place over the chunk's logits;
+//      otherwise: a cuBLAS GEMM into the chunk buffer, then the fused
+//      cross-entropy pass of this library on it;
+//      either way scaled with the kept-row count of the whole batch (counted
+//      once, up front);
+//   2. grad_hidden_c = dlogits_c . weight    cuBLAS GEMM;
 //      grad_weight  += dlogits_c^T . hidden_c cuBLAS GEMM, float32 accumulation.
 //
-// The three products are plain library GEMMs; the pass between them is this
-// library's kernels.  At a hidden size in the thousands the GEMMs dominate
-// (about 6*H flops per logit against a few bytes of logits traffic), so the
-// chunk buffer's round trip through memory costs little.
+// At a hidden size in the thousands the GEMMs dominate (about 6*H flops per
+// logit against a few bytes of logits traffic), so the chunk buffer's round
+// trip through memory costs little.
 #include <cublas_v2.h>
 #include <string.h>
 
@@ -53,15 +58,21 @@ cudaDataType_t cuda_type(int dtype) {
 }
 
 struct LinLayout {
-    size_t rows_off, chunk_off, part_off, cublas_off, total;
+    size_t rows_off, chunk_off, lse_off, part_off, cublas_off, total;
 };
 
+// Workspace: header, per-row losses (N), one chunk of logits (rows padded to
+// a multiple of 8 elements), the chunk's lse, partials (two-stage path, or
+// the tensor-core path's per-tile statistics), cuBLAS's workspace.
 LinLayout lin_layout(int64_t N, int64_t V, int es, int64_t chunk_rows) {
     LinLayout L;
     L.rows_off = kWsHeaderBytes;
     L.chunk_off = L.rows_off + align_up((size_t)N * sizeof(float), 256);
-    L.part_off = L.chunk_off + align_up((size_t)chunk_rows * (size_t)V * es, 256);
-    L.cublas_off = L.part_off + partial_bytes_for(chunk_rows, V);
+    L.lse_off = L.chunk_off + align_up((size_t)chunk_rows * (size_t)lmhead_ldl(V) * es, 256);
+    L.part_off = L.lse_off + align_up((size_t)chunk_rows * sizeof(float), 256);
+    const size_t parts = partial_bytes_for(chunk_rows, V);
+    const size_t tiles = lmhead_part_bytes(chunk_rows, V);
+    L.cublas_off = L.part_off + (parts > tiles ? parts : tiles);
     L.total = L.cublas_off + kCublasWorkspaceBytes;
     return L;
 }
@@ -129,44 +140,100 @@ ce_status ce_linear_fwd_bwd(const void* hidden, const void* weight, ce_dtype dty
     const float one = 1.f, zero = 0.f;
     char* chunk = w + L.chunk_off;
     const char* hid = static_cast<const char*>(hidden);
+    const bool grads = grad_hidden != nullptr || grad_weight != nullptr;
+    // the tensor-core path: this library's GEMM with the statistics in its
+    // epilogue; its chunk rows are padded to a multiple of 8 elements
+    const bool tc = lmhead_supported(dtype, H, V, hidden, weight);
+    const int64_t ld = tc ? lmhead_ldl(V) : V;
 
     for (int64_t r0 = 0; r0 < N; r0 += chunk_rows) {
         const int64_t rows = (N - r0 < chunk_rows) ? N - r0 : chunk_rows;
-        // 1. logits of the chunk, row-major (rows, V): column-major C[V, rows] = W^T-op . h
-        if (cublasGemmEx(h, CUBLAS_OP_T, CUBLAS_OP_N, (int)V, (int)rows, (int)H, &one, weight, ty,
-                         (int)H, hid + (size_t)r0 * H * es, ty, (int)H, &zero, chunk, ty, (int)V,
-                         CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
-            return CE_ERR_LAUNCH;
-        // 2. the cross-entropy pass over the chunk, gradient in place, after
-        //    the GEMM has completed (see ce_order_kernel)
-        ce_order_kernel<<<1, 32, 0, s>>>();
-        if (cudaGetLastError() != cudaSuccess) return CE_ERR_LAUNCH;
-        const int64_t c_strides[3] = {rows * V, V, 1};
-        const int64_t ct_strides[2] = {rows, 1};
-        Problem pb;
-        problem_init(pb, chunk, dtype, 1, rows, V, c_strides, targets + r0, ct_strides,
-                     label_smoothing, ignore_idx, reduce_loss);
-        pb.err = all.err;
-        pb.n_dev = all.n_dev;
-        pb.ticket = all.ticket;
-        pb.row_claim = all.row_claim;  // zeroed by the count kernel, then by each pass's last CTA
-        pb.row_done = all.row_done;
-        pb.dloss = reduce_loss ? dloss : (dloss ? dloss + r0 : nullptr);
-        pb.loss_rows = all.loss_rows + r0;
-        pb.grad = grad_hidden != nullptr || grad_weight != nullptr;
-        if (launch_main_pass(pb, nullptr, reinterpret_cast<float4*>(w + L.part_off),
-                             L.cublas_off - L.part_off, s) != cudaSuccess)
-            return CE_ERR_LAUNCH;
-        // 3. gradients through the projection
+        if (tc) {
+            // 1. logits of the chunk and their per-tile statistics, then lse
+            //    and the row losses
+            LmHeadProblem lp;
+            memset(&lp, 0, sizeof lp);
+            lp.hidden = hid + (size_t)r0 * H * es;
+            lp.weight = weight;
+            lp.dtype = dtype;
+            lp.rows = rows;
+            lp.H = H;
+            lp.V = V;
+            lp.ldl = ld;
+            lp.logits = chunk;
+            lp.part = reinterpret_cast<float4*>(w + L.part_off);
+            lp.targets = targets + r0;
+            lp.ignore_idx = ignore_idx;
+            lp.a = label_smoothing;
+            lp.loss_rows = all.loss_rows + r0;
+            lp.lse = reinterpret_cast<float*>(w + L.lse_off);
+            lp.err = all.err;
+            if (launch_lmhead(lp, s) != cudaSuccess) return CE_ERR_LAUNCH;
+            //    the gradient in place over the chunk's logits, from lse
+            if (grads) {
+                BwdProblem bp;
+                memset(&bp, 0, sizeof bp);
+                bp.logits = chunk;
+                bp.grad = chunk;
+                bp.dtype = dtype;
+                bp.dim1 = rows;
+                bp.N = rows;
+                bp.V = V;
+                bp.s0 = rows * ld;
+                bp.s1 = ld;
+                bp.gs0 = rows * ld;
+                bp.gs1 = ld;
+                bp.targets = targets + r0;
+                bp.ts0 = rows;
+                bp.ts1 = 1;
+                bp.ignore_idx = ignore_idx;
+                bp.lse = lp.lse;
+                bp.a = label_smoothing;
+                bp.reduce = reduce_loss ? 1 : 0;
+                bp.dloss = reduce_loss ? dloss : (dloss ? dloss + r0 : nullptr);
+                bp.n_dev = all.n_dev;
+                bp.vec_ok = true;
+                bp.vocab_offset = 0;
+                bp.V_total = V;
+                if (launch_bwd(bp, s) != cudaSuccess) return CE_ERR_LAUNCH;
+            }
+        } else {
+            // 1. logits of the chunk, row-major (rows, V): column-major C[V, rows] = W^T-op . h
+            if (cublasGemmEx(h, CUBLAS_OP_T, CUBLAS_OP_N, (int)V, (int)rows, (int)H, &one, weight, ty,
+                             (int)H, hid + (size_t)r0 * H * es, ty, (int)H, &zero, chunk, ty, (int)V,
+                             CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
+                return CE_ERR_LAUNCH;
+            //    the cross-entropy pass over the chunk, gradient in place,
+            //    after the GEMM has completed (see ce_order_kernel)
+            ce_order_kernel<<<1, 32, 0, s>>>();
+            if (cudaGetLastError() != cudaSuccess) return CE_ERR_LAUNCH;
+            const int64_t c_strides[3] = {rows * V, V, 1};
+            const int64_t ct_strides[2] = {rows, 1};
+            Problem pb;
+            problem_init(pb, chunk, dtype, 1, rows, V, c_strides, targets + r0, ct_strides,
+                         label_smoothing, ignore_idx, reduce_loss);
+            pb.err = all.err;
+            pb.n_dev = all.n_dev;
+            pb.ticket = all.ticket;
+            pb.row_claim = all.row_claim;  // zeroed by the count kernel, then by each pass's last CTA
+            pb.row_done = all.row_done;
+            pb.dloss = reduce_loss ? dloss : (dloss ? dloss + r0 : nullptr);
+            pb.loss_rows = all.loss_rows + r0;
+            pb.grad = grads;
+            if (launch_main_pass(pb, nullptr, reinterpret_cast<float4*>(w + L.part_off),
+                                 L.cublas_off - L.part_off, s) != cudaSuccess)
+                return CE_ERR_LAUNCH;
+        }
+        // 2. gradients through the projection
         if (grad_hidden &&
             cublasGemmEx(h, CUBLAS_OP_N, CUBLAS_OP_N, (int)H, (int)rows, (int)V, &one, weight, ty,
-                         (int)H, chunk, ty, (int)V, &zero,
+                         (int)H, chunk, ty, (int)ld, &zero,
                          static_cast<char*>(grad_hidden) + (size_t)r0 * H * es, ty, (int)H,
                          CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
             return CE_ERR_LAUNCH;
         if (grad_weight &&
             cublasGemmEx(h, CUBLAS_OP_N, CUBLAS_OP_T, (int)H, (int)V, (int)rows, &one,
-                         hid + (size_t)r0 * H * es, ty, (int)H, chunk, ty, (int)V, &one, grad_weight,
+                         hid + (size_t)r0 * H * es, ty, (int)H, chunk, ty, (int)ld, &one, grad_weight,
                          CUDA_R_32F, (int)H, CUBLAS_COMPUTE_32F,
                          CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
             return CE_ERR_LAUNCH;

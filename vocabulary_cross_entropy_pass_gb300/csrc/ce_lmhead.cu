@@ -1,0 +1,493 @@
+// ce_lmhead.cu -- the lm_head projection on the 5th-generation tensor cores
+// with the cross-entropy statistics in its epilogue.
+//
+// hyper-parallel #269 (background: the TorchTitan ChunkedLossWrapper) runs the
+// lm_head projection and the loss a chunk of rows at a time.  Here the logits
+// tiles come off the tensor cores straight into the online-softmax
+// statistics.  For one chunk of rows, logits = hidden . W^T:
+//
+//   ce_lmhead_kernel   a persistent kernel over 128 x 256 output tiles:
+//     warp 0   issues TMA tile loads (128-byte swizzle) of hidden (128 x 64)
+//              and W (256 x 64) into a 4-deep ring of shared-memory stages;
+//     warp 1   owns the tensor memory (two 256-column fp32 accumulators) and,
+//              from one thread, issues tcgen05.mma (M 128, N 256, K 16) over
+//              the ring, committing each stage back to the producer and each
+//              finished accumulator to the epilogue;
+//     warps 2-5  the epilogue: each thread reads its row of the accumulator
+//              (tcgen05.ld, 32 columns at a time), rounds every logit to the
+//              storage dtype (the logits the chunked pass works on), stores
+//              them, and folds them into the tile's row partial -- running max
+//              m, sum of exp(x - m), plain sum S, and the target logit when the
+//              target's column lies in the tile -- written as one float4 per
+//              (row, tile).  While it works, the MMA warp fills the other
+//              accumulator.
+//   ce_lm_combine_kernel  per row, the tiles' partials folded in a fixed
+//     order -- the (m, d, x_y) combine of the vocabulary-parallel ranks of
+//     hyper-parallel #269 section 3.1 -- into lse and the row's loss
+//     lse - (1-a) x_y - (a/V) S (CSDN "Ascend CANN ops-nn cross-entropy
+//     fusion", "Fusion scheme: log_softmax + NLL"; smoothing over V).
+//
+// Every wait is an mbarrier poll bounded by %globaltimer; a wait that gives up
+// sets CE_DEVERR_TIMEOUT, stops the kernel's roles, lets issued copies and
+// MMAs complete (bounded) and frees the tensor memory before returning.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "ce_device.cuh"
+#include "ce_internal.h"
+
+namespace gbce {
+namespace {
+
+constexpr int kBM = 128;   // tile rows (hidden rows)
+constexpr int kBN = 256;   // tile columns (vocabulary)
+constexpr int kBK = 64;    // K per stage: 64 16-bit values = one 128-byte swizzle row
+constexpr int kStages = 4;
+constexpr int kABytes = kBM * kBK * 2;          // 16 KB
+constexpr int kBBytes = kBN * kBK * 2;          // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;  // 48 KB
+constexpr int kLmThreads = 192;                 // 6 warps
+constexpr uint32_t kTmemCols = 2 * kBN;         // two fp32 accumulators
+constexpr size_t kLmSmem = (size_t)kStages * kStageBytes + 1024 /* alignment */ + 256;
+
+struct LmArgs {
+    int64_t rows;             // rows of this chunk
+    int64_t V;
+    int64_t ldl;              // elements between logits rows in the output
+    char* logits;             // out: (rows, ldl) in the storage dtype
+    float4* part;             // out: [rows][ntn] {m, d, S, x_y}
+    const int64_t* targets;   // [rows]
+    int64_t ignore_idx;
+    int mb, ntn;              // row blocks, column tiles
+    int ksteps;               // ceil(H / 64)
+    uint32_t* err;
+};
+
+// ------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int x, int y,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Arrives on `bar` once every tcgen05.mma this thread issued so far is done.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+// D[tmem] (+)= A[smem] . B[smem]^T, both K-major; accumulate when acc != 0.
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+          "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+          "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+          "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor of a K-major operand written by TMA with
+// the 128-byte swizzle: 8-row atoms of 128 bytes, 1024 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address
+    d |= (uint64_t)1 << 16;                              // leading offset (unused with this swizzle)
+    d |= (uint64_t)(1024 >> 4) << 32;                    // stride offset: next 8-row atom
+    d |= (uint64_t)1 << 46;                              // descriptor version
+    d |= (uint64_t)2 << 61;                              // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, A and B of the
+// storage type (bf16 or fp16, both the same), both K-major, M 128, N 256.
+template <typename T>
+struct AbFormat;  // operand format code of kind::f16
+template <>
+struct AbFormat<__half> {
+    static constexpr uint32_t kCode = 0;
+};
+template <>
+struct AbFormat<__nv_bfloat16> {
+    static constexpr uint32_t kCode = 1;
+};
+
+template <typename T>
+__host__ __device__ constexpr uint32_t idesc_f16() {
+    return (1u << 4) | (AbFormat<T>::kCode << 7) | (AbFormat<T>::kCode << 10) |
+           ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+}
+
+// Round to the storage dtype and back (the value the chunk buffer holds).
+template <typename T>
+__device__ __forceinline__ float round_store(float x);
+template <>
+__device__ __forceinline__ float round_store<__nv_bfloat16>(float x) {
+    return __bfloat162float(__float2bfloat16_rn(x));
+}
+template <>
+__device__ __forceinline__ float round_store<__half>(float x) {
+    return __half2float(__float2half_rn(x));
+}
+
+// ------------------------------------------------------------ the GEMM + statistics kernel
+template <typename T>
+__global__ void __launch_bounds__(kLmThreads, 1)
+ce_lmhead_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const __grid_constant__ LmArgs p) {
+    extern __shared__ uint8_t smem_raw[];
+    // stages on a 1024-byte boundary: the swizzle atoms (8 rows of 128 bytes)
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t* sm = smem_raw + (sbase - raw);
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + (size_t)kStages * kStageBytes);
+    uint64_t* empty = full + kStages;
+    uint64_t* tfull = empty + kStages;  // [2] accumulator b holds a finished tile
+    uint64_t* tempty = tfull + 2;       // [2] the epilogue has read accumulator b
+    uint64_t* done = tempty + 2;        // every MMA issued has completed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 4);  // one arrival per epilogue warp
+        }
+        mbar_init(done, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int ntiles = p.mb * p.ntn;
+    auto give_up = [&]() {
+        atomicOr(p.err, CE_DEVERR_TIMEOUT);
+        *abort_flag = 1;
+    };
+
+    if (warp == 0) {
+        // ---------------------------------------------------- TMA producer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0, issued = 0;
+            for (int t = blockIdx.x; t < ntiles && !*abort_flag; t += gridDim.x) {
+                const int mblk = t % p.mb, nblk = t / p.mb;
+                for (int k = 0; k < p.ksteps; ++k) {
+                    if (!mbar_wait_bounded(&empty[s], ph ^ 1u)) {
+                        give_up();
+                        break;
+                    }
+                    const uint32_t st = sbase + (uint32_t)(s * kStageBytes);
+                    mbar_arrive_expect_tx(&full[s], (uint32_t)kStageBytes);
+                    tma_load_2d(st, &tmA, k * kBK, mblk * kBM, &full[s]);
+                    tma_load_2d(st + kABytes, &tmB, k * kBK, nblk * kBN, &full[s]);
+                    ++issued;
+                    if (++s == kStages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (*abort_flag) {
+                // let every copy already issued land before the CTA goes away
+                for (int q = 0; q < kStages; ++q)
+                    if (issued > (uint32_t)q) {
+                        const uint32_t last = (issued - 1u - (uint32_t)q) / (uint32_t)kStages;
+                        (void)mbar_wait_bounded(&full[q], last & 1u);
+                    }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16<T>();
+            int s = 0;
+            uint32_t ph = 0;
+            int it = 0;
+            for (int t = blockIdx.x; t < ntiles && !*abort_flag; t += gridDim.x, ++it) {
+                const int b = it & 1;
+                const uint32_t bph = (uint32_t)(it >> 1) & 1u;
+                if (!mbar_wait_bounded(&tempty[b], bph ^ 1u)) {  // the epilogue drained it
+                    give_up();
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(b * kBN);
+                bool ok = true;
+                for (int k = 0; k < p.ksteps; ++k) {
+                    if (!mbar_wait_bounded(&full[s], ph)) {
+                        give_up();
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = sbase + (uint32_t)(s * kStageBytes);
+                    const uint32_t b_addr = a_addr + kABytes;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)  // K 16 per MMA: 32 bytes along the row
+                        tc_mma(d, sdesc_sw128(a_addr + kk * 32), sdesc_sw128(b_addr + kk * 32), idesc,
+                               (k | kk) != 0);
+                    tc_commit(&empty[s]);  // the stage is free once these MMAs are done
+                    if (++s == kStages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(&tfull[b]);  // accumulator b is complete
+            }
+            tc_commit(done);
+            (void)mbar_wait_bounded(done, 0);
+        }
+    } else {
+        // ---------------------------------------------------- epilogue
+        const int q = warp & 3;            // this warp's quarter of the TMEM lanes
+        const int rin = q * 32 + lane;     // row within the tile
+        int it = 0;
+        for (int t = blockIdx.x; t < ntiles && !*abort_flag; t += gridDim.x, ++it) {
+            const int b = it & 1;
+            const uint32_t bph = (uint32_t)(it >> 1) & 1u;
+            const int mblk = t % p.mb, nblk = t / p.mb;
+            if (!__all_sync(kFull, mbar_wait_bounded(&tfull[b], bph))) {
+                if (lane == 0) give_up();
+                break;
+            }
+            tc_fence_after();
+            const int64_t row = (int64_t)mblk * kBM + rin;
+            const bool live = row < p.rows;
+            const int64_t y = live ? __ldg(p.targets + row) : p.ignore_idx;
+            const int64_t j0 = (int64_t)nblk * kBN;
+            T* out = reinterpret_cast<T*>(p.logits) + row * p.ldl;
+            float m = -INFINITY, d = 0.f, S = 0.f, xy = 0.f;
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * kBN);
+#pragma unroll 1
+            for (int c = 0; c < kBN / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tbase + (uint32_t)(c * 32), v);
+                tmem_wait_ld();
+                const int64_t jc = j0 + c * 32;
+                const int nval = (int)max((int64_t)0, min((int64_t)32, p.V - jc));
+                float x[32];
+                float cm = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    x[i] = round_store<T>(__uint_as_float(v[i]));
+                    if (i < nval) cm = fmaxf(cm, x[i]);
+                }
+                if (cm > m) {
+                    if (m != -INFINITY) d *= ex2_approx((m - cm) * kLog2e);
+                    m = cm;
+                }
+                const float nm = -m * kLog2e;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    if (i < nval) {
+                        d += ex2_approx(fmaf(x[i], kLog2e, nm));
+                        S += x[i];
+                    }
+                    if (jc + i == y) xy = x[i];
+                }
+                if (live) {
+                    if (nval == 32) {
+                        uint4* o4 = reinterpret_cast<uint4*>(out + jc);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            float2 pr[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) pr[e] = make_float2(x[8 * u + 2 * e], x[8 * u + 2 * e + 1]);
+                            o4[u] = Vec<T>::pack2(pr);
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (i < nval) Vec<T>::store1(out + jc + i, x[i]);
+                    }
+                }
+            }
+            // every read of accumulator b is done: hand it back to the MMA warp
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[b]);
+            if (live) p.part[row * p.ntn + nblk] = make_float4(m, d, S, xy);
+        }
+    }
+
+    // teardown: every role has finished (or given up); free the tensor memory
+    __syncwarp();  // lane 0 of warps 0 and 1 ran their role alone
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+// ------------------------------------------------------------ per-row combine of the tiles
+// One warp per row: lane l folds tiles l, l + 32, ... in order, then a fixed
+// butterfly; the target's tile gives x_y.
+__global__ void __launch_bounds__(256) ce_lm_combine_kernel(const float4* __restrict__ part, int ntn,
+                                                            int64_t rows, int64_t V,
+                                                            const int64_t* __restrict__ targets,
+                                                            int64_t ignore_idx, float a,
+                                                            float* __restrict__ loss,
+                                                            float* __restrict__ lse_out) {
+    const int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const int64_t y = __ldg(targets + row);
+    if (y == ignore_idx || y < 0 || y >= V) {  // out of range: the count kernel set the error bit
+        if (lane == 0) {
+            loss[row] = (y == ignore_idx) ? 0.f : __int_as_float(0x7fc00000);
+            lse_out[row] = __int_as_float(0x7fc00000);
+        }
+        return;
+    }
+    const float4* pr = part + row * (int64_t)ntn;
+    Part G = part_identity();
+    for (int t = lane; t < ntn; t += 32) {
+        const float4 v = __ldg(pr + t);
+        G = part_combine(G, Part{v.x, v.y, v.z});
+    }
+    G = warp_allreduce_part(G);
+    if (lane == 0) {
+        const float xy = __ldg(pr + y / kBN).w;
+        const float l = G.m + logf(G.d);
+        loss[row] = l - (1.f - a) * xy - (a / (float)V) * G.S;
+        lse_out[row] = l;
+    }
+}
+
+// ------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// A 2-D row-major (outer x inner) 16-bit matrix, boxes of box_outer x 64.
+bool make_map(CUtensorMap* m, const void* ptr, int dtype, uint64_t inner, uint64_t outer,
+              uint32_t box_outer) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {inner * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kBK, box_outer};
+    const cuuint32_t es[2] = {1, 1};
+    return fn(m, dtype == CE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+              const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename T>
+cudaError_t launch_lmhead_typed(const LmHeadProblem& lp, cudaStream_t s) {
+    CUtensorMap ta, tb;
+    memset(&ta, 0, sizeof ta);
+    memset(&tb, 0, sizeof tb);
+    if (!make_map(&ta, lp.hidden, lp.dtype, (uint64_t)lp.H, (uint64_t)lp.rows, kBM) ||
+        !make_map(&tb, lp.weight, lp.dtype, (uint64_t)lp.H, (uint64_t)lp.V, kBN))
+        return cudaErrorInvalidValue;
+    LmArgs a;
+    memset(&a, 0, sizeof a);
+    a.rows = lp.rows;
+    a.V = lp.V;
+    a.ldl = lp.ldl;
+    a.logits = static_cast<char*>(lp.logits);
+    a.part = lp.part;
+    a.targets = lp.targets;
+    a.ignore_idx = lp.ignore_idx;
+    a.mb = (int)((lp.rows + kBM - 1) / kBM);
+    a.ntn = (int)((lp.V + kBN - 1) / kBN);
+    a.ksteps = (int)((lp.H + kBK - 1) / kBK);
+    a.err = lp.err;
+    auto kern = ce_lmhead_kernel<T>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLmSmem);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t ntiles = (int64_t)a.mb * a.ntn;
+    const int grid = (int)(ntiles < sms ? ntiles : sms);
+    kern<<<grid, kLmThreads, kLmSmem, s>>>(ta, tb, a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int rows_per_cta = 8;
+    ce_lm_combine_kernel<<<(unsigned)((lp.rows + rows_per_cta - 1) / rows_per_cta), 32 * rows_per_cta, 0,
+                           s>>>(lp.part, a.ntn, lp.rows, lp.V, lp.targets, lp.ignore_idx, lp.a,
+                                lp.loss_rows, lp.lse);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool lmhead_supported(int dtype, int64_t H, int64_t V, const void* hidden, const void* weight) {
+    if (dtype != CE_BF16 && dtype != CE_F16) return false;
+    if (H % 8 || H > 0x7fffffffLL || V > 0x7fffffffLL) return false;  // 16-byte TMA row strides
+    if (reinterpret_cast<uintptr_t>(hidden) % 16 || reinterpret_cast<uintptr_t>(weight) % 16) return false;
+    return encode_fn() != nullptr;
+}
+
+size_t lmhead_part_bytes(int64_t rows, int64_t V) {
+    return align_up((size_t)rows * (size_t)((V + kBN - 1) / kBN) * sizeof(float4), 256);
+}
+
+int64_t lmhead_ldl(int64_t V) { return (V + 7) / 8 * 8; }
+
+cudaError_t launch_lmhead(const LmHeadProblem& lp, cudaStream_t s) {
+    if (lp.rows <= 0) return cudaSuccess;
+    if (lp.ldl % 8 || lp.ldl < lp.V) return cudaErrorInvalidValue;
+    return lp.dtype == CE_BF16 ? launch_lmhead_typed<__nv_bfloat16>(lp, s)
+                               : launch_lmhead_typed<__half>(lp, s);
+}
+
+}  // namespace gbce
