@@ -218,6 +218,37 @@ def oracle_rows_per_s(w, x_host, t_host, budget_s: float, block: int = 256, max_
     return rows_done / t_used, rows_done, t_used, oracle.num_threads(lib)
 
 
+def torch_cross_entropy(w, x, t, steps: int = 5, warmup: int = 3) -> dict:
+    """PyTorch's own cross-entropy on the same device logits, for context:
+    F.cross_entropy (mean, ignore_index, label_smoothing) and its autograd
+    backward per step, timed with CUDA events on the current stream."""
+    import torch
+    import torch.nn.functional as F
+    xr = x.view(w.N, w.V).detach().requires_grad_(True)
+    tr = t.reshape(-1)
+
+    def step():
+        loss = F.cross_entropy(xr, tr, ignore_index=w.ignore_idx,
+                               label_smoothing=w.label_smoothing,
+                               reduction="mean" if w.reduce_loss else "none")
+        (loss if w.reduce_loss else loss.sum()).backward()
+        xr.grad = None
+
+    for _ in range(warmup):
+        step()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    s0.record()
+    for _ in range(steps):
+        step()
+    s1.record()
+    torch.cuda.synchronize()
+    ms = s0.elapsed_time(s1) / steps
+    return {"value": w.N / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
+            "what": "torch.nn.functional.cross_entropy forward + autograd backward (eager, "
+                    f"torch {torch.__version__}) on the same device logits"}
+
+
 # ----------------------------------------------------------------- arms
 def run_reference(args, w, rank: int, world: int) -> None:
     if rank != 0:
@@ -533,6 +564,7 @@ def run_ours(args, w, rank: int, world: int, dist) -> None:
     peaks = measured_peaks()
     nbytes = pass_bytes(w.N, w.V, w.elem_bytes)
     traffic = profiled_traffic(w, path)
+    torch_ref = None if args.no_torch_ref else torch_cross_entropy(w, x, t)
     achieved = nbytes / (kernel_ms / 1e3) / 1e9
     cpu = None
     if not args.no_cpu_baseline:
@@ -570,6 +602,7 @@ def run_ours(args, w, rank: int, world: int, dist) -> None:
                        "(two device buffers: the copy of step k+1 overlaps the pass of "
                        "step k) and the loss read back"},
         "gpu_launches": kernels_per_step(path, w.reduce_loss) * args.steps,
+        "torch_cross_entropy": torch_ref,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
@@ -586,6 +619,7 @@ def main(argv=None) -> int:
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--ref-rows", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-torch-ref", action="store_true")
     # secondary passes: "split" = ce_fwd_only + ce_bwd (autograd order), "vp" = the
     # vocabulary-parallel steps over --vocab-shards shards on one GPU, "weighted" =
     # the class-weighted pass, "linear" = lm_head + cross-entropy chunked over rows
