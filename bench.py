@@ -602,7 +602,7 @@ def run_ours(args, w, rank: int, world: int, dist) -> None:
                      "traffic_source": "ncu dram__bytes_read of the committed capture "
                                        "(profiles/ce_stream_kernel_traffic.json) scaled by "
                                        "rows + the required gradient write N*V*s",
-                     "achieved_is": "algorithmic bytes (north-star formula: logits read + "
+                     "achieved_is": "algorithmic bytes (logits read + "
                                     "gradient write + targets) / kernel time",
                      "dram_gbs": traffic / (kernel_ms / 1e3) / 1e9 if traffic else None,
                      "dram_frac": traffic / (kernel_ms / 1e3) / 1e9 / peaks["hbm_gbs"]
