@@ -180,7 +180,8 @@ Plan make_plan(const Problem& p, const ce_options* o) {
         const int vec = 16 / p.es;
         const int64_t C = round_up_int((p.V + K - 1) / K, vec);
         const int64_t nch = (p.V + C - 1) / C;
-        if (nch <= kMaxStreamChunks && plan_stream(o, &pl.stream, 16, 6) &&
+        // (a chunk's byte count is kept in 32 bits)
+        if (nch <= kMaxStreamChunks && C * p.es <= 0xffffffffLL && plan_stream(o, &pl.stream, 16, 6) &&
             pl.stream.threads == 256) {
             pl.stream.geo = kStreamChunks;
             pl.stream.chunk_elems = C;

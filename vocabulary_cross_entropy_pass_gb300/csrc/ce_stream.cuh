@@ -876,7 +876,7 @@ cudaError_t launch_stream_one(const Problem& pb, const StreamPlan& plan, float4*
         if (C < 1 || (C * (int64_t)sizeof(T)) % 16) return cudaErrorInvalidValue;
         const int64_t CB = C * (int64_t)sizeof(T);
         const int64_t nchunks = (pb.V + C - 1) / C;
-        if (nchunks > kMaxStreamChunks) return cudaErrorInvalidValue;
+        if (nchunks > kMaxStreamChunks || CB > 0xffffffffLL) return cudaErrorInvalidValue;
         const int64_t tpc = (CB + TB - 1) / TB;
         const int64_t last = row_bytes - (nchunks - 1) * CB;
         a.chunk_elems = C;
