@@ -339,6 +339,37 @@ def test_warp_path_tiles(V, dtype, tile_kb, stages):
         _compare(w, x, t, loss, xd, n)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("V", [4096, 8192, 12000])
+def test_warp_rows_wide_range(dtype, V):
+    """16-bit rows on the warp path with extreme ranges: spikes of +60 to
+    +120 away from and inside the first vectors, hugely negative first
+    vectors and single elements, a uniform shift of -1000; against the
+    oracle."""
+    N = 24
+    w = wl.Workload("warp_range", 1, N, V, dtype, sigma=2.0, label_smoothing=0.1,
+                    reduce_loss=False, seed=7700 + V)
+    x = wl.logits(w).float()
+    low = -1e30 if dtype == "bf16" else -60000.0
+    c = 3001
+    for r, spike in enumerate([100.0, 100.0, 60.0, 80.0, 88.5, 89.0, 120.0]):
+        x[0, r, c] += spike
+    x[0, 7, 5] += 100.0                  # in lane 0's first vector
+    x[0, 8, 0:8] = low                   # lane 0's first vector
+    x[0, 9, 0:256] = low                 # every lane's first vector
+    x[0, 10, :] -= 1000.0                # a uniform shift
+    x[0, 11, c] = low                    # one very low element
+    x = x.to(TDT[dtype])
+    t = wl.targets(w)
+    t[0, :12] = torch.arange(12) * 97 + 300  # away from the edited columns
+    xd, td = x.to(DEV), t.to(DEV)
+    assert pkg.ce_plan_path(xd)[0] == pkg.CE_PATH_WARP
+    ws = torch.empty(pkg.ce_workspace_bytes(1, N, V, xd.dtype), dtype=torch.uint8, device=DEV)
+    loss = pkg.ce_fwd_bwd(xd, td, label_smoothing=0.1, reduce_loss=False, workspace=ws)
+    assert pkg.ce_get_error(ws) == (0, 0)
+    _compare(w, x, t, loss, xd)
+
+
 @pytest.mark.parametrize("grad", [True, False])
 def test_row_counter_left_zeroed(grad):
     """The stream kernel hands out rows past each CTA's first two from a

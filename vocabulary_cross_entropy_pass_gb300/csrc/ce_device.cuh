@@ -241,6 +241,13 @@ struct Vec<__nv_bfloat16> {
         x[2] = make_float2(__uint_as_float(r.z << 16), __uint_as_float(r.z & 0xffff0000u));
         x[3] = make_float2(__uint_as_float(r.w << 16), __uint_as_float(r.w & 0xffff0000u));
     }
+    // one packed pair (4 bytes)
+    __device__ __forceinline__ static float2 unpack_pair(uint32_t u) {
+        return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+    }
+    __device__ __forceinline__ static uint32_t pack_pair(float2 g) {
+        return bf162_bits(__floats2bfloat162_rn(g.x, g.y));
+    }
     __device__ __forceinline__ static uint4 pack2(const float2* g) {
         return make_uint4(bf162_bits(__floats2bfloat162_rn(g[0].x, g[0].y)),
                           bf162_bits(__floats2bfloat162_rn(g[1].x, g[1].y)),
@@ -290,6 +297,8 @@ struct Vec<__half> {
         x[2] = __half22float2(as_h2(r.z));
         x[3] = __half22float2(as_h2(r.w));
     }
+    __device__ __forceinline__ static float2 unpack_pair(uint32_t u) { return __half22float2(as_h2(u)); }
+    __device__ __forceinline__ static uint32_t pack_pair(float2 g) { return h2_bits(__floats2half2_rn(g.x, g.y)); }
     __device__ __forceinline__ static uint4 pack2(const float2* g) {
         return make_uint4(h2_bits(__floats2half2_rn(g[0].x, g[0].y)), h2_bits(__floats2half2_rn(g[1].x, g[1].y)),
                           h2_bits(__floats2half2_rn(g[2].x, g[2].y)), h2_bits(__floats2half2_rn(g[3].x, g[3].y)));

@@ -220,8 +220,9 @@ struct Ring {
 // packed f32x2 arithmetic.  FULL: every vector valid.  e0: the row element of
 // the tile's first vector (weights only).  UNI: the running max is the
 // warp's (one redux per tile), so every lane's sums share it and the warp's
-// partial is two plain sums.
-template <typename T, int NC, int NV, bool FULL, bool WS, bool UNI = false>
+// partial is two plain sums.  SUM: accumulate the plain sum at all (the
+// weighted gradient pass takes the weighted sum in pass 2 instead).
+template <typename T, int NC, int NV, bool FULL, bool WS, bool UNI = false, bool SUM = true>
 __device__ __forceinline__ void stats_tile(const uint4* tile, int tid, int nvec, float& m,
                                            float2& d2, float2& s2, const float* cw, int64_t e0) {
     using VT = Vec<T>;
@@ -260,7 +261,7 @@ __device__ __forceinline__ void stats_tile(const uint4* tile, int tid, int nvec,
                 d2 = __fadd2_rn(d2, make_float2(ex2_approx(a.x), ex2_approx(a.y)));
                 if constexpr (WS)
                     s2 = __ffma2_rn(w[j], x[j], s2);
-                else
+                else if constexpr (SUM)
                     s2 = __fadd2_rn(s2, x[j]);
             }
         }
@@ -315,6 +316,43 @@ __device__ __forceinline__ void grad_tile(const uint4* tile, uint4* dst, int tid
                 o[j] = __ffma2_rn(make_float2(ex2_approx(a.x), ex2_approx(a.y)), G2, b);
             }
             stg128_stream(dst + tid + i * NC, VT::pack2(o));
+        }
+    }
+}
+
+// The weighted gradient pass of 16-bit logits, in 8-byte units u = tid + j NC
+// (four logits each, weights in slot j / NV at float4 tid + (j % NV) NC): a
+// warp's logits loads (8 bytes a lane) and weight loads (16 bytes a lane) are
+// both contiguous, so neither meets a shared-memory bank conflict (with 16-byte
+// logit vectors each lane's 32 bytes of weights are two 16-byte loads 32 bytes
+// apart across the warp: two-way conflicts).  Same arithmetic as grad_tile.
+template <typename T, int NC, int NV, bool FULL>
+__device__ __forceinline__ void grad_tile_w16(const unsigned char* tile, unsigned char* dst, int tid,
+                                              int nunit, float2 NL, float2 G2, float2 NB,
+                                              const unsigned char* const* wslot, float2& sw2) {
+    using VT = Vec<T>;
+    static_assert(sizeof(T) == 2, "8-byte units of 16-bit logits");
+    constexpr int NU = 2 * NV;
+    const float2 L2 = make_float2(kLog2e, kLog2e);
+    uint2 raw[NU];
+#pragma unroll
+    for (int j = 0; j < NU; ++j)
+        if (FULL || tid + j * NC < nunit) raw[j] = reinterpret_cast<const uint2*>(tile)[tid + j * NC];
+#pragma unroll
+    for (int j = 0; j < NU; ++j) {
+        if (FULL || tid + j * NC < nunit) {
+            const float4 f = reinterpret_cast<const float4*>(wslot[j / NV])[tid + (j % NV) * NC];
+            const float2 x[2] = {VT::unpack_pair(raw[j].x), VT::unpack_pair(raw[j].y)};
+            const float2 w[2] = {make_float2(f.x, f.y), make_float2(f.z, f.w)};
+            uint32_t o[2];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const float2 a = __ffma2_rn(x[k], L2, NL);
+                const float2 b = __fmul2_rn(w[k], NB);
+                sw2 = __ffma2_rn(w[k], x[k], sw2);
+                o[k] = VT::pack_pair(__ffma2_rn(make_float2(ex2_approx(a.x), ex2_approx(a.y)), G2, b));
+            }
+            __stcs(reinterpret_cast<uint2*>(dst) + tid + j * NC, make_uint2(o[0], o[1]));
         }
     }
 }
@@ -654,11 +692,12 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
             // the weighted sum comes with pass 2 when there is one; chunked
             // rows keep the warp's running max
             constexpr bool UNI = GEO == kGeoChunks;
+            constexpr bool SUM = !(WT && GRAD);
             if (bytes == (uint32_t)TB)
-                stats_tile<T, NC, NV, true, WT && !GRAD, UNI>(tile, tid, TV, m, d2, s2, p.cw, e0);
+                stats_tile<T, NC, NV, true, WT && !GRAD, UNI, SUM>(tile, tid, TV, m, d2, s2, p.cw, e0);
             else
-                stats_tile<T, NC, NV, false, WT && !GRAD, UNI>(tile, tid, (int)(bytes / 16), m, d2, s2,
-                                                               p.cw, e0);
+                stats_tile<T, NC, NV, false, WT && !GRAD, UNI, SUM>(tile, tid, (int)(bytes / 16), m, d2,
+                                                                    s2, p.cw, e0);
             release();
             if constexpr (GEO == kGeoChunks) {
                 // end of a chunk: the warp's partial of this chunk (its lanes
@@ -766,10 +805,18 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
                         wslot[h] = ring + (size_t)rg.s * TB;
                         rg.next();
                     }
-                    if (bytes == (uint32_t)TB)
+                    if constexpr (ES == 2) {
+                        const unsigned char* tb = ring + (size_t)st * TB;
+                        unsigned char* db = reinterpret_cast<unsigned char*>(dst);
+                        if (bytes == (uint32_t)TB)
+                            grad_tile_w16<T, NC, NV, true>(tb, db, tid, 2 * TV, NL, G2, NB, wslot, sw2);
+                        else
+                            grad_tile_w16<T, NC, NV, false>(tb, db, tid, (int)(bytes / 8), NL, G2, NB, wslot, sw2);
+                    } else if (bytes == (uint32_t)TB) {
                         grad_tile<T, NC, NV, true, true>(tile, dst, tid, TV, NL, G2, NB, wslot, sw2);
-                    else
+                    } else {
                         grad_tile<T, NC, NV, false, true>(tile, dst, tid, (int)(bytes / 16), NL, G2, NB, wslot, sw2);
+                    }
                     __syncwarp();
                     if (lane == 0) {
                         mbar_arrive(&empty[st]);
@@ -784,10 +831,12 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&empty[st]);
                 }
-                // the target element: the thread that stored its vector rewrites
-                // it with the one-hot term subtracted (same thread, so the second
-                // store lands after the first)
-                if (t == ty && tid == yv % NC) {
+                // the target element: the thread that stored its vector (its
+                // 8-byte unit in the weighted 16-bit pass) rewrites it with the
+                // one-hot term subtracted (same thread, so the second store
+                // lands after the first)
+                const int yown = (WT && ES == 2 && wring) ? (yoff / 8) % NC : yv % NC;
+                if (t == ty && tid == yown) {
                     const float e = ex2_approx(fmaf(xy, kLog2e, nll));
                     VT::store1(rowp + ybyte, fmaf(e, c, -bb * wy) - g * (1.f - p.a) * wy);
                 }
