@@ -6,6 +6,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import vocabulary_cross_entropy_pass_gb300 as pkg
 from tests import harness
 from vocabulary_cross_entropy_pass_gb300 import workloads as wl
@@ -69,3 +70,34 @@ def test_vocab_parallel_partials_combine_lse():
     assert np.all(np.isnan(lg[~ok]))
     assert np.max(np.abs(lg[ok] - ref["lse"][ok]) / np.abs(ref["lse"][ok])) <= 1e-5
     harness.check_loss(loss.cpu().numpy(), ref["loss"], "bf16")
+
+
+@pytest.mark.parametrize("dtype,V,cuts", [("bf16", 64000, [0, 20000, 40000, 64000]),
+                                          ("f16", 50000, [0, 8192, 50000]),
+                                          ("f32", 24003, [0, 4096, 12196, 24003]),
+                                          ("bf16", 30000, [0, 8191, 30000])])
+def test_vp_partials_against_oracle(dtype, V, cuts):
+    """Step 1 on shards on and off the 16-byte grid, of 16 KB and more and
+    less: each row's {m, d, S, x_y} against the oracle's partial of the same
+    columns (hyper-parallel #269 section 3.1), ignored rows {-inf, 0, 0, 0},
+    targets inside and outside each shard."""
+    w = wl.Workload("vp_part", 3, 101, V, dtype, sigma=2.0, ignore_frac=0.2, seed=V + len(cuts))
+    x = wl.logits(w)
+    t = wl.targets(w)
+    td = t.to(DEV)
+    xv = x.float().numpy().reshape(w.N, V).astype(np.float64)
+    tt = t.numpy().ravel()
+    for k0, k1 in zip(cuts[:-1], cuts[1:]):
+        part = pkg.ce_vp_partials(x[..., k0:k1].contiguous().to(DEV), td, k0).cpu().numpy()
+        part = part.reshape(w.N, 4).astype(np.float64)
+        for r in range(w.N):
+            m, d, S, xy = part[r]
+            if tt[r] == w.ignore_idx:
+                assert m == -np.inf and d == 0.0 and S == 0.0 and xy == 0.0, (k0, r)
+                continue
+            ref = oracle.chunk_partials(xv[r], k0, k1, tt[r])
+            assert m == ref[0], (k0, r)                            # max of stored values: exact
+            assert abs(d - ref[1]) <= 1e-5 * ref[1], (k0, r)
+            assert abs(S - ref[2]) <= 1e-5 * np.abs(xv[r, k0:k1]).sum() + 1e-6, (k0, r)
+            assert xy == ref[3], (k0, r)                           # the target logit, exact
+
