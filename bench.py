@@ -367,10 +367,10 @@ def run_ours(args, w, rank: int, world: int, dist) -> None:
         gw = torch.zeros(w.V, args.hidden, dtype=torch.float32, device=dev)
         lws = torch.empty(pkg._lib.load().ce_linear_workspace_bytes(
             w.N, args.hidden, w.V, 1, args.chunk_rows), dtype=torch.uint8, device=dev)
-        t1 = t.reshape(-1)
+        t_flat = t.reshape(-1)
 
         def step(o=opts):
-            pkg.ce_linear_fwd_bwd(hid, wmat, t1, label_smoothing=w.label_smoothing,
+            pkg.ce_linear_fwd_bwd(hid, wmat, t_flat, label_smoothing=w.label_smoothing,
                                   ignore_idx=w.ignore_idx, reduce_loss=w.reduce_loss,
                                   grad_hidden=gh, grad_weight=gw, chunk_rows=args.chunk_rows,
                                   loss_out=loss, workspace=lws)
