@@ -484,7 +484,8 @@ def run_ours(args, w, rank: int, world: int, dist) -> None:
                     "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                     "dtype": "bf16", "data": "synthetic",
                     "config": config_of(w, args) | {"mode": "linear", "hidden": args.hidden,
-                                                     "chunk_rows": args.chunk_rows},
+                                                     "chunk_rows": args.chunk_rows,
+                                                     "logits_gemm": args.linear_gemm},
                     "roofline": {"bound": "tensor", "kernel": "whole step (3 GEMMs + CE)",
                                  "achieved": ach, "peak": peak, "unit": "TFLOP/s",
                                  "frac": ach / peak, "traffic": None,
@@ -646,6 +647,8 @@ def main(argv=None) -> int:
                     default="fused")
     ap.add_argument("--hidden", type=int, default=4096)      # linear mode: H
     ap.add_argument("--chunk-rows", type=int, default=4096)  # linear mode: rows per chunk
+    # linear mode: "library" puts the logits GEMM on cuBLAS (GBCE_LINEAR_GEMM)
+    ap.add_argument("--linear-gemm", choices=["tcgen05", "library"], default="tcgen05")
     ap.add_argument("--vocab-shards", type=int, default=8)
     # planner overrides, for tuning sweeps (defaults: the planner's choice)
     ap.add_argument("--force-path", type=int, default=0)
@@ -672,6 +675,8 @@ def main(argv=None) -> int:
         N = args.rows or w.N
         w = w.with_(name=f"{w.name}_as_{N}x{V}", dim0=1, dim1=N, V=V, layout="bsv",
                     vocab_chunks=0)
+    if args.linear_gemm == "library":
+        os.environ["GBCE_LINEAR_GEMM"] = "library"
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":

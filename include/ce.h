@@ -293,6 +293,8 @@ ce_status ce_vp_bwd(const void* shard_logits, ce_dtype dtype, int64_t dim0, int6
  * otherwise a cuBLAS GEMM and this library's fused pass -- scaled with the
  * kept-row count of the whole batch; then grad_hidden = dlogits . weight and
  * grad_weight += dlogits^T . hidden (cuBLAS GEMMs, fp32 accumulation).
+ * GBCE_LINEAR_GEMM=library in the environment (read once, at the first
+ * call) takes the cuBLAS branch for every dtype and shape, for comparison.
  *   hidden       (N, H) row-major, dtype; weight (V, H) row-major, dtype.
  *   targets      int64 [N], contiguous.
  *   loss_out     one value (reduce_loss) or N values.

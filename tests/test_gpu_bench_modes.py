@@ -16,7 +16,9 @@ SMALL = ["--steps", "2", "--warmup", "3", "--no-cpu-baseline", "--no-torch-ref",
 
 @pytest.mark.parametrize("mode,extra", [("fused", []), ("split", []), ("vp", ["--vocab-shards", "4"]),
                                         ("weighted", []),
-                                        ("linear", ["--hidden", "256", "--chunk-rows", "256"])])
+                                        ("linear", ["--hidden", "256", "--chunk-rows", "256"]),
+                                        ("linear", ["--hidden", "256", "--chunk-rows", "256",
+                                                    "--linear-gemm", "library"])])
 def test_bench_mode_runs(mode, extra):
     out = subprocess.run([sys.executable, "bench.py", "--mode", mode, *SMALL, *extra], cwd=ROOT,
                          capture_output=True, text=True, timeout=600)

@@ -23,6 +23,7 @@
 // logit against a few bytes of logits traffic), so the chunk buffer's round
 // trip through memory costs little.
 #include <cublas_v2.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <mutex>
@@ -51,6 +52,17 @@ cublasHandle_t thread_handle(int dev) {
     if (dev < 0 || dev >= kLinMaxDevices) return nullptr;
     if (!handles[dev] && cublasCreate(&handles[dev]) != CUBLAS_STATUS_SUCCESS) handles[dev] = nullptr;
     return handles[dev];
+}
+
+// GBCE_LINEAR_GEMM=library in the environment (read once, at the first call)
+// puts the logits GEMM on cuBLAS even where this library's tcgen05 kernel
+// applies: the same step with the library GEMM, for comparison.
+bool library_gemm_asked() {
+    static const bool asked = [] {
+        const char* e = getenv("GBCE_LINEAR_GEMM");
+        return e != nullptr && strcmp(e, "library") == 0;
+    }();
+    return asked;
 }
 
 cudaDataType_t cuda_type(int dtype) {
@@ -143,7 +155,7 @@ ce_status ce_linear_fwd_bwd(const void* hidden, const void* weight, ce_dtype dty
     const bool grads = grad_hidden != nullptr || grad_weight != nullptr;
     // the tensor-core path: this library's GEMM with the statistics in its
     // epilogue; its chunk rows are padded to a multiple of 8 elements
-    const bool tc = lmhead_supported(dtype, H, V, hidden, weight);
+    const bool tc = !library_gemm_asked() && lmhead_supported(dtype, H, V, hidden, weight);
     const int64_t ld = tc ? lmhead_ldl(V) : V;
 
     for (int64_t r0 = 0; r0 < N; r0 += chunk_rows) {
