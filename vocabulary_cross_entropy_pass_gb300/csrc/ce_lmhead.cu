@@ -149,74 +149,110 @@ __host__ __device__ constexpr uint32_t idesc_f16() {
            ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
 }
 
-// Round to the storage dtype and back (the value the chunk buffer holds).
-template <typename T>
-__device__ __forceinline__ float round_store(float x);
-template <>
-__device__ __forceinline__ float round_store<__nv_bfloat16>(float x) {
-    return __bfloat162float(__float2bfloat16_rn(x));
-}
-template <>
-__device__ __forceinline__ float round_store<__half>(float x) {
-    return __half2float(__float2half_rn(x));
+// Orders the uses of 8 registers after the tcgen05.wait::ld before it: an
+// empty volatile statement that takes and gives back the registers, so the
+// compiler cannot move a use above the wait.
+__device__ __forceinline__ void reg_fence8(uint32_t* r) {
+    asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]));
 }
 
 // The epilogue's work on one accumulator row of this thread: the logits
-// (row, j0 .. j0 + 255) read from TMEM (tbase: this row's lane, column j0),
-// rounded to the storage dtype and stored (row < rows), and their statistics
-// {m, d, S, x_y} (x_y 0 when the target lies outside the tile).
+// (row, j0 .. j0 + 255) read from TMEM (tbase: this row's lane, column j0)
+// 32 columns at a time, the next 32 in flight while these are worked on;
+// rounded to the storage dtype in pairs and stored (row < rows); their
+// statistics {m, d, S} over the columns inside the vocabulary, from the
+// rounded values (what the chunk buffer holds), in packed f32x2 arithmetic.
+// The target logit is read back from the stored row by the per-row combine.
 template <typename T>
 __device__ __forceinline__ float4 epilogue_row(const LmArgs& p, uint32_t tbase, int64_t row,
                                                int64_t j0) {
+    using VT = Vec<T>;
     const bool live = row < p.rows;
-    const int64_t y = live ? __ldg(p.targets + row) : p.ignore_idx;
     T* out = reinterpret_cast<T*>(p.logits) + row * p.ldl;
-    float m = -INFINITY, d = 0.f, S = 0.f, xy = 0.f;
-#pragma unroll 1
+    const int nvt = (int)max((int64_t)0, min((int64_t)kBN, p.V - j0));  // columns inside V
+    const float2 L2 = make_float2(kLog2e, kLog2e);
+    float m = -INFINITY;
+    float2 d2 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
+    uint32_t v[2][32];
+    tmem_ld32(tbase, v[0]);
+#pragma unroll
     for (int c = 0; c < kBN / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tbase + (uint32_t)(c * 32), v);
+        uint32_t* u = v[c & 1];
         tmem_wait_ld();
-        const int64_t jc = j0 + c * 32;
-        const int nval = (int)max((int64_t)0, min((int64_t)32, p.V - jc));
-        float x[32];
-        float cm = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            x[i] = round_store<T>(__uint_as_float(v[i]));
-            if (i < nval) cm = fmaxf(cm, x[i]);
-        }
-        if (cm > m) {
-            if (m != -INFINITY) d *= ex2_approx((m - cm) * kLog2e);
-            m = cm;
-        }
-        const float nm = -m * kLog2e;
+        for (int g = 0; g < 4; ++g) reg_fence8(u + 8 * g);
+        if (c + 1 < kBN / 32) tmem_ld32(tbase + (uint32_t)((c + 1) * 32), v[(c + 1) & 1]);
+        // round to the storage type, two values at a time
+        uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            if (i < nval) {
-                d += ex2_approx(fmaf(x[i], kLog2e, nm));
-                S += x[i];
-            }
-            if (jc + i == y) xy = x[i];
-        }
-        if (live) {
-            if (nval == 32) {
-                uint4* o4 = reinterpret_cast<uint4*>(out + jc);
+        for (int e = 0; e < 16; ++e)
+            pk[e] = VT::pack_pair(make_float2(__uint_as_float(u[2 * e]), __uint_as_float(u[2 * e + 1])));
+        const int nval = min(32, max(0, nvt - c * 32));
+        if (nval == 32) {
+            typename VT::Max tm = VT::max_init();  // max on the packed pairs: exact
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    float2 pr[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) pr[e] = make_float2(x[8 * u + 2 * e], x[8 * u + 2 * e + 1]);
-                    o4[u] = Vec<T>::pack2(pr);
+            for (int q = 0; q < 4; ++q)
+                tm = VT::max_acc(tm, make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]));
+            const float cm = VT::max_done(tm);
+            if (cm > m) {
+                if (m != -INFINITY) {
+                    const float r = ex2_approx((m - cm) * kLog2e);
+                    d2.x *= r;
+                    d2.y *= r;
                 }
-            } else {
+                m = cm;
+            }
+            const float nm = -m * kLog2e;
+            const float2 NM = make_float2(nm, nm);
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (i < nval) Vec<T>::store1(out + jc + i, x[i]);
+            for (int e = 0; e < 16; ++e) {
+                const float2 x = VT::unpack_pair(pk[e]);
+                const float2 a = __ffma2_rn(x, L2, NM);
+                d2 = __fadd2_rn(d2, make_float2(ex2_approx(a.x), ex2_approx(a.y)));
+                s2 = __fadd2_rn(s2, x);
+            }
+            if (live) {
+                uint4* o4 = reinterpret_cast<uint4*>(out + j0 + c * 32);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    o4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            }
+        } else if (nval > 0) {
+            // the vocabulary ends inside these 32 columns (predicated,
+            // unrolled: the pairs stay in registers)
+            float cm = -INFINITY;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const float2 x = VT::unpack_pair(pk[e]);
+                if (2 * e < nval) cm = fmaxf(cm, x.x);
+                if (2 * e + 1 < nval) cm = fmaxf(cm, x.y);
+            }
+            if (cm > m) {
+                if (m != -INFINITY) {
+                    const float r = ex2_approx((m - cm) * kLog2e);
+                    d2.x *= r;
+                    d2.y *= r;
+                }
+                m = cm;
+            }
+            const float nm = -m * kLog2e;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const float2 x = VT::unpack_pair(pk[e]);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float xv = h ? x.y : x.x;
+                    if (2 * e + h < nval) {
+                        d2.x += ex2_approx(fmaf(xv, kLog2e, nm));
+                        s2.x += xv;
+                        if (live) VT::store1(out + j0 + c * 32 + 2 * e + h, xv);
+                    }
+                }
             }
         }
     }
-    return make_float4(m, d, S, xy);
+    return make_float4(m, d2.x + d2.y, s2.x + s2.y, 0.f);
 }
 
 // ------------------------------------------------------------ the GEMM + statistics kernel
@@ -593,9 +629,11 @@ ce_lmhead2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 
 // ------------------------------------------------------------ per-row combine of the tiles
 // One warp per row: lane l folds tiles l, l + 32, ... in order, then a fixed
-// butterfly; the target's tile gives x_y.
+// butterfly; x_y is the target's logit as the chunk buffer holds it.
+template <typename T>
 __global__ void __launch_bounds__(256) ce_lm_combine_kernel(const float4* __restrict__ part, int ntn,
                                                             int64_t rows, int64_t V,
+                                                            const T* __restrict__ logits, int64_t ldl,
                                                             const int64_t* __restrict__ targets,
                                                             int64_t ignore_idx, float a,
                                                             float* __restrict__ loss,
@@ -619,7 +657,7 @@ __global__ void __launch_bounds__(256) ce_lm_combine_kernel(const float4* __rest
     }
     G = warp_allreduce_part(G);
     if (lane == 0) {
-        const float xy = __ldg(pr + y / kBN).w;
+        const float xy = Vec<T>::load1(logits + row * ldl + y);
         const float l = G.m + logf(G.d);
         loss[row] = l - (1.f - a) * xy - (a / (float)V) * G.S;
         lse_out[row] = l;
@@ -720,9 +758,9 @@ cudaError_t launch_lmhead_typed(const LmHeadProblem& lp, cudaStream_t s) {
     }
     if (e != cudaSuccess) return e;
     const int rows_per_cta = 8;
-    ce_lm_combine_kernel<<<(unsigned)((lp.rows + rows_per_cta - 1) / rows_per_cta), 32 * rows_per_cta, 0,
-                           s>>>(lp.part, a.ntn, lp.rows, lp.V, lp.targets, lp.ignore_idx, lp.a,
-                                lp.loss_rows, lp.lse);
+    ce_lm_combine_kernel<T><<<(unsigned)((lp.rows + rows_per_cta - 1) / rows_per_cta), 32 * rows_per_cta,
+                              0, s>>>(lp.part, a.ntn, lp.rows, lp.V, static_cast<const T*>(lp.logits),
+                                      lp.ldl, lp.targets, lp.ignore_idx, lp.a, lp.loss_rows, lp.lse);
     return cudaGetLastError();
 }
 
