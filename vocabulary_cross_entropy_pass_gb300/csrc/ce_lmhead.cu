@@ -55,7 +55,10 @@ constexpr int kBBytes = kBN * kBK * 2;          // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;  // 48 KB
 constexpr int kLmThreads = 192;                 // 6 warps
 constexpr uint32_t kTmemCols = 2 * kBN;         // two fp32 accumulators
-constexpr size_t kLmSmem = (size_t)kStages * kStageBytes + 1024 /* alignment */ + 256;
+// Each epilogue warp stages 64 columns of its 32 rows (4 KB) in shared memory
+// to store them a row segment of 128 bytes at a time, after the barriers.
+constexpr int kStoreStageBytes = 4 * 4096;
+constexpr size_t kLmSmem = (size_t)kStages * kStageBytes + 1024 /* alignment */ + 256 + kStoreStageBytes;
 
 struct LmArgs {
     int64_t rows;             // rows of this chunk
@@ -160,16 +163,24 @@ __device__ __forceinline__ void reg_fence8(uint32_t* r) {
 // The epilogue's work on one accumulator row of this thread: the logits
 // (row, j0 .. j0 + 255) read from TMEM (tbase: this row's lane, column j0)
 // 32 columns at a time, the next 32 in flight while these are worked on;
-// rounded to the storage dtype in pairs and stored (row < rows); their
+// rounded to the storage dtype in pairs and stored (rows < p.rows); their
 // statistics {m, d, S} over the columns inside the vocabulary, from the
 // rounded values (what the chunk buffer holds), in packed f32x2 arithmetic.
 // The target logit is read back from the stored row by the per-row combine.
+// Stores: every 64 columns the warp's 32 rows x 128 bytes go through its 4 KB
+// of shared memory (`stage`; 16-byte units of row r at unit u ^ (r & 7), so
+// neither the writes by row nor the reads by row segment meet a bank
+// conflict) and out as four rows of 128 contiguous bytes per instruction,
+// instead of 32 rows of 16 bytes; where the vocabulary ends inside the 64
+// columns each lane stores its own row's elements.
 template <typename T>
 __device__ __forceinline__ float4 epilogue_row(const LmArgs& p, uint32_t tbase, int64_t row,
-                                               int64_t j0) {
+                                               int64_t j0, uint4* stage, int lane) {
     using VT = Vec<T>;
     const bool live = row < p.rows;
     T* out = reinterpret_cast<T*>(p.logits) + row * p.ldl;
+    const int64_t row0 = row - lane;  // the warp's first row
+    uint32_t pkp[16];                 // the previous (even) chunk, rounded
     const int nvt = (int)max((int64_t)0, min((int64_t)kBN, p.V - j0));  // columns inside V
     const float2 L2 = make_float2(kLog2e, kLog2e);
     float m = -INFINITY;
@@ -212,12 +223,6 @@ __device__ __forceinline__ float4 epilogue_row(const LmArgs& p, uint32_t tbase, 
                 d2 = __fadd2_rn(d2, make_float2(ex2_approx(a.x), ex2_approx(a.y)));
                 s2 = __fadd2_rn(s2, x);
             }
-            if (live) {
-                uint4* o4 = reinterpret_cast<uint4*>(out + j0 + c * 32);
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    o4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-            }
         } else if (nval > 0) {
             // the vocabulary ends inside these 32 columns (predicated,
             // unrolled: the pairs stay in registers)
@@ -250,6 +255,34 @@ __device__ __forceinline__ float4 epilogue_row(const LmArgs& p, uint32_t tbase, 
                     }
                 }
             }
+        }
+        if ((c & 1) == 0) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) pkp[e] = pk[e];
+        } else if (nvt - (c - 1) * 32 >= 64) {
+            // chunks c-1 and c, whole: through the warp's stage (nvt is the
+            // same for every lane, so the whole warp takes this branch)
+            __syncwarp();  // the previous pair's reads are done
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const uint32_t* w = u < 4 ? pkp + 4 * u : pk + 4 * (u - 4);
+                stage[lane * 8 + (u ^ (lane & 7))] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            __syncwarp();
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                const int R = 4 * jj + (lane >> 3), k = lane & 7;
+                const uint4 w = stage[R * 8 + (k ^ (R & 7))];
+                if (row0 + R < p.rows)
+                    *reinterpret_cast<uint4*>(reinterpret_cast<T*>(p.logits) + (row0 + R) * p.ldl + j0 +
+                                              (c - 1) * 32 + k * 8) = w;
+            }
+        } else if (live && nvt - (c - 1) * 32 >= 32) {
+            // the vocabulary ends inside chunk c: chunk c-1 is whole, stored
+            // by this lane (chunk c's elements went out above)
+            uint4* o4 = reinterpret_cast<uint4*>(out + j0 + (c - 1) * 32);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) o4[q] = make_uint4(pkp[4 * q], pkp[4 * q + 1], pkp[4 * q + 2], pkp[4 * q + 3]);
         }
     }
     return make_float4(m, d2.x + d2.y, s2.x + s2.y, 0.f);
@@ -380,7 +413,8 @@ ce_lmhead_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         }
     } else {
         // ---------------------------------------------------- epilogue
-        const int q = warp & 3;            // this warp's quarter of the TMEM lanes
+        const int q = warp & 3;
+        uint4* stage = reinterpret_cast<uint4*>(sm + (size_t)kStages * kStageBytes + 256) + q * 256;            // this warp's quarter of the TMEM lanes
         const int rin = q * 32 + lane;     // row within the tile
         int it = 0;
         for (int t = blockIdx.x; t < ntiles && !*abort_flag; t += gridDim.x, ++it) {
@@ -393,8 +427,8 @@ ce_lmhead_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             }
             tc_fence_after();
             const int64_t row = (int64_t)mblk * kBM + rin;
-            const float4 pt = epilogue_row<T>(
-                p, tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * kBN), row, (int64_t)nblk * kBN);
+            const float4 pt = epilogue_row<T>(p, tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * kBN),
+                                              row, (int64_t)nblk * kBN, stage, lane);
             // every read of accumulator b is done: hand it back to the MMA warp
             tc_fence_before();
             __syncwarp();
@@ -423,13 +457,14 @@ ce_lmhead_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 // finished accumulator to the barriers of both CTAs at once; each CTA's TMEM
 // holds its 128 rows of the accumulator, read by its own epilogue warps, which
 // report back to the leader.  Per SM: 32 KB of operands per 512 tensor-core
-// clocks instead of 48 KB, in a 7-deep ring (225 KB of shared memory; the
-// whole lm_head step at N 16384, H 4096, V 128000 measured 1 % faster than
-// with 6 stages and 5 stages on the same GPU).
-constexpr int kStages2 = 7;
+// clocks instead of 48 KB, in a 6-deep ring (192 KB), beside the epilogue
+// warps' 16 KB store stage (with the logits stored straight from registers,
+// 32 rows of 16 bytes per instruction, a 7-deep ring had measured 1 % faster
+// than 6 on the whole lm_head step).
+constexpr int kStages2 = 6;
 constexpr int kHalfBytes = 128 * kBK * 2;     // 16 KB: 128 rows x 64 16-bit values
 constexpr int kStage2Bytes = 2 * kHalfBytes;  // per CTA: its hidden half + its W half
-constexpr size_t kLmSmem2 = (size_t)kStages2 * kStage2Bytes + 1024 + 256;
+constexpr size_t kLmSmem2 = (size_t)kStages2 * kStage2Bytes + 1024 + 256 + kStoreStageBytes;
 
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* tm, int x, int y,
                                                  uint32_t bar_cluster) {
@@ -592,6 +627,7 @@ ce_lmhead2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     } else {
         // ---------------------------------------------------- epilogue (both CTAs)
         const int q = warp & 3;
+        uint4* stage = reinterpret_cast<uint4*>(sm + (size_t)kStages2 * kStage2Bytes + 256) + q * 256;
         int it = 0;
         for (int t = pair; t < ntiles && !*abort_flag; t += npairs, ++it) {
             const int b = it & 1;
@@ -603,8 +639,8 @@ ce_lmhead2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             }
             tc_fence_after();
             const int64_t row = (int64_t)mblk * 256 + rank * 128 + q * 32 + lane;
-            const float4 pt = epilogue_row<T>(
-                p, tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * kBN), row, (int64_t)nblk * kBN);
+            const float4 pt = epilogue_row<T>(p, tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * kBN),
+                                              row, (int64_t)nblk * kBN, stage, lane);
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
