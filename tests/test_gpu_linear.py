@@ -37,6 +37,10 @@ TDT = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
     (300, 256, 4001, "bf16", 300, 0.0, False),    # odd vocabulary: padded logits rows
     (260, 320, 5000, "f16", 130, 0.1, False),     # 5 K steps, the last half out of range
     (200, 100, 3000, "bf16", 100, 0.1, True),     # hidden size off 8: the cuBLAS path
+    # one-CTA kernel (64-row chunks), 2 K steps of which the second is mostly
+    # out of range, a last vocabulary tile of one column
+    (64, 72, 4097, "bf16", 64, 0.1, True),
+    (300, 128, 200, "f16", 300, 0.0, False),      # paired kernel, the vocabulary inside one tile
 ])
 def test_linear_ce_matches_oracle(N, H, V, dtype, chunk, a, red):
     rng = np.random.default_rng(N + V)
