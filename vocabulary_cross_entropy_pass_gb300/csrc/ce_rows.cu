@@ -213,7 +213,7 @@ ce_rows_kernel(const __grid_constant__ RowsArgs p) {
         typename VT::Max pm = VT::max_init();
 #pragma unroll 4
         for (int v = lane; v < nvec; v += 32) pm = VT::max_acc(pm, tile[v]);
-        const float m = warp_allmax(VT::max_done(pm));
+        const float m = warp_max_redux(VT::max_done(pm));
         const float nml = -m * kLog2e;
         const float2 NM = make_float2(nml, nml);
 
