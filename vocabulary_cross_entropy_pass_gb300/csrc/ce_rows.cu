@@ -45,6 +45,7 @@ struct RowsArgs {
     uint32_t* err;
     uint32_t* ticket;      // CTAs done (zeroed by the count kernel)
     float* mean_out;       // reduce_loss: the last CTA to finish writes the mean here
+    int flat;              // row r at r * s1, its target at r * ts1
 };
 
 __device__ __forceinline__ void mbar_arrive_rows(uint64_t* bar) {
@@ -87,10 +88,12 @@ ce_rows_kernel(const __grid_constant__ RowsArgs p) {
     __syncthreads();
 
     auto row_target = [&](int64_t r) -> int64_t {
+        if (p.flat) return __ldg(p.targets + r * p.ts1);
         const int64_t i = r / p.dim1, j = r - (r / p.dim1) * p.dim1;
         return __ldg(p.targets + i * p.ts0 + j * p.ts1);
     };
     auto row_ptr = [&](int64_t r) -> char* {
+        if (p.flat) return p.logits + r * p.s1 * ES;
         const int64_t i = r / p.dim1, j = r - (r / p.dim1) * p.dim1;
         return p.logits + (i * p.s0 + j * p.s1) * ES;
     };
@@ -323,6 +326,7 @@ cudaError_t launch_rows_one(const Problem& pb, const RowsPlan& plan, cudaStream_
     a.err = pb.err;
     a.ticket = pb.ticket;
     a.mean_out = pb.mean_out;
+    a.flat = rows_flat(pb) ? 1 : 0;
     const size_t smem = (size_t)plan.stages * TB + 32 * sizeof(uint64_t) + NW * sizeof(double) +
                         2 * sizeof(int) + 16;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -110,6 +110,7 @@ struct StreamArgs {
     int32_t tpc;
     int32_t nchunks;
     float4* part;
+    int flat;              // row r at r * s1, its target at r * ts1
 };
 
 // The part of a row that goes through the ring: `body` (16-byte aligned),
@@ -405,10 +406,12 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
     __syncthreads();
 
     auto row_target = [&](int64_t r) -> int64_t {
+        if (p.flat) return __ldg(p.targets + r * p.ts1);
         const int64_t i = r / p.dim1, j = r - (r / p.dim1) * p.dim1;
         return __ldg(p.targets + i * p.ts0 + j * p.ts1);
     };
     auto row_ptr = [&](int64_t r) -> char* {
+        if (p.flat) return p.logits + r * p.s1 * ES;
         const int64_t i = r / p.dim1, j = r - (r / p.dim1) * p.dim1;
         return p.logits + (i * p.s0 + j * p.s1) * ES;
     };
@@ -959,6 +962,7 @@ cudaError_t launch_stream_one(const Problem& pb, const StreamPlan& plan, float4*
     // rows handed out by a shared counter while row indices fit it
     a.row_claim = pb.N < (int64_t)0x7fffffff ? pb.row_claim : nullptr;
     a.row_done = pb.row_done;
+    a.flat = rows_flat(pb) ? 1 : 0;
     const size_t smem = (size_t)plan.stages * a.tile_bytes + (24 + 4 * kRowQ) * sizeof(uint64_t) +
                         2 * KS * NW * sizeof(float4) + (2 + 2 * NW) * sizeof(float) + 2 * sizeof(int) +
                         16;
