@@ -60,6 +60,7 @@ struct VecRowArgs {
     float* loss;       // per-row losses
     float* lse_out;    // optional
     const int64_t* n_dev;
+    int flat;          // row r at r * s1, its target at r * ts1
 };
 
 // Pass 1's 16-byte load, with an L2 evict-last policy: the row's second pass
@@ -100,9 +101,16 @@ __global__ void __launch_bounds__(THREADS, VrShape<THREADS>::kCtasPerSm)
     const int64_t r0 = WARPROW ? (int64_t)blockIdx.x * kVrWarps + warp : (int64_t)blockIdx.x;
     const int64_t rstep = WARPROW ? (int64_t)gridDim.x * kVrWarps : (int64_t)gridDim.x;
     for (int64_t r = r0; r < p.N; r += rstep) {
-        const int64_t i = r / p.dim1, j = r - i * p.dim1;
-        const int64_t y = __ldg(p.targets + i * p.ts0 + j * p.ts1);
-        char* row = p.logits + (i * p.s0 + j * p.s1) * (int64_t)ES;
+        int64_t y;
+        char* row;
+        if (p.flat) {
+            y = __ldg(p.targets + r * p.ts1);
+            row = p.logits + r * p.s1 * (int64_t)ES;
+        } else {
+            const int64_t i = r / p.dim1, j = r - i * p.dim1;
+            y = __ldg(p.targets + i * p.ts0 + j * p.ts1);
+            row = p.logits + (i * p.s0 + j * p.s1) * (int64_t)ES;
+        }
         const Span16 sp = span16<ES>(row, 0, p.V);
         const int64_t ee = span16_edge(sp, 0, p.V, tid);
         uint4* rv = reinterpret_cast<uint4*>(row + sp.h1 * ES);
@@ -288,6 +296,7 @@ cudaError_t launch_vecrow_typed(const Problem& pb, const VecRowPlan& plan, cudaS
     a.loss = pb.loss_rows;
     a.lse_out = pb.lse_out;
     a.n_dev = pb.n_dev;
+    a.flat = rows_flat(pb) ? 1 : 0;
     if (plan.warp_rows) return launch_vecrow_shaped<T, 512, true>(a, pb, plan.ctas_per_sm_cap, s);
     if (plan.threads == 256) return launch_vecrow_shaped<T, 256, false>(a, pb, plan.ctas_per_sm_cap, s);
     if (plan.threads == 1024) return launch_vecrow_shaped<T, 1024, false>(a, pb, plan.ctas_per_sm_cap, s);

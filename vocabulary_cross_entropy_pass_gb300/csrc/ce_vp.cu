@@ -33,6 +33,7 @@ struct VpPartArgs {
     const int64_t* targets;
     int64_t ts0, ts1, ignore_idx;
     float4* part;                      // [N]
+    int flat;                          // row r at r * s1, its target at r * ts1
 };
 
 // One CTA per row: a running (max, sum-exp, sum) per thread over 16-byte
@@ -54,13 +55,20 @@ __global__ void __launch_bounds__(kVpThreads, 6) ce_vp_partials_kernel(const __g
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const float2 L2 = make_float2(kLog2e, kLog2e);
     for (int64_t r = blockIdx.x; r < p.N; r += gridDim.x) {
-        const int64_t i = r / p.dim1, j = r - i * p.dim1;
-        const int64_t y = __ldg(p.targets + i * p.ts0 + j * p.ts1);
+        int64_t y;
+        const char* row;
+        if (p.flat) {
+            y = __ldg(p.targets + r * p.ts1);
+            row = p.logits + r * p.s1 * ES;
+        } else {
+            const int64_t i = r / p.dim1, j = r - i * p.dim1;
+            y = __ldg(p.targets + i * p.ts0 + j * p.ts1);
+            row = p.logits + (i * p.s0 + j * p.s1) * ES;
+        }
         if (y == p.ignore_idx) {
             if (threadIdx.x == 0) p.part[r] = make_float4(-INFINITY, 0.f, 0.f, 0.f);
             continue;
         }
-        const char* row = p.logits + (i * p.s0 + j * p.s1) * ES;
         float m = -INFINITY;
         float2 d2 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
         // head and tail (rows off a 16-byte boundary) one element per thread
@@ -188,6 +196,13 @@ cudaError_t launch_vp_partials(const VpPartProblem& vp, cudaStream_t s) {
     a.ts1 = vp.ts1;
     a.ignore_idx = vp.ignore_idx;
     a.part = vp.part;
+    {
+        const int64_t lim = (int64_t)1 << 31;
+        a.flat = (vp.dim1 >= 1 && vp.dim1 < lim && vp.s1 >= 0 && vp.s1 < lim && vp.ts1 >= 0 && vp.ts1 < lim &&
+                  vp.s0 == vp.dim1 * vp.s1 && vp.ts0 == vp.dim1 * vp.ts1)
+                     ? 1
+                     : 0;
+    }
     switch (vp.dtype) {
         case CE_F32:
             return launch_vp_partials_typed<float>(a, s);
