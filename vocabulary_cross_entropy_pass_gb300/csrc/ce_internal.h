@@ -59,12 +59,12 @@ struct Problem {
 
 // Rows and targets laid out so that flattened row r sits at r * s1 and its
 // target at r * ts1 (s0 = dim1 * s1, ts0 = dim1 * ts1: every contiguous
-// (B,SQ,V) or (SQ,B,V) tensor): the kernels then skip the 64-bit division
-// r / dim1 per row.
+// (B,SQ,V) or (SQ,B,V) tensor; or dim0 = 1, where r = j): the kernels then
+// skip the 64-bit division r / dim1 per row.
 inline bool rows_flat(const Problem& p) {
     const int64_t lim = (int64_t)1 << 31;
     if (p.dim1 < 1 || p.dim1 >= lim || p.s1 < 0 || p.s1 >= lim || p.ts1 < 0 || p.ts1 >= lim) return false;
-    return p.s0 == p.dim1 * p.s1 && p.ts0 == p.dim1 * p.ts1;
+    return p.dim0 == 1 || (p.s0 == p.dim1 * p.s1 && p.ts0 == p.dim1 * p.ts1);
 }
 
 // Plan of the fused (row / cluster) kernel.
