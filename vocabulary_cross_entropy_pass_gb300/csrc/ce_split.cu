@@ -53,6 +53,26 @@ __device__ __forceinline__ void row_of(const SplitArgs& p, int64_t r, int64_t& y
     off = i * p.s0 + j * p.s1;
 }
 
+// The class weights of one 16-byte vector of logits (VEC of them, from
+// base): 16-byte loads when base sits on the 16-byte grid (it stays there from
+// vector to vector: VEC * 4 bytes apart), one float at a time otherwise.
+template <int VEC>
+__device__ __forceinline__ void weights_of(const float* base, bool vec16, float (&w)[VEC]) {
+    if (vec16) {
+#pragma unroll
+        for (int k = 0; k < VEC / 4; ++k) {
+            const float4 f = __ldg(reinterpret_cast<const float4*>(base) + k);
+            w[4 * k] = f.x;
+            w[4 * k + 1] = f.y;
+            w[4 * k + 2] = f.z;
+            w[4 * k + 3] = f.w;
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) w[e] = __ldg(base + e);
+    }
+}
+
 // Stage 1.  WT: the class-weighted pass, whose third statistic is
 // sum_j w_j x_j.  The chunk's elements outside whole 16-byte vectors (a row
 // that starts off a 16-byte boundary, a ragged chunk end) go one per thread;
@@ -125,6 +145,7 @@ __global__ void __launch_bounds__(kSplitThreads) ce_split_stats_kernel(const __g
     }
     const uint4* rv = reinterpret_cast<const uint4*>(row + sp.h1 * ES);
     const float* cwb = WT ? p.cw + sp.h1 : nullptr;
+    const bool wvec = WT && reinterpret_cast<uintptr_t>(cwb) % 16 == 0;
     for (int64_t vb = threadIdx.x; vb < sp.nv; vb += kSplitThreads * kSplitBatch) {
         uint4 raw[kSplitBatch];
         float vm = -INFINITY;
@@ -145,12 +166,13 @@ __global__ void __launch_bounds__(kSplitThreads) ce_split_stats_kernel(const __g
         for (int u = 0; u < kSplitBatch; ++u) {
             const int64_t v = vb + (int64_t)u * kSplitThreads;
             if (v < sp.nv) {
-                float x[VEC];
+                float x[VEC], w[VEC];
                 VT::unpack(raw[u], x);
+                if (WT) weights_of<VEC>(cwb + v * VEC, wvec, w);
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) {
                     d += ex2_approx(fmaf(x[e], kLog2e, nml));
-                    S = WT ? fmaf(__ldg(cwb + v * VEC + e), x[e], S) : S + x[e];
+                    S = WT ? fmaf(w[e], x[e], S) : S + x[e];
                 }
             }
         }
@@ -299,6 +321,7 @@ __global__ void __launch_bounds__(kSplitThreads) ce_split_grad_kernel(const __gr
     const float2 L2 = make_float2(kLog2e, kLog2e), NL = make_float2(nll, nll);
     const float2 C2 = make_float2(c, c), NB = make_float2(-ga, -ga);
     const float* cwb = WT ? p.cw + sp.h1 : nullptr;
+    const bool wvec = WT && reinterpret_cast<uintptr_t>(cwb) % 16 == 0;
     const int64_t yb = y - sp.h1;  // the target's place in the body
     for (int64_t vb = threadIdx.x; vb < sp.nv; vb += kSplitThreads * kSplitBatch) {
         uint4 raw[kSplitBatch];
@@ -312,14 +335,15 @@ __global__ void __launch_bounds__(kSplitThreads) ce_split_grad_kernel(const __gr
             const int64_t v = vb + (int64_t)u * kSplitThreads;
             if (v >= sp.nv) continue;
             float2 x[PP], o[PP];
+            float w[VEC];
             VT::unpack2(raw[u], x);
+            if (WT) weights_of<VEC>(cwb + v * VEC, wvec, w);
 #pragma unroll
             for (int q = 0; q < PP; ++q) {
                 const float2 e = __ffma2_rn(x[q], L2, NL);
                 const float2 pe = make_float2(ex2_approx(e.x), ex2_approx(e.y));
                 if (WT) {
-                    const float w0 = __ldg(cwb + v * VEC + 2 * q), w1 = __ldg(cwb + v * VEC + 2 * q + 1);
-                    o[q] = __ffma2_rn(pe, C2, make_float2(-ga * w0, -ga * w1));
+                    o[q] = __ffma2_rn(pe, C2, make_float2(-ga * w[2 * q], -ga * w[2 * q + 1]));
                 } else {
                     o[q] = __ffma2_rn(pe, C2, NB);
                 }
