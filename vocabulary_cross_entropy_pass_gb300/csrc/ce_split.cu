@@ -83,6 +83,7 @@ __device__ __forceinline__ void weights_of(const float* base, bool vec16, float 
 // The weighted pass always takes the head/tail form.
 template <typename T, bool WT, bool VECOK>
 __global__ void __launch_bounds__(kSplitThreads) ce_split_stats_kernel(const __grid_constant__ SplitArgs p) {
+    static_assert(!(WT && VECOK), "the weighted pass takes the head/tail form");
     using VT = Vec<T>;
     constexpr int VEC = VT::kElems;
     constexpr int ES = sizeof(T);
@@ -128,7 +129,7 @@ __global__ void __launch_bounds__(kSplitThreads) ce_split_stats_kernel(const __g
 #pragma unroll
                     for (int e = 0; e < VEC; ++e) {
                         d += ex2_approx(fmaf(x[e], kLog2e, nml));
-                        S = WT ? fmaf(__ldg(p.cw + v * VEC + e), x[e], S) : S + x[e];
+                        S += x[e];
                     }
                 }
             }
@@ -196,6 +197,7 @@ __global__ void __launch_bounds__(kSplitThreads) ce_split_stats_kernel(const __g
 // body in 16-byte vectors, as in stage 1).
 template <typename T, bool GRAD, bool WT, bool VECOK>
 __global__ void __launch_bounds__(kSplitThreads) ce_split_grad_kernel(const __grid_constant__ SplitArgs p) {
+    static_assert(!(WT && VECOK), "the weighted pass takes the head/tail form");
     using VT = Vec<T>;
     constexpr int VEC = VT::kElems;
     constexpr int ES = sizeof(T);
@@ -291,12 +293,7 @@ __global__ void __launch_bounds__(kSplitThreads) ce_split_grad_kernel(const __gr
                 for (int q = 0; q < PP; ++q) {
                     const float2 e = __ffma2_rn(x[q], L2, NL);
                     const float2 pe = make_float2(ex2_approx(e.x), ex2_approx(e.y));
-                    if (WT) {
-                        const float w0 = __ldg(p.cw + v * VEC + 2 * q), w1 = __ldg(p.cw + v * VEC + 2 * q + 1);
-                        o[q] = __ffma2_rn(pe, C2, make_float2(-ga * w0, -ga * w1));
-                    } else {
-                        o[q] = __ffma2_rn(pe, C2, NB);
-                    }
+                    o[q] = __ffma2_rn(pe, C2, NB);
                 }
                 if (v == y / VEC) {
                     const int ey = (int)(y % VEC);
