@@ -39,14 +39,16 @@ struct VpPartArgs {
 // One CTA per row: a running (max, sum-exp, sum) per thread over 16-byte
 // vectors, kVpBatch loads in flight per thread (one rescale per batch whose
 // max is new), then the CTA combine.
-constexpr int kVpBatch = 4;
+constexpr int kVpBatch = 8;
 
 template <typename T>
-// Six CTAs per SM (<= 42 registers): at the unbounded 54 registers only four
-// fit, too few loads in flight (ncu: long-scoreboard stalls 5.65 per issue,
-// 52 % DRAM throughput); 8 shards of the bench workload: 2.054 ms per step
-// against 2.134 ms (eight CTAs per SM spill and measured 2.181 ms).
-__global__ void __launch_bounds__(kVpThreads, 6) ce_vp_partials_kernel(const __grid_constant__ VpPartArgs p) {
+// Eight loads in flight per thread at four CTAs per SM (64 registers, no
+// spills): 128 KB of loads in flight per SM.  Four loads at six CTAs per SM
+// (96 KB; 40 registers, small spills) measured 2.010 / 1.876 ms for 8 / 2
+// shards of the bench workload against 2.004 / 1.852 ms, six loads at five
+// CTAs per SM (spills) 2.089 ms for 8 shards; four loads at the unbounded 54
+// registers (four CTAs per SM, 64 KB in flight) had measured 2.134 ms.
+__global__ void __launch_bounds__(kVpThreads, 4) ce_vp_partials_kernel(const __grid_constant__ VpPartArgs p) {
     using VT = Vec<T>;
     constexpr int VEC = VT::kElems;
     constexpr int ES = sizeof(T);
