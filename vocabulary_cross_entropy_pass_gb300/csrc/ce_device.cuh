@@ -369,12 +369,34 @@ __device__ __forceinline__ float warp_allsum(float v) {
     return v;
 }
 
-// Sum in double of x[t], x[t + T], x[t + 2T], ... in that order (t: this
-// thread's index among T threads), eight loads in flight at a time: the first
-// level of the fixed-order mean, the same on every run.
+// The first level of the fixed-order mean, the same on every run: this
+// thread's share of x[0 .. n) summed in double in a fixed order (t: the
+// thread's index among T threads), eight loads in flight at a time.  On a
+// 16-byte aligned x the thread takes 4-float groups t, t + T, ... (each group
+// added in float, (x0 + x1) + (x2 + x3), then to the double sum: a quarter of
+// the double adds, which this GPU issues slowly, and a quarter of the loads),
+// and threads t < n % 4 one element each of the last n % 4; otherwise single
+// elements t, t + T, ....
 __device__ __forceinline__ double strided_sum_fixed(const float* x, int64_t n, int t, int T) {
     constexpr int B = 8;
     double acc = 0.0;
+    if (reinterpret_cast<uintptr_t>(x) % 16 == 0) {
+        const float4* x4 = reinterpret_cast<const float4*>(x);
+        const int64_t n4 = n / 4;
+        for (int64_t q0 = t; q0 < n4; q0 += (int64_t)T * B) {
+            float4 v[B];
+#pragma unroll
+            for (int u = 0; u < B; ++u) {
+                const int64_t q = q0 + (int64_t)u * T;
+                v[u] = q < n4 ? __ldcg(x4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < B; ++u)
+                if (q0 + (int64_t)u * T < n4) acc += (double)((v[u].x + v[u].y) + (v[u].z + v[u].w));
+        }
+        if (t < (int)(n - n4 * 4)) acc += (double)__ldcg(x + n4 * 4 + t);
+        return acc;
+    }
     for (int64_t r0 = t; r0 < n; r0 += (int64_t)T * B) {
         float v[B];
 #pragma unroll
