@@ -372,11 +372,13 @@ __device__ __forceinline__ float warp_allsum(float v) {
 // The first level of the fixed-order mean, the same on every run: this
 // thread's share of x[0 .. n) summed in double in a fixed order (t: the
 // thread's index among T threads), eight loads in flight at a time.  On a
-// 16-byte aligned x the thread takes 4-float groups t, t + T, ... (each group
-// added in float, (x0 + x1) + (x2 + x3), then to the double sum: a quarter of
-// the double adds, which this GPU issues slowly, and a quarter of the loads),
-// and threads t < n % 4 one element each of the last n % 4; otherwise single
-// elements t, t + T, ....
+// 16-byte aligned x the thread takes 4-float groups t, t + T, ..., eight at a
+// time, and adds the eight groups in float as a fixed tree -- each group
+// (x0 + x1) + (x2 + x3), then the groups pairwise -- before one double add
+// (a 32nd of the double adds, which this GPU issues slowly, and a quarter of
+// the loads; the float tree's error, a few units in 2^-24 of its 32 values,
+// stays far below the mean's tolerance); threads t < n % 4 take one element
+// each of the last n % 4.  Otherwise single elements t, t + T, ....
 __device__ __forceinline__ double strided_sum_fixed(const float* x, int64_t n, int t, int T) {
     constexpr int B = 8;
     double acc = 0.0;
@@ -390,9 +392,10 @@ __device__ __forceinline__ double strided_sum_fixed(const float* x, int64_t n, i
                 const int64_t q = q0 + (int64_t)u * T;
                 v[u] = q < n4 ? __ldcg(x4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
+            float f[B];
 #pragma unroll
-            for (int u = 0; u < B; ++u)
-                if (q0 + (int64_t)u * T < n4) acc += (double)((v[u].x + v[u].y) + (v[u].z + v[u].w));
+            for (int u = 0; u < B; ++u) f[u] = (v[u].x + v[u].y) + (v[u].z + v[u].w);  // 0 past n4
+            acc += (double)(((f[0] + f[1]) + (f[2] + f[3])) + ((f[4] + f[5]) + (f[6] + f[7])));
         }
         if (t < (int)(n - n4 * 4)) acc += (double)__ldcg(x + n4 * 4 + t);
         return acc;
