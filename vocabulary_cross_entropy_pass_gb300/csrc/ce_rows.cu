@@ -182,9 +182,19 @@ ce_rows_kernel(const __grid_constant__ RowsArgs p) {
     }
 
     // ------------------------------------------------------------ consumer warps
-    griddep_wait();  // n and the error word come from the count kernel
+    // n and the error word come from the count kernel, which may still run:
+    // a warp waits for it (griddepcontrol.wait) only where it first needs
+    // them -- its first gradient sweep, an error to record, or the mean --
+    // so its first row's statistics overlap the count
+    bool counted = false;
     float g_reduce = 1.f;
-    if (p.reduce) g_reduce = (p.dloss ? __ldg(p.dloss) : 1.f) / (float)(*p.n_dev);
+    auto need_count = [&]() {
+        if (!counted) {
+            griddep_wait();
+            if (p.reduce) g_reduce = (p.dloss ? __ldg(p.dloss) : 1.f) / (float)(*p.n_dev);
+            counted = true;
+        }
+    };
     uint32_t k = 0;  // kept rows seen by the whole CTA
     const float2 L2 = make_float2(kLog2e, kLog2e);
     for (int64_t q0 = 0;; q0 += 32) {
@@ -206,11 +216,11 @@ ce_rows_kernel(const __grid_constant__ RowsArgs p) {
         const int s = warp * tpw + (int)(j % (uint32_t)tpw);
         const uint32_t ph = (j / (uint32_t)tpw) & 1u;
         if (!flags[0] && !mbar_wait_bounded(&full[s], ph)) {
+            need_count();  // the count kernel starts the error word
             atomicOr(p.err, CE_DEVERR_TIMEOUT);
             flags[0] = 1;
         }
         const uint4* tile = reinterpret_cast<const uint4*>(ring + (size_t)s * TB);
-        const float g = p.reduce ? g_reduce : (p.dloss ? __ldg(p.dloss + r) : 1.f);
 
         // sweep 1: row max (packed pairs), warp-wide
         typename VT::Max pm = VT::max_init();
@@ -244,6 +254,8 @@ ce_rows_kernel(const __grid_constant__ RowsArgs p) {
 
         // sweep 3: gradient over the row, stored in place
         if (GRAD) {
+            need_count();
+            const float g = p.reduce ? g_reduce : (p.dloss ? __ldg(p.dloss + r) : 1.f);
             char* rowp = row_ptr(r);
             const float nll = -lse * kLog2e;
             const float bb = g * p.a_over_v;
@@ -274,6 +286,7 @@ ce_rows_kernel(const __grid_constant__ RowsArgs p) {
     }
 
     // reduce_loss: the last CTA to finish sums the per-row losses in a fixed order
+    need_count();  // the mean divides by n; a warp with no gradient sweep has not waited yet
     if (p.mean_out) {
         // wait for the producer warp's loss writes, then take the ticket
         __threadfence();
