@@ -340,18 +340,27 @@ ce_status ce_linear_fwd_bwd(const void* hidden, const void* weight, ce_dtype dty
  * array and it keeps the last call's contents, so calls that may overlap on
  * the GPU (different streams, or threads enqueuing at once) race on it:
  * serialise them.  The error word lives in that internal scratch, so
- * ce_get_error cannot read it: out-of-range targets still show as NaN row
- * losses, but a bounded wait inside a kernel that gave up (CE_DEVERR_TIMEOUT,
- * see ce_wait_timeout_probe) is not reported to the caller of this entry
- * point at all -- the call has returned CE_OK and some loss and gradient rows
- * may be left unwritten.  Callers that need that signal use ce_fwd_bwd with a
- * workspace. */
+ * ce_get_error cannot read it; ce_noalloc_get_error (below) reads it
+ * instead.  Out-of-range targets also show as NaN row losses; a bounded wait
+ * inside a kernel that gave up (CE_DEVERR_TIMEOUT, see ce_wait_timeout_probe)
+ * shows only there: the call has already returned CE_OK, and some loss and
+ * gradient rows may be left unwritten. */
 ce_status ce_fwd_bwd_noalloc(void* logits, ce_dtype dtype, ce_layout layout, int64_t dim0,
                              int64_t dim1, int64_t V, const int64_t strides[3],
                              const int64_t* targets, const int64_t target_strides[2],
                              float label_smoothing, int64_t ignore_idx, int reduce_loss,
                              const float* dloss, float* loss_out, void* grad_inplace,
                              int64_t* n_non_ignore_out, const ce_options* opts, void* stream);
+
+/* ce_get_error for ce_fwd_bwd_noalloc: waits for `stream`, then copies the
+ * error word of the last no-alloc pass on the current device (the one its
+ * fixed scratch array holds) into *host_err (host pointer) and decodes it as
+ * ce_get_error does.  Serialise it with the no-alloc passes like they are
+ * serialised with each other: a pass enqueued on another stream meanwhile
+ * rewrites the word.  Returns CE_ERR_INVALID_ARG if host_err is NULL,
+ * CE_ERR_LAUNCH if the scratch's address cannot be looked up or the copy
+ * fails. */
+ce_status ce_noalloc_get_error(void* stream, uint32_t* host_err);
 
 /* Waits for `stream`, then copies the device error word of the last pass that
  * used `workspace` into *host_err (host pointer).  Returns CE_OK,

@@ -106,3 +106,24 @@ def test_noalloc_python_binding():
     ref = pkg.ce_fwd_bwd(xa, t, label_smoothing=w.label_smoothing, reduce_loss=True)
     pkg.ce_fwd_bwd_noalloc(x, t, loss, label_smoothing=w.label_smoothing, reduce_loss=True)
     assert torch.equal(loss, ref) and torch.equal(x, xa)
+
+
+@pytest.mark.gpu
+def test_noalloc_error_word():
+    """Out-of-range targets set the error word of the library's own scratch,
+    which ce_noalloc_get_error reads; the next clean pass clears it."""
+    import vocabulary_cross_entropy_pass_gb300 as pkg
+    w = wl.Workload("oor_noalloc", 1, 6, 8192, "bf16", sigma=2.0, ignore_frac=0.0, seed=73)
+    dev = torch.device("cuda")
+    t = wl.targets(w)
+    t[0, 2] = 8192
+    t[0, 4] = -7
+    x = wl.logits(w).to(dev)
+    loss = torch.empty(6, dtype=torch.float32, device=dev)
+    pkg.ce_fwd_bwd_noalloc(x, t.to(dev), loss, reduce_loss=False)
+    st, err = pkg.ce_noalloc_get_error()
+    assert err & 1 and st == 6
+    lc = loss.cpu()
+    assert torch.isnan(lc[2]) and torch.isnan(lc[4]) and torch.isfinite(lc[[0, 1, 3, 5]]).all()
+    pkg.ce_fwd_bwd_noalloc(wl.logits(w).to(dev), wl.targets(w).to(dev), loss, reduce_loss=False)
+    assert pkg.ce_noalloc_get_error() == (0, 0)

@@ -8,7 +8,7 @@ entry points keep the C names:
   ce_fwd_only(logits, targets, ...)  loss (and optionally lse); logits kept
   ce_bwd(logits, targets, lse, ...)  gradient from a saved lse
   ce_workspace_bytes(...), ce_get_error(...), ce_status_string(...),
-  ce_plan_path(...), ce_fwd_bwd_noalloc(...)
+  ce_plan_path(...), ce_fwd_bwd_noalloc(...), ce_noalloc_get_error(...)
 
 whose arguments follow the TENPU "Parallel Cross Entropy (Triton)" interface
 (Ascend/TransformerEngineNPU issue #29, section 1), and
@@ -31,7 +31,8 @@ from ._lib import (CE_PATH_AUTO, CE_PATH_CLUSTER, CE_PATH_ROW, CE_PATH_STREAM,
 
 __all__ = ["ce_fwd_bwd", "ce_fwd_bwd_noalloc", "ce_fwd_only", "ce_bwd", "parallel_cross_entropy",
            "ce_vp_partials", "ce_vp_combine", "ce_vp_bwd", "vocab_parallel_cross_entropy",
-           "ce_linear_fwd_bwd", "ce_workspace_bytes", "ce_get_error", "ce_status_string",
+           "ce_linear_fwd_bwd", "ce_workspace_bytes", "ce_get_error", "ce_noalloc_get_error",
+           "ce_status_string",
            "ce_wait_timeout_probe",
            "ce_plan_path", "CEError", "make_options", "ce_options",
            "CE_PATH_AUTO", "CE_PATH_ROW", "CE_PATH_CLUSTER", "CE_PATH_TWO_STAGE", "CE_PATH_STREAM",
@@ -225,6 +226,17 @@ def ce_get_error(workspace: torch.Tensor, stream=None) -> tuple[int, int]:
     err = ctypes.c_uint32(0)
     rc = lib.ce_get_error(ctypes.c_void_p(workspace.data_ptr()), _stream(workspace.device, stream),
                           ctypes.byref(err))
+    return int(rc), int(err.value)
+
+
+def ce_noalloc_get_error(device=None, stream=None) -> tuple[int, int]:
+    """(status, device error word) of the last ce_fwd_bwd_noalloc pass on
+    ``device`` (default: the current CUDA device); waits for the stream."""
+    lib = _lib.load()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    err = ctypes.c_uint32(0)
+    with torch.cuda.device(dev):
+        rc = lib.ce_noalloc_get_error(_stream(dev, stream), ctypes.byref(err))
     return int(rc), int(err.value)
 
 

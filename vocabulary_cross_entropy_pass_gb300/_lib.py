@@ -35,7 +35,8 @@ STATUS = {
 # every function include/ce.h declares
 EXPORTS = ("ce_workspace_bytes", "ce_fwd_bwd", "ce_fwd_only", "ce_get_error", "ce_status_string",
            "ce_plan_path", "ce_fwd_bwd_noalloc", "ce_bwd", "ce_vp_partials", "ce_vp_combine",
-           "ce_vp_bwd", "ce_linear_workspace_bytes", "ce_linear_fwd_bwd", "ce_wait_timeout_probe")
+           "ce_vp_bwd", "ce_linear_workspace_bytes", "ce_linear_fwd_bwd", "ce_wait_timeout_probe",
+           "ce_noalloc_get_error")
 
 
 class ce_options(ctypes.Structure):
@@ -110,6 +111,8 @@ def load(path: str = LIB_PATH):
         lib.ce_wait_timeout_probe.argtypes = [vp, ctypes.c_size_t, vp]
         lib.ce_get_error.restype = i32
         lib.ce_get_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
+        lib.ce_noalloc_get_error.restype = i32
+        lib.ce_noalloc_get_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
         lib.ce_status_string.restype = ctypes.c_char_p
         lib.ce_status_string.argtypes = [i32]
         lib.ce_plan_path.restype = i32

@@ -782,3 +782,11 @@ extern "C" ce_status ce_fwd_bwd_noalloc(void* logits, ce_dtype dtype, ce_layout 
     return run_pass(pb, opts, loss_out, n_non_ignore_out, scratch,
                     static_cast<cudaStream_t>(stream));
 }
+
+extern "C" ce_status ce_noalloc_get_error(void* stream, uint32_t* host_err) {
+    if (!host_err) return CE_ERR_INVALID_ARG;
+    void* scratch = nullptr;
+    const ce_status st = gbce::noalloc_scratch(&scratch);
+    if (st != CE_OK) return st;
+    return ce_get_error(scratch, stream, host_err);
+}
