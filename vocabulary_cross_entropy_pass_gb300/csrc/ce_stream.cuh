@@ -575,19 +575,28 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
     }
 
     // ------------------------------------------------------------ consumer warps
-    // the count kernel before this one may still run: wait for n and the
-    // error word (the producer's first copies are already in flight)
-    griddep_wait();
-    // the mean divides by the number of kept rows, or (weighted) by their
-    // summed target weight
-    float g_reduce = 1.f;
-    if (p.reduce)
-        g_reduce = (p.dloss ? __ldg(p.dloss) : 1.f) / (WT ? (float)(*p.wdenom) : (float)(*p.n_dev));
-    const float wsum = WT ? (float)(*p.wsum) : 0.f;
+    // The count kernel before this one may still run.  A thread waits for it
+    // (griddepcontrol.wait) only where it first needs its results: the
+    // gradient scale and the weight sum (after the first row's statistics
+    // pass), the error word it starts, the row counters and the mean.  The
+    // mean divides by the number of kept rows, or (weighted) by their summed
+    // target weight.
+    bool counted = false;
+    float g_reduce = 1.f, wsum = 0.f;
+    auto need_count = [&]() {
+        if (!counted) {
+            griddep_wait();
+            if (p.reduce)
+                g_reduce = (p.dloss ? __ldg(p.dloss) : 1.f) / (WT ? (float)(*p.wdenom) : (float)(*p.n_dev));
+            if (WT) wsum = (float)(*p.wsum);
+            counted = true;
+        }
+    };
     Ring rg(p.stages);
     int par = 0;
     auto wait_full = [&]() {
         if (!*abort_flag && !mbar_wait_bounded(&full[rg.s], rg.ph)) {
+            need_count();
             atomicOr(p.err, CE_DEVERR_TIMEOUT);
             *abort_flag = 1;
         }
@@ -616,6 +625,7 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&qempty[qr.s]);
             } else {
+                need_count();
                 atomicOr(p.err, CE_DEVERR_TIMEOUT);
                 *abort_flag = 1;
             }
@@ -652,7 +662,6 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
             y = ny;
             continue;
         }
-        const float g = p.reduce ? g_reduce : (p.dloss ? __ldg(p.dloss + r) : 1.f);
         const int64_t ybyte = y * ES;
         // the tile holding the target and the target's byte in that tile (-1:
         // the target is a head or tail element, outside the ring)
@@ -757,6 +766,8 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
                 G = part_combine(G, Part{v4.x, v4.y, v4.z});
             }
         }
+        need_count();
+        const float g = p.reduce ? g_reduce : (p.dloss ? __ldg(p.dloss + r) : 1.f);
         const float lse = G.m + logf(G.d);
         const float xy = xy_s[par];
         const float wy = WT ? __ldg(p.cw + y) : 1.f;
@@ -864,6 +875,7 @@ ce_stream_kernel(const __grid_constant__ StreamArgs p) {
         y = ny;
     }
 
+    need_count();
     // the last CTA done claiming rows zeroes the row counter for the next pass
     // (its rows were all claimed before the end mark this CTA has read)
     if (p.row_claim && tid == 0) {
