@@ -187,6 +187,14 @@ def test_overlapping_rows_rejected_for_in_place_gradient(lib):
     assert _call(lib, d0=2, d1=3, strides=(4096, 2 * 4096, 1)) not in (1, 2, 3, 4)
 
 
+def test_error_getters_reject_null_pointers(lib):
+    # no CUDA call is made before these checks
+    err = ctypes.c_uint32(0)
+    assert lib.ce_get_error(None, None, ctypes.byref(err)) == 1
+    assert lib.ce_get_error(ctypes.c_void_p(0x1000), None, None) == 1
+    assert lib.ce_noalloc_get_error(None, None) == 1
+
+
 def test_bwd_host_validation(lib):
     def call(**kw):
         a = dict(logits=0x1000, dtype=1, d0=2, d1=3, V=4096, st=(3 * 4096, 4096, 1), tgt=0x2000,
